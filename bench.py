@@ -1,0 +1,440 @@
+#!/usr/bin/env python3
+"""Throughput benchmark: one step = forward + backward of the packed width-4
+causal depthwise Conv1d + SiLU on the GDP conv-channel workload
+(C = 7168 = V 2048*2 + K 8*128*2 + Q 1024, rows 65536 holding 200
+lognormal-length sequences, weight BF16, bias FP32), through the C ABI.
+
+Prints one JSON line (rank 0).  ``value`` is valid tokens per second of the
+whole job (all ranks; each rank is an independent replica on its own GPU),
+timed with CUDA events on the launch stream over K steps after W warm-up
+steps, inputs resident in HBM.  ``e2e`` is the same metric with the inputs
+copied from pinned host memory and the results copied back inside every
+step.  ``roofline`` is for the backward call (the dominant kernel),
+``cpu_baseline`` times the float64 oracle on a bounded sample of the same
+workload on this host's cores.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "fwd+bwd tokens/s and effective HBM GB/s (% of ~8 TB/s) at C=7168 packed"
+UNIT = "tokens/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------ setup --
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws, backend):
+    if ws > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+        return dist
+    return None
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def algorithmic_bytes(wl):
+    """Bytes the method must move (no halo re-reads, chunk map or partials).
+
+    Forward: x read + out written for valid tokens of live sequences (-1
+    sequences write zeros and read nothing), weights, bias, and 3 state rows
+    read / written per sequence with a pool.  Backward: x, dy read and dx
+    written per valid token, saved history read, weights, bias, dweight and
+    dbias written."""
+    T, C = wl.valid_tokens, wl.C
+    wsz = wl.weight.element_size()
+    bsz = 0 if wl.bias is None else wl.bias.element_size()
+    lens = wl.lengths
+    if wl.cache_indices is not None:
+        live = wl.cache_indices.cpu().numpy() != -1
+    else:
+        live = np.ones(len(lens), dtype=bool)
+    T_live = int(lens[live].sum())
+    fwd = T_live * C * 2 + T * C * 2 + C * 4 * wsz + C * bsz
+    if wl.conv_state is not None:
+        hi = wl.has_initial_state.cpu().numpy() if wl.has_initial_state is not None else np.zeros(len(lens), bool)
+        fwd += int((live & hi & (lens > 0)).sum()) * 3 * C * 2 + int((live & (lens > 0)).sum()) * 3 * C * 2
+    bwd = T_live * C * 4 + T * C * 2 + C * 4 * wsz + C * bsz + C * 5 * 4
+    return fwd, bwd
+
+
+# ----------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"ccc_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        try:
+            os.unlink(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, flags in rows for i, f in enumerate(flags) if f.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- traffic --
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "ssm_depthwise_causal_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()
+
+
+def recorded_traffic():
+    """DRAM bytes per backward launch from the committed ncu summary, or None
+    when the kernel sources changed since it was captured."""
+    p = os.path.join(ROOT, "profiles", "bwd_packed_traffic.json")
+    try:
+        rec = json.load(open(p))
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_sha256") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------- cpu oracle --
+
+def oracle_sample(wl, chans):
+    x = wl.x[:, :chans].contiguous().cpu()
+    dy = wl.dy[:, :chans].contiguous().cpu()
+    w = wl.weight[:chans].cpu()
+    b = None if wl.bias is None else wl.bias[:chans].cpu()
+    return x, dy, w, b, wl.cu_seqlens.cpu()
+
+
+def time_oracle(wl, target_s=12.0, max_chans=None):
+    import oracle
+    oracle.build()
+    C = wl.C
+    chans = 8
+    x, dy, w, b, cu = oracle_sample(wl, chans)
+    t0 = time.perf_counter()
+    _, _, hist = oracle.fwd(x, w, b, cu)
+    oracle.bwd(x, w, b, cu, dy, hist)
+    dt = time.perf_counter() - t0
+    # grow the sample to about target_s of CPU work
+    chans = int(min(C if max_chans is None else max_chans, max(8, chans * target_s / max(dt, 1e-3))))
+    chans = max(8, chans - chans % 8)
+    x, dy, w, b, cu = oracle_sample(wl, chans)
+    t0 = time.perf_counter()
+    _, _, hist = oracle.fwd(x, w, b, cu)
+    oracle.bwd(x, w, b, cu, dy, hist)
+    dt = time.perf_counter() - t0
+    tok_s = wl.valid_tokens * (chans / C) / dt
+    sample = (f"all {wl.valid_tokens} valid tokens of the workload, first {chans} of {C} channels "
+              f"(fwd+bwd, {dt:.2f} s); tokens/s scaled by {chans}/{C}")
+    return tok_s, oracle.threads(), sample, dt
+
+
+# ------------------------------------------------------------------ runs --
+
+def run_reference(args, ws, rank):
+    from ssm_depthwise_causal_gb300 import workloads
+    if rank != 0:
+        return
+    wl = workloads.packed(device="cpu")
+    vals = []
+    threads, sample = 0, ""
+    for _ in range(args.warmup):
+        time_oracle(wl, target_s=2.0)
+    for _ in range(args.steps):
+        v, threads, sample, _ = time_oracle(wl, target_s=args.ref_seconds)
+        vals.append(v)
+    v = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wl.valid_tokens / v,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "packed C=7168 rows=65536 N=200 lognormal lengths, fwd+bwd",
+                   "rows": wl.rows, "C": wl.C, "n_seqs": wl.n_seqs, "valid_tokens": wl.valid_tokens},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, ws, rank, local):
+    import ssm_depthwise_causal_gb300 as ccc
+    from ssm_depthwise_causal_gb300 import workloads
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = init_dist(ws, "nccl")
+    ccc._lib.lib()  # fail loudly if the library is missing
+
+    wl = workloads.packed(device=dev)
+    T, C, N, rows = wl.valid_tokens, wl.C, wl.n_seqs, wl.rows
+    out = torch.empty_like(wl.x)
+    dx = torch.empty_like(wl.x)
+    hist = torch.empty((N, 3, C), dtype=torch.bfloat16, device=dev)
+    dw = torch.empty((C, 4), dtype=torch.float32, device=dev)
+    db = torch.empty((C,), dtype=torch.float32, device=dev)
+    ws_f = torch.empty(max(1, ccc.ccc_workspace_size(rows, N, C, False)), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(ccc.ccc_workspace_size(rows, N, C, True), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    launches = {"n": 0}
+
+    def step(x, dy, s):
+        ccc.ccc_fwd(x, wl.weight, wl.bias, None, wl.cu_seqlens, None, None, out, hist, ws_f, stream=s)
+        launches["n"] += ccc.last_launch_count()
+        ccc.ccc_bwd(x, wl.weight, wl.bias, hist, wl.cu_seqlens, None, None, dy, None, dx, dw, db, None,
+                    ws_b, stream=s)
+        launches["n"] += ccc.last_launch_count()
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step(wl.x, wl.dy, stream)
+    torch.cuda.synchronize()
+
+    # ---- device-resident timing
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    launches["n"] = 0
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for k in range(K):
+            ev[k][0].record(stream)
+            ccc.ccc_fwd(wl.x, wl.weight, wl.bias, None, wl.cu_seqlens, None, None, out, hist, ws_f, stream=stream)
+            launches["n"] += ccc.last_launch_count()
+            ev[k][1].record(stream)
+            ccc.ccc_bwd(wl.x, wl.weight, wl.bias, hist, wl.cu_seqlens, None, None, wl.dy, None, dx, dw, db,
+                        None, ws_b, stream=stream)
+            launches["n"] += ccc.last_launch_count()
+            ev[k][2].record(stream)
+        t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if dist:
+        dist.barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if dist:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    gpu_launches = launches["n"]
+    fwd_ms = statistics.mean(ev[k][0].elapsed_time(ev[k][1]) for k in range(K))
+    bwd_ms = statistics.mean(ev[k][1].elapsed_time(ev[k][2]) for k in range(K))
+    ms_step = elapsed_ms / K
+    value = ws * T / (ms_step / 1e3)
+    fb, bb = algorithmic_bytes(wl)
+    peak, peak_kind = measured_peak()
+    eff_gbs = (fb + bb) / (ms_step / 1e3) / 1e9
+    bwd_gbs = bb / (bwd_ms / 1e3) / 1e9
+
+    # ---- end to end: pinned host inputs in, results out, every step
+    hx = torch.empty(wl.x.shape, dtype=wl.x.dtype, pin_memory=True)
+    hdy = torch.empty(wl.dy.shape, dtype=wl.dy.dtype, pin_memory=True)
+    hx.copy_(wl.x)
+    hdy.copy_(wl.dy)
+    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    hdx = torch.empty(dx.shape, dtype=dx.dtype, pin_memory=True)
+    hdw = torch.empty(dw.shape, dtype=dw.dtype, pin_memory=True)
+    hdb = torch.empty(db.shape, dtype=db.dtype, pin_memory=True)
+    dxin = torch.empty_like(wl.x)
+    ddyin = torch.empty_like(wl.dy)
+    h2d = hx.numel() * 2 + hdy.numel() * 2
+    d2h = hout.numel() * 2 + hdx.numel() * 2 + hdw.numel() * 4 + hdb.numel() * 4
+    e2e_steps = max(1, min(K, 5))
+
+    def e2e_step():
+        dxin.copy_(hx, non_blocking=True)
+        ddyin.copy_(hdy, non_blocking=True)
+        step(dxin, ddyin, stream)
+        hout.copy_(out, non_blocking=True)
+        hdx.copy_(dx, non_blocking=True)
+        hdw.copy_(dw, non_blocking=True)
+        hdb.copy_(db, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_val = ws * T / (e2e_ms / 1e3)
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        tok_s, threads, sample, _ = time_oracle(wl, target_s=args.ref_seconds)
+        cpu = {"value": tok_s, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "storage_dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "packed C=7168 rows=65536 N=200 lognormal lengths, fwd+bwd",
+                       "rows": rows, "C": C, "n_seqs": N, "valid_tokens": T,
+                       "weight": "bf16", "bias": "f32", "state": "none",
+                       "l2": "inputs larger than L2 (x, dy, out, dx 939 MB each)",
+                       "parallelism": f"replicas x{ws}"},
+            "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+            "fwd_tokens_per_s": ws * T / (fwd_ms / 1e3),
+            "effective_gbs": eff_gbs, "frac_of_nominal_8tbs": eff_gbs / NOMINAL_HBM_GBS,
+            "frac_of_measured_hbm": eff_gbs / peak,
+            "roofline": {"kernel": "ccc_bwd call (chunk map + fused backward + ordered reduce)",
+                         "bound": "hbm", "achieved": bwd_gbs, "peak": peak, "peak_kind": peak_kind,
+                         "unit": "GB/s", "frac": bwd_gbs / peak, "traffic": recorded_traffic(),
+                         "algorithmic_bytes_per_launch": bb},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms, "steps": e2e_steps},
+            "gpu_launches": gpu_launches,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_profile(args, local):
+    """W warm-up steps then one step of the same calls, nothing else: the
+    command the ncu captures run."""
+    import ssm_depthwise_causal_gb300 as ccc
+    from ssm_depthwise_causal_gb300 import workloads
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = workloads.WORKLOADS[args.workload](device=dev)
+    T, C, N, rows = wl.valid_tokens, wl.C, wl.n_seqs, wl.rows
+    out = torch.empty_like(wl.x)
+    hist = torch.empty((N, 3, C), dtype=torch.bfloat16, device=dev)
+    ws_f = torch.empty(max(1, ccc.ccc_workspace_size(rows, N, C, False)), dtype=torch.uint8, device=dev)
+    state = None if wl.conv_state is None else wl.conv_state.clone()
+    if wl.training:
+        dx = torch.empty_like(wl.x)
+        dw = torch.empty((C, 4), dtype=torch.float32, device=dev)
+        db = None if wl.bias is None else torch.empty((C,), dtype=torch.float32, device=dev)
+        ws_b = torch.empty(ccc.ccc_workspace_size(rows, N, C, True), dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup + 1):
+        ccc.ccc_fwd(wl.x, wl.weight, wl.bias, state, wl.cu_seqlens, wl.cache_indices,
+                    wl.has_initial_state, out, hist, ws_f)
+        if wl.training:
+            ccc.ccc_bwd(wl.x, wl.weight, wl.bias, hist, wl.cu_seqlens, wl.cache_indices,
+                        wl.has_initial_state, wl.dy, None, dx, dw, db, None, ws_b)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": wl.name, "valid_tokens": T}), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--ref-seconds", type=float, default=12.0,
+                    help="approximate CPU seconds of one oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="run warm-up + one step of --workload only (for ncu captures)")
+    ap.add_argument("--workload", default="packed", choices=["tiny", "dense", "packed", "serving", "long"])
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    ws, rank, local = dist_env()
+    if args.profile:
+        run_profile(args, local)
+    elif args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_ours(args, ws, rank, local)
+
+
+if __name__ == "__main__":
+    main()

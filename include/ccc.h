@@ -1,0 +1,178 @@
+/*
+ * ccc.h -- C ABI of the GB300 (sm_103a) packed, width-4, depthwise causal
+ * Conv1d + SiLU ("ccc"): forward with in-place conv_state pool update, and
+ * the fused backward with a deterministic FP32 weight/bias gradient.
+ *
+ * The operation (FlashInfer "flashinfer.mamba.causal_conv1d_fn", Parameters
+ * and Notes): sequence n owns the packed rows [cu_seqlens[n], cu_seqlens[n+1])
+ * of x.  Its history h is three initial values followed by its raw inputs;
+ * the initial values are conv_state positions 0:3 of slot cache_indices[n]
+ * when has_initial_state[n] is true, zeros otherwise.  For token j and
+ * channel c, with FP32 accumulation,
+ *
+ *     z = bias[c] + w[c][0]*h[j] + w[c][1]*h[j+1] + w[c][2]*h[j+2] + w[c][3]*h[j+3]
+ *     out[j][c] = BF16_rne( z * sigmoid(z) )
+ *
+ * (tap 3 multiplies the current token; the bias is added before the four
+ * FMAs, which run in the order k = 0, 1, 2, 3).  cache_indices[n] == -1
+ * produces a zero output and no state access.  Each nonempty live sequence
+ * writes its final three raw history values to its slot's positions 0:3
+ * (position 0 = oldest); nothing else in the pool changes.  Rows after
+ * cu_seqlens[N] are never written.
+ *
+ * The backward (FlashInfer "cake_causal_conv1d_train.cake_causal_conv1d_kcp",
+ * Returns: fused dx + deterministic FP32 dweight) recomputes z, forms
+ * dz = dy * s * (1 + z * (1 - s)) with s = sigmoid(z), and gives
+ *
+ *     dH[i] = carry + w[c][0]*dz[i] + w[c][1]*dz[i-1] + w[c][2]*dz[i-2] + w[c][3]*dz[i-3]
+ *
+ * for every history index i (terms with an index outside the sequence are
+ * absent; carry = d_final_state[n][i-len] for the three indices past the end,
+ * else 0), dx = dH for the input rows, d_init_state = dH for the three initial
+ * values, and dweight[c][k] = sum of dz[j]*h[j+k], dbias[c] = sum of dz[j]
+ * over all live tokens.  The weight/bias sums use per-block FP32 partials in
+ * workspace combined by an ordered reduction, never atomics (Megatron-Core
+ * "core.ssm.causal_conv1d", assert_causal_conv1d_deterministic), so repeated
+ * calls with the same arguments match bit for bit.
+ *
+ * Conventions for every entry point:
+ *  - The caller owns every buffer.  The library allocates nothing, keeps no
+ *    state between calls, never synchronizes the host and never reads device
+ *    values on the host (Notes of causal_conv1d_fn: graph-capturable).  Work is
+ *    enqueued on `cuda_stream` (a cudaStream_t; NULL = legacy default stream).
+ *  - Device pointers are marked [dev]; sizes are in elements unless stated.
+ *  - BF16 tensors are raw IEEE bfloat16 (uint16 storage).
+ *  - All checks are host-side.  A failed check returns a negative ccc_status
+ *    and enqueues nothing.  Device-side values (offsets, slot IDs, flags) are
+ *    caller-owned constraints: if invalid, the results are undefined, but
+ *    the kernels clamp offsets to [0, rows] and skip slot IDs outside
+ *    [0, n_slots), so they do not access memory outside the buffers given.
+ *  - rows == 0 or N == 0 returns CCC_OK (the backward still zeroes dweight /
+ *    dbias).
+ *  - Concurrent calls on different streams need disjoint live slots, outputs
+ *    and workspaces.
+ */
+#ifndef CCC_H_
+#define CCC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { CCC_F32 = 0, CCC_BF16 = 1, CCC_NONE = -1 } ccc_dtype;
+
+typedef enum {
+    CCC_OK = 0,
+    CCC_ERR_NULL = -1,      /* a required pointer is NULL */
+    CCC_ERR_SHAPE = -2,     /* a size or stride is invalid (C % 8, state_len < 3, ...) */
+    CCC_ERR_DTYPE = -3,     /* unknown dtype code, or a dtype code without its buffer */
+    CCC_ERR_ALIGN = -4,     /* x/out/dy/dx/saved_hist not 16-byte aligned, or misaligned element pointers */
+    CCC_ERR_WORKSPACE = -5, /* workspace NULL or smaller than ccc_workspace_size() */
+    CCC_ERR_ALIAS = -6,     /* an output overlaps another operand */
+    CCC_ERR_CUDA = -7       /* a CUDA launch failed (cudaGetLastError after launch) */
+} ccc_status;
+
+/*
+ * Bytes of device scratch ("workspace") that ccc_fwd (for_bwd = 0) or ccc_bwd
+ * (for_bwd != 0) needs for `rows` packed rows, `n_seqs` sequences and
+ * `channels` channels.  Pure host arithmetic; no CUDA call.
+ *
+ * Forward: 0 for n_seqs <= 32 (the work items are derived in-kernel), else
+ * the device chunk map (causal_conv1d_fn, workspace: rebuilt on every call).
+ * Backward: the chunk map when n_seqs > 32, plus the FP32 partial sums of the
+ * ordered weight/bias reduction.  The value depends only on the three sizes,
+ * so a workspace sized for the largest shape can be reused (and captured in
+ * a CUDA graph).  Returns 0 for invalid sizes.
+ */
+size_t ccc_workspace_size(int64_t rows, int32_t n_seqs, int32_t channels, int32_t for_bwd);
+
+/*
+ * Forward (causal_conv1d_fn).
+ *
+ *  x            [dev] BF16 [rows][x_row_stride], channels contiguous; 16-byte
+ *               aligned; x_row_stride >= C, a multiple of 8.  Rows after
+ *               cu_seqlens[N] may be padding.
+ *  rows, C      C > 0 and a multiple of 8 (cake_causal_conv1d_kcp, x_local).
+ *  weight       [dev] [C][4] contiguous, w_dtype CCC_F32 or CCC_BF16.
+ *  bias         [dev] [C] with b_dtype CCC_F32/CCC_BF16, or NULL with
+ *               b_dtype CCC_NONE.
+ *  conv_state   [dev] BF16 pool, in place, or NULL (zero history, no
+ *               write-back).  Element (slot, c, l) is at
+ *               st_slot*slot + st_c*c + st_l*l; st_c == 1 or st_l == 1; slots
+ *               must not overlap; state_len >= 3; n_slots >= 1.
+ *  cu_seqlens   [dev] int32 [N+1]: 0, nondecreasing, cu_seqlens[N] <= rows.
+ *  cache_indices[dev] int32 [N] slot per sequence, -1 = zero output and no
+ *               state access.  Required with a pool; optional without (then
+ *               only the -1 rule applies).  Live slots unique, in [0, n_slots).
+ *  has_initial_state [dev] uint8/bool [N] or NULL (= all false).
+ *  out          [dev] BF16 [rows][out_row_stride], 16-byte aligned, must not
+ *               overlap any operand.  Rows after cu_seqlens[N] are not written.
+ *  saved_hist   [dev] BF16 [N][3][C] or NULL.  When given, every nonempty
+ *               sequence's initial history (what the forward read before it
+ *               overwrote the slot; zeros for a -1 request) is stored, for
+ *               ccc_bwd.  Rows of empty sequences are not written.
+ *  workspace    [dev] >= ccc_workspace_size(rows, N, C, 0) bytes, 256-byte
+ *               aligned (NULL allowed when that size is 0).
+ */
+int ccc_fwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
+            const void *weight, int32_t w_dtype, const void *bias, int32_t b_dtype,
+            void *conv_state, int32_t n_slots, int32_t state_len,
+            int64_t st_slot, int64_t st_c, int64_t st_l,
+            const int32_t *cu_seqlens, int32_t N,
+            const int32_t *cache_indices, const uint8_t *has_initial_state,
+            void *out, int64_t out_row_stride,
+            void *saved_hist,
+            void *workspace, size_t workspace_bytes, void *cuda_stream);
+
+/*
+ * Backward (cake_causal_conv1d_kcp, Returns: fused dx + deterministic FP32
+ * dweight; core.ssm.causal_conv1d, _exchange_initial_states: the state
+ * gradient is what a preceding fragment receives).
+ *
+ *  x, rows, C, x_row_stride, weight, w_dtype, bias, b_dtype: as in ccc_fwd
+ *               (the same values the forward saw).
+ *  saved_hist   [dev] BF16 [N][3][C] from ccc_fwd, or NULL (zero history).
+ *  cu_seqlens, N, cache_indices (NULL = all live), has_initial_state (NULL =
+ *               all false): as in ccc_fwd.
+ *  dy           [dev] BF16 [rows][dy_row_stride], gradient of out; rows after
+ *               cu_seqlens[N] are ignored.
+ *  d_final_state[dev] FP32 [N][3][C] or NULL: gradient of the three state
+ *               values the forward wrote (position order), e.g. the
+ *               d_init_state of the fragment that continued this one.
+ *  dx           [dev] BF16 [rows][dx_row_stride]; rows after cu_seqlens[N] are
+ *               not written; zero for -1 requests.
+ *  dweight      [dev] FP32 [C][4], overwritten (not accumulated).
+ *  dbias        [dev] FP32 [C] or NULL, overwritten.
+ *  d_init_state [dev] FP32 [N][3][C] or NULL: gradient of the initial history
+ *               for sequences that read their state (has_initial_state true,
+ *               live, nonempty); 0 for every other sequence.
+ *  workspace    [dev] >= ccc_workspace_size(rows, N, C, 1) bytes, 256-byte
+ *               aligned.
+ * Every buffer written must not overlap any other operand.
+ */
+int ccc_bwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
+            const void *weight, int32_t w_dtype, const void *bias, int32_t b_dtype,
+            const void *saved_hist,
+            const int32_t *cu_seqlens, int32_t N,
+            const int32_t *cache_indices, const uint8_t *has_initial_state,
+            const void *dy, int64_t dy_row_stride,
+            const float *d_final_state,
+            void *dx, int64_t dx_row_stride,
+            float *dweight, float *dbias, float *d_init_state,
+            void *workspace, size_t workspace_bytes, void *cuda_stream);
+
+/* Name of a ccc_status value ("CCC_OK", ...); "unknown" otherwise. */
+const char *ccc_status_string(int status);
+
+/* Number of kernel launches the last successful ccc_fwd / ccc_bwd on this
+ * host thread enqueued (for launch accounting; memsets not included). */
+int ccc_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CCC_H_ */

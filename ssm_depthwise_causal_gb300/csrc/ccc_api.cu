@@ -1,0 +1,317 @@
+// ccc_api.cu -- the C ABI declared in include/ccc.h: host-side argument
+// checks, workspace carve-up and kernel launches.  No device value is read on
+// the host and nothing synchronizes (FlashInfer
+// "flashinfer.mamba.causal_conv1d_fn", Notes), so every call can be captured
+// in a CUDA graph once out and workspace are supplied.
+#include <algorithm>
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "ccc.h"
+#include "ccc_internal.h"
+
+namespace {
+
+using ccc::ceil_div;
+
+thread_local int g_last_launches = 0;
+
+constexpr size_t kAlignWs = 256;
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Byte span [lo, hi) of a buffer, or empty.
+struct Span {
+    uintptr_t lo = 0, hi = 0;
+    bool empty() const { return hi <= lo; }
+};
+
+Span span(const void *p, size_t bytes) {
+    Span s;
+    if (p && bytes) {
+        s.lo = reinterpret_cast<uintptr_t>(p);
+        s.hi = s.lo + bytes;
+    }
+    return s;
+}
+
+bool overlap(const Span &a, const Span &b) {
+    return !a.empty() && !b.empty() && a.lo < b.hi && b.lo < a.hi;
+}
+
+// Rows of a [rows][stride] BF16 matrix with C used columns, in bytes.
+size_t mat_bytes(int64_t rows, int64_t stride, int C) {
+    return rows > 0 ? static_cast<size_t>(((rows - 1) * stride + C) * 2) : 0;
+}
+
+size_t map_bytes(int64_t rows, int N, int B) {
+    if (N <= ccc::kMaxInlineSeqs || rows <= 0) return 0;
+    const int64_t cap = ccc::item_capacity(rows, N, B);
+    return round_up(static_cast<size_t>(1 + 2 * cap) * sizeof(int32_t), kAlignWs);
+}
+
+int dtype_size(int code) { return code == CCC_F32 ? 4 : (code == CCC_BF16 ? 2 : 0); }
+
+// Pool layout check: strides non-negative, channel or history axis
+// contiguous, and distinct (slot, c, l) never share an element (sorted-stride
+// criterion: each stride exceeds the span of the smaller dimensions).
+bool state_layout_ok(int n_slots, int C, int L, int64_t s_slot, int64_t s_c, int64_t s_l) {
+    if (s_slot < 0 || s_c < 0 || s_l < 0) return false;
+    if (s_c != 1 && s_l != 1) return false;
+    struct D { int64_t stride, extent; } d[3] = {{s_slot, n_slots}, {s_c, C}, {s_l, L}};
+    std::sort(d, d + 3, [](const D &a, const D &b) { return a.stride < b.stride; });
+    int64_t span_below = 0;
+    for (const D &e : d) {
+        if (e.extent > 1 && e.stride <= span_below) return false;
+        span_below += (e.extent - 1) * e.stride;
+    }
+    return true;
+}
+
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 152;
+    if (dev < 64 && cached[dev]) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+    if (dev < 64) cached[dev] = n;
+    return n;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ccc_workspace_size(int64_t rows, int32_t n_seqs, int32_t channels, int32_t for_bwd) {
+    if (rows < 0 || n_seqs < 0 || channels <= 0 || channels % 8) return 0;
+    if (rows == 0 || n_seqs == 0) return 0;
+    if (!for_bwd) return map_bytes(rows, n_seqs, ccc::kFwdChunk);
+    const size_t mb = map_bytes(rows, n_seqs, ccc::kBwdChunk);
+    const int G = ccc::bwd_groups(rows, n_seqs, channels);
+    return mb + round_up(static_cast<size_t>(G) * 5 * channels * sizeof(float), kAlignWs);
+}
+
+const char *ccc_status_string(int status) {
+    switch (status) {
+        case CCC_OK: return "CCC_OK";
+        case CCC_ERR_NULL: return "CCC_ERR_NULL";
+        case CCC_ERR_SHAPE: return "CCC_ERR_SHAPE";
+        case CCC_ERR_DTYPE: return "CCC_ERR_DTYPE";
+        case CCC_ERR_ALIGN: return "CCC_ERR_ALIGN";
+        case CCC_ERR_WORKSPACE: return "CCC_ERR_WORKSPACE";
+        case CCC_ERR_ALIAS: return "CCC_ERR_ALIAS";
+        case CCC_ERR_CUDA: return "CCC_ERR_CUDA";
+        default: return "unknown";
+    }
+}
+
+int ccc_last_launch_count(void) { return g_last_launches; }
+
+int ccc_fwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
+            const void *weight, int32_t w_dtype, const void *bias, int32_t b_dtype,
+            void *conv_state, int32_t n_slots, int32_t state_len,
+            int64_t st_slot, int64_t st_c, int64_t st_l,
+            const int32_t *cu_seqlens, int32_t N,
+            const int32_t *cache_indices, const uint8_t *has_initial_state,
+            void *out, int64_t out_row_stride,
+            void *saved_hist,
+            void *workspace, size_t workspace_bytes, void *cuda_stream) {
+    // ---- shapes and dtypes
+    if (rows < 0 || N < 0 || C <= 0 || C % 8 != 0) return CCC_ERR_SHAPE;
+    if (rows > INT32_MAX) return CCC_ERR_SHAPE;  // cu_seqlens is int32
+    if (x_row_stride < C || out_row_stride < C || x_row_stride % 8 || out_row_stride % 8) return CCC_ERR_SHAPE;
+    if (w_dtype != CCC_F32 && w_dtype != CCC_BF16) return CCC_ERR_DTYPE;
+    if (bias ? (b_dtype != CCC_F32 && b_dtype != CCC_BF16) : (b_dtype != CCC_NONE)) return CCC_ERR_DTYPE;
+    if (conv_state) {
+        if (state_len < 3 || n_slots < 1) return CCC_ERR_SHAPE;
+        if (!state_layout_ok(n_slots, C, state_len, st_slot, st_c, st_l)) return CCC_ERR_SHAPE;
+    }
+    // ---- pointers
+    if (!x || !weight || !cu_seqlens || !out) return CCC_ERR_NULL;
+    if (conv_state && !cache_indices) return CCC_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(out, 16) || (saved_hist && !aligned(saved_hist, 16))) return CCC_ERR_ALIGN;
+    if (!aligned(weight, dtype_size(w_dtype)) || (bias && !aligned(bias, dtype_size(b_dtype)))) return CCC_ERR_ALIGN;
+    if ((conv_state && !aligned(conv_state, 2)) || !aligned(cu_seqlens, 4) ||
+        (cache_indices && !aligned(cache_indices, 4)))
+        return CCC_ERR_ALIGN;
+    const size_t ws_need = ccc_workspace_size(rows, N, C, 0);
+    if (ws_need && (!workspace || workspace_bytes < ws_need)) return CCC_ERR_WORKSPACE;
+    if (ws_need && !aligned(workspace, kAlignWs)) return CCC_ERR_ALIGN;
+    // ---- aliasing: every written buffer against every other operand
+    const Span s_x = span(x, mat_bytes(rows, x_row_stride, C));
+    const Span s_out = span(out, mat_bytes(rows, out_row_stride, C));
+    const Span s_w = span(weight, static_cast<size_t>(C) * 4 * dtype_size(w_dtype));
+    const Span s_b = span(bias, bias ? static_cast<size_t>(C) * dtype_size(b_dtype) : 0);
+    Span s_st;
+    if (conv_state) {
+        const int64_t last = (n_slots - 1) * st_slot + (C - 1) * st_c + (state_len - 1) * st_l;
+        s_st = span(conv_state, static_cast<size_t>(last + 1) * 2);
+    }
+    const Span s_cu = span(cu_seqlens, static_cast<size_t>(N + 1) * 4);
+    const Span s_ci = span(cache_indices, static_cast<size_t>(N) * 4);
+    const Span s_hi = span(has_initial_state, static_cast<size_t>(N));
+    const Span s_h = span(saved_hist, static_cast<size_t>(N) * 3 * C * 2);
+    const Span s_ws = span(workspace, ws_need);
+    const Span *all[] = {&s_x, &s_out, &s_w, &s_b, &s_st, &s_cu, &s_ci, &s_hi, &s_h, &s_ws};
+    const Span *written[] = {&s_out, &s_st, &s_h, &s_ws};
+    for (const Span *wsp : written)
+        for (const Span *o : all)
+            if (o != wsp && overlap(*wsp, *o)) return CCC_ERR_ALIAS;
+
+    g_last_launches = 0;
+    if (rows == 0 || N == 0) return CCC_OK;
+
+    cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+    ccc::FwdArgs a = {};
+    a.x = static_cast<const uint16_t *>(x);
+    a.rows = rows;
+    a.C = C;
+    a.xs = x_row_stride;
+    a.w = weight;
+    a.w_bf16 = w_dtype == CCC_BF16;
+    a.b = bias;
+    a.b_kind = bias ? (b_dtype == CCC_F32 ? 1 : 2) : 0;
+    a.state = static_cast<uint16_t *>(conv_state);
+    a.n_slots = n_slots;
+    a.st_slot = st_slot;
+    a.st_c = st_c;
+    a.st_l = st_l;
+    a.state_vec = conv_state && st_c == 1 && st_slot % 8 == 0 && st_l % 8 == 0 && aligned(conv_state, 16);
+    a.cu = cu_seqlens;
+    a.N = N;
+    a.cache = cache_indices;
+    a.has_init = has_initial_state;
+    a.out = static_cast<uint16_t *>(out);
+    a.os = out_row_stride;
+    a.hist = static_cast<uint16_t *>(saved_hist);
+    a.cap = static_cast<int>(std::min<int64_t>(ccc::item_capacity(rows, N, ccc::kFwdChunk), INT32_MAX));
+    a.map = nullptr;
+
+    int launches = 0;
+    bool pdl = false;
+    if (N > ccc::kMaxInlineSeqs) {
+        int32_t *map = static_cast<int32_t *>(workspace);
+        if (ccc::launch_chunkmap(cu_seqlens, N, rows, ccc::kFwdChunk, 0, map, a.cap, st) != cudaSuccess)
+            return CCC_ERR_CUDA;
+        ++launches;
+        a.map = map;
+        pdl = true;
+    }
+    const int64_t slabs = ceil_div(C, 32 * ccc::kFwdVec);
+    const int64_t want = ceil_div(static_cast<int64_t>(sm_count()) * 2 * 2, slabs);  // 2 waves of 2 CTAs/SM
+    const int64_t gy = std::max<int64_t>(1, std::min<int64_t>(want, ceil_div(a.cap, ccc::kWarpsPerCta)));
+    if (ccc::launch_fwd(a, static_cast<int>(gy), pdl, st) != cudaSuccess) return CCC_ERR_CUDA;
+    ++launches;
+    g_last_launches = launches;
+    return CCC_OK;
+}
+
+int ccc_bwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
+            const void *weight, int32_t w_dtype, const void *bias, int32_t b_dtype,
+            const void *saved_hist,
+            const int32_t *cu_seqlens, int32_t N,
+            const int32_t *cache_indices, const uint8_t *has_initial_state,
+            const void *dy, int64_t dy_row_stride,
+            const float *d_final_state,
+            void *dx, int64_t dx_row_stride,
+            float *dweight, float *dbias, float *d_init_state,
+            void *workspace, size_t workspace_bytes, void *cuda_stream) {
+    if (rows < 0 || N < 0 || C <= 0 || C % 8 != 0) return CCC_ERR_SHAPE;
+    if (rows > INT32_MAX) return CCC_ERR_SHAPE;
+    if (x_row_stride < C || dy_row_stride < C || dx_row_stride < C || x_row_stride % 8 || dy_row_stride % 8 ||
+        dx_row_stride % 8)
+        return CCC_ERR_SHAPE;
+    if (w_dtype != CCC_F32 && w_dtype != CCC_BF16) return CCC_ERR_DTYPE;
+    if (bias ? (b_dtype != CCC_F32 && b_dtype != CCC_BF16) : (b_dtype != CCC_NONE)) return CCC_ERR_DTYPE;
+    if (!x || !weight || !cu_seqlens || !dy || !dx || !dweight) return CCC_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(dy, 16) || !aligned(dx, 16) || (saved_hist && !aligned(saved_hist, 16)) ||
+        (d_final_state && !aligned(d_final_state, 16)) || (d_init_state && !aligned(d_init_state, 16)))
+        return CCC_ERR_ALIGN;
+    if (!aligned(weight, dtype_size(w_dtype)) || (bias && !aligned(bias, dtype_size(b_dtype))) ||
+        !aligned(dweight, 4) || (dbias && !aligned(dbias, 4)) || !aligned(cu_seqlens, 4) ||
+        (cache_indices && !aligned(cache_indices, 4)))
+        return CCC_ERR_ALIGN;
+    const size_t ws_need = ccc_workspace_size(rows, N, C, 1);
+    if (ws_need && (!workspace || workspace_bytes < ws_need)) return CCC_ERR_WORKSPACE;
+    if (ws_need && !aligned(workspace, kAlignWs)) return CCC_ERR_ALIGN;
+
+    const Span s_x = span(x, mat_bytes(rows, x_row_stride, C));
+    const Span s_dy = span(dy, mat_bytes(rows, dy_row_stride, C));
+    const Span s_dx = span(dx, mat_bytes(rows, dx_row_stride, C));
+    const Span s_w = span(weight, static_cast<size_t>(C) * 4 * dtype_size(w_dtype));
+    const Span s_b = span(bias, bias ? static_cast<size_t>(C) * dtype_size(b_dtype) : 0);
+    const Span s_h = span(saved_hist, static_cast<size_t>(N) * 3 * C * 2);
+    const Span s_cu = span(cu_seqlens, static_cast<size_t>(N + 1) * 4);
+    const Span s_ci = span(cache_indices, static_cast<size_t>(N) * 4);
+    const Span s_hi = span(has_initial_state, static_cast<size_t>(N));
+    const Span s_df = span(d_final_state, static_cast<size_t>(N) * 3 * C * 4);
+    const Span s_dw = span(dweight, static_cast<size_t>(C) * 4 * 4);
+    const Span s_db = span(dbias, static_cast<size_t>(C) * 4);
+    const Span s_di = span(d_init_state, static_cast<size_t>(N) * 3 * C * 4);
+    const Span s_ws = span(workspace, ws_need);
+    const Span *all[] = {&s_x, &s_dy, &s_dx, &s_w, &s_b, &s_h, &s_cu, &s_ci, &s_hi, &s_df, &s_dw, &s_db, &s_di, &s_ws};
+    const Span *written[] = {&s_dx, &s_dw, &s_db, &s_di, &s_ws};
+    for (const Span *wsp : written)
+        for (const Span *o : all)
+            if (o != wsp && overlap(*wsp, *o)) return CCC_ERR_ALIAS;
+
+    g_last_launches = 0;
+    cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+    if (rows == 0 || N == 0) {  // no token: the gradients are zero
+        if (cudaMemsetAsync(dweight, 0, static_cast<size_t>(C) * 4 * sizeof(float), st) != cudaSuccess)
+            return CCC_ERR_CUDA;
+        if (dbias && cudaMemsetAsync(dbias, 0, static_cast<size_t>(C) * sizeof(float), st) != cudaSuccess)
+            return CCC_ERR_CUDA;
+        return CCC_OK;
+    }
+
+    ccc::BwdArgs a = {};
+    a.x = static_cast<const uint16_t *>(x);
+    a.rows = rows;
+    a.C = C;
+    a.xs = x_row_stride;
+    a.w = weight;
+    a.w_bf16 = w_dtype == CCC_BF16;
+    a.b = bias;
+    a.b_kind = bias ? (b_dtype == CCC_F32 ? 1 : 2) : 0;
+    a.hist = static_cast<const uint16_t *>(saved_hist);
+    a.cu = cu_seqlens;
+    a.N = N;
+    a.cache = cache_indices;
+    a.has_init = has_initial_state;
+    a.dy = static_cast<const uint16_t *>(dy);
+    a.dys = dy_row_stride;
+    a.d_final = d_final_state;
+    a.dx = static_cast<uint16_t *>(dx);
+    a.dxs = dx_row_stride;
+    a.d_init = d_init_state;
+    a.cap = static_cast<int>(std::min<int64_t>(ccc::item_capacity(rows, N, ccc::kBwdChunk), INT32_MAX));
+    const size_t mb = map_bytes(rows, N, ccc::kBwdChunk);
+    a.part = reinterpret_cast<float *>(static_cast<char *>(workspace) + mb);
+    a.map = nullptr;
+
+    int launches = 0;
+    bool pdl = false;
+    if (N > ccc::kMaxInlineSeqs) {
+        int32_t *map = static_cast<int32_t *>(workspace);
+        if (ccc::launch_chunkmap(cu_seqlens, N, rows, ccc::kBwdChunk, 1, map, a.cap, st) != cudaSuccess)
+            return CCC_ERR_CUDA;
+        ++launches;
+        a.map = map;
+        pdl = true;
+    }
+    const int G = ccc::bwd_groups(rows, N, C);
+    if (ccc::launch_bwd(a, G, pdl, st) != cudaSuccess) return CCC_ERR_CUDA;
+    ++launches;
+    if (ccc::launch_reduce(a.part, G, C, dweight, dbias, true, st) != cudaSuccess) return CCC_ERR_CUDA;
+    ++launches;
+    g_last_launches = launches;
+    return CCC_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,278 @@
+// ccc_device.cuh -- device-side building blocks shared by the forward and
+// backward kernels of the packed width-4 causal depthwise Conv1d + SiLU.
+//
+// Data layout (FlashInfer "flashinfer.mamba.causal_conv1d_fn", Parameters):
+// activations are BF16 [rows][C] with channels contiguous, so one lane owns
+// VEC consecutive channels (VEC = 8 -> one 16-byte vector per row, VEC = 4 ->
+// 8 bytes) and a warp covers a 32*VEC-channel slab of every row it touches:
+// each row access of a warp is one fully-used, contiguous 256/512-byte span.
+// FP32 math runs on packed float2 pairs (sm_100+ FFMA2/FADD2/FMUL2), two
+// channels per instruction.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "ccc_internal.h"
+
+namespace ccc {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kCtaThreads = kWarpsPerCta * 32;
+
+// ---------------------------------------------------------------- raw I/O --
+
+// NV packed bf16x2 words = 2*NV channels of one row.
+template <int NV>
+struct Raw {
+    uint32_t u[NV];
+};
+
+template <int NV>
+__device__ __forceinline__ Raw<NV> raw_zero() {
+    Raw<NV> r;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) r.u[i] = 0u;
+    return r;
+}
+
+// Read-only (non-coherent) vector load: x and dy are never written by the
+// kernels that read them.
+template <int NV>
+__device__ __forceinline__ Raw<NV> ld_ro(const void *p) {
+    Raw<NV> r;
+    if constexpr (NV == 4) {
+        const uint4 t = __ldg(reinterpret_cast<const uint4 *>(p));
+        r.u[0] = t.x; r.u[1] = t.y; r.u[2] = t.z; r.u[3] = t.w;
+    } else {
+        static_assert(NV == 2, "VEC must be 4 or 8");
+        const uint2 t = __ldg(reinterpret_cast<const uint2 *>(p));
+        r.u[0] = t.x; r.u[1] = t.y;
+    }
+    return r;
+}
+
+// Coherent vector load (for buffers the same kernel may also write).
+template <int NV>
+__device__ __forceinline__ Raw<NV> ld_rw(const void *p) {
+    Raw<NV> r;
+    if constexpr (NV == 4) {
+        const uint4 t = *reinterpret_cast<const uint4 *>(p);
+        r.u[0] = t.x; r.u[1] = t.y; r.u[2] = t.z; r.u[3] = t.w;
+    } else {
+        const uint2 t = *reinterpret_cast<const uint2 *>(p);
+        r.u[0] = t.x; r.u[1] = t.y;
+    }
+    return r;
+}
+
+// Streaming (evict-first) store: outputs are not re-read by this kernel.
+template <int NV>
+__device__ __forceinline__ void st_stream(void *p, const Raw<NV> &r) {
+    if constexpr (NV == 4) {
+        __stcs(reinterpret_cast<uint4 *>(p), make_uint4(r.u[0], r.u[1], r.u[2], r.u[3]));
+    } else {
+        __stcs(reinterpret_cast<uint2 *>(p), make_uint2(r.u[0], r.u[1]));
+    }
+}
+
+template <int NV>
+__device__ __forceinline__ void st_plain(void *p, const Raw<NV> &r) {
+    if constexpr (NV == 4) {
+        *reinterpret_cast<uint4 *>(p) = make_uint4(r.u[0], r.u[1], r.u[2], r.u[3]);
+    } else {
+        *reinterpret_cast<uint2 *>(p) = make_uint2(r.u[0], r.u[1]);
+    }
+}
+
+// bf16x2 word -> two floats (exact: a BF16 value is the top half of an FP32).
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+
+// two floats -> bf16x2 word, round-to-nearest-even; .x goes to the low half
+// (the lower channel, as stored in memory).
+__device__ __forceinline__ uint32_t f2_to_bf2(float2 v) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+template <int NV>
+__device__ __forceinline__ void unpack(const Raw<NV> &r, float2 (&f)[NV]) {
+#pragma unroll
+    for (int i = 0; i < NV; ++i) f[i] = bf2_to_f2(r.u[i]);
+}
+
+// ------------------------------------------------------------------ math --
+
+// Documented PTX approximations (PTX ISA: ex2.approx.ftz.f32, rcp.approx.ftz.f32).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// sigmoid(z) = 1 / (1 + 2^(-z*log2(e))) on a pair.  Saturates cleanly:
+// z -> -inf gives 2^+big = inf and rcp(inf) = 0; z -> +inf gives 1.
+__device__ __forceinline__ float2 sigmoid2(float2 z) {
+    constexpr float kNegLog2e = -1.4426950408889634f;
+    const float2 m = __fmul2_rn(z, make_float2(kNegLog2e, kNegLog2e));
+    float2 d = make_float2(ex2_approx(m.x), ex2_approx(m.y));
+    d = __fadd2_rn(d, make_float2(1.0f, 1.0f));
+    return make_float2(rcp_approx(d.x), rcp_approx(d.y));
+}
+
+__device__ __forceinline__ float2 f2_zero() { return make_float2(0.0f, 0.0f); }
+
+// ------------------------------------------------------ taps and bias --
+
+// Weights [C][4] FP32 or BF16 and bias [C] FP32 / BF16 / none, read once per
+// lane into packed pairs: w_k[v] holds tap k of channels c0+2v, c0+2v+1.
+template <int NV>
+__device__ __forceinline__ void load_taps(const void *w, int w_bf16, const void *b, int b_kind,
+                                          int c0, bool act, float2 (&w0)[NV], float2 (&w1)[NV],
+                                          float2 (&w2)[NV], float2 (&w3)[NV], float2 (&bb)[NV]) {
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        float t[2][4], bv[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int c = c0 + 2 * v + h;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                float val = 0.0f;
+                if (act) {
+                    if (w_bf16) {
+                        val = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(w)[4 * c + k]);
+                    } else {
+                        val = __ldg(reinterpret_cast<const float *>(w) + 4 * c + k);
+                    }
+                }
+                t[h][k] = val;
+            }
+            float bval = 0.0f;
+            if (act && b_kind == 1) bval = __ldg(reinterpret_cast<const float *>(b) + c);
+            if (act && b_kind == 2) bval = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(b)[c]);
+            bv[h] = bval;
+        }
+        w0[v] = make_float2(t[0][0], t[1][0]);
+        w1[v] = make_float2(t[0][1], t[1][1]);
+        w2[v] = make_float2(t[0][2], t[1][2]);
+        w3[v] = make_float2(t[0][3], t[1][3]);
+        bb[v] = make_float2(bv[0], bv[1]);
+    }
+}
+
+// ---------------------------------------------------------- work items --
+//
+// A work item is (sequence n, first row r0, rows nr <= B) inside one
+// sequence; items of a sequence are consecutive B-row chunks in order, and
+// items are numbered sequence by sequence.  For n_seqs <= 32 every warp
+// derives the numbering itself from cu_seqlens with one shuffle scan, so
+// small batches need no scratch; otherwise the chunk-map kernel has written
+// (n, r0) pairs and the count to the workspace, afresh on each call
+// (causal_conv1d_fn, workspace).
+// `empty_items` gives each empty sequence one zero-row item (the backward
+// needs one to zero that sequence's d_init_state).
+
+struct Item {
+    int n;
+    int64_t s, e, r0;
+    int nr;
+};
+
+struct ItemDecoder {
+    const int32_t *map;
+    const int32_t *cu;
+    int64_t rows;
+    int B;
+    int total;
+    // register-scan state (map == nullptr)
+    int lane_s, lane_e, lane_excl, lane_incl;
+
+    __device__ __forceinline__ void init(const int32_t *map_, int cap, const int32_t *cu_, int N,
+                                         int64_t rows_, int B_, bool empty_items, int lane) {
+        map = map_;
+        cu = cu_;
+        rows = rows_;
+        B = B_;
+        if (map) {
+            const int cnt = __ldg(map);
+            total = cnt < cap ? cnt : cap;
+            return;
+        }
+        int s = 0, e = 0, ni = 0;
+        if (lane < N) {
+            s = clamp_row(__ldg(cu + lane));
+            e = clamp_row(__ldg(cu + lane + 1));
+            if (e < s) e = s;
+            ni = (e - s + B - 1) / B;
+            if (empty_items && ni == 0) ni = 1;
+        }
+        int incl = ni;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int t = __shfl_up_sync(kFull, incl, off);
+            if (lane >= off) incl += t;
+        }
+        lane_s = s;
+        lane_e = e;
+        lane_excl = incl - ni;
+        lane_incl = incl;
+        total = __shfl_sync(kFull, incl, 31);
+    }
+
+    __device__ __forceinline__ int clamp_row(int v) const {
+        return v < 0 ? 0 : (v > rows ? static_cast<int>(rows) : v);
+    }
+
+    // Must be called by all 32 lanes with the same `it`.
+    __device__ __forceinline__ Item get(int it) const {
+        Item t;
+        if (map) {
+            t.n = __ldg(map + 1 + 2 * it);
+            const int r0 = __ldg(map + 2 + 2 * it);
+            int s = clamp_row(__ldg(cu + t.n));
+            int e = clamp_row(__ldg(cu + t.n + 1));
+            if (e < s) e = s;
+            t.s = s;
+            t.e = e;
+            t.r0 = r0 < s ? s : (r0 > e ? e : r0);
+        } else {
+            // Sequences whose items all precede `it` form a lane prefix.
+            const unsigned m = __ballot_sync(kFull, lane_incl <= it);
+            t.n = __popc(m);
+            t.s = __shfl_sync(kFull, lane_s, t.n);
+            t.e = __shfl_sync(kFull, lane_e, t.n);
+            const int ex = __shfl_sync(kFull, lane_excl, t.n);
+            t.r0 = t.s + static_cast<int64_t>(it - ex) * B;
+        }
+        const int64_t left = t.e - t.r0;
+        t.nr = static_cast<int>(left < B ? left : B);
+        return t;
+    }
+};
+
+// ------------------------------------------------- programmatic launch --
+
+// Wait until the preceding kernel in the stream has finished and its writes
+// are visible (no-op when this grid was not launched as a programmatic
+// dependent).
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next kernel in the stream (launched as a programmatic dependent)
+// to be scheduled; it still waits in grid_dependency_wait() for our writes.
+__device__ __forceinline__ void grid_dependents_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+}  // namespace ccc

@@ -1,0 +1,193 @@
+// ccc_fwd.cu -- forward kernel: packed width-4 causal depthwise Conv1d +
+// SiLU with the conv_state gather/scatter fused in.
+//
+// FlashInfer "flashinfer.mamba.causal_conv1d_fn" (Parameters): for token j of
+// sequence n and channel c, z = bias + w0*h[j] + w1*h[j+1] + w2*h[j+2] +
+// w3*h[j+3] (bias first, then the four FMAs, tap 3 on the current token),
+// out = BF16(z * sigmoid(z)); h starts with three state values (slot
+// cache_indices[n], positions 0:3, when has_initial_state[n]) or zeros; a -1
+// slot gives zero output and no state access; each nonempty live sequence
+// leaves its last three raw history values in positions 0:3.
+//
+// Mapping.  A warp owns one (work item, 32*VEC-channel slab): up to B rows
+// of one sequence.  Lane l holds channels [c0, c0+VEC) with c0 = (slab*32 +
+// l)*VEC, keeps the three previous rows in registers as FP32 pairs, and
+// streams its rows U at a time (U independent 16-byte loads in flight per
+// lane before any math).  The three rows before an item come from x (an L2
+// hit: the previous item of the same sequence has just read them) or, for a
+// sequence's first item, from the state slot.  The warp that runs a
+// sequence's first item is the only one that touches that slot: it reads the
+// initial history and, after its own rows, writes the final three values (for
+// len >= 3 these are x's last three rows, re-read from global; for shorter
+// sequences they mix the initial history and x), so the read always precedes
+// the write in program order and no other warp can race with it.
+//
+// The grid is persistent: (slabs, G) CTAs of 8 warps, each warp striding
+// over items.  Consecutive items sit in the same CTA, so an item's halo rows
+// are read while the neighbouring warp still has them in L1/L2.
+#include "ccc_device.cuh"
+#include "ccc_internal.h"
+
+namespace ccc {
+
+namespace {
+
+template <int NV>
+__device__ __forceinline__ void gather_state(const FwdArgs &a, int q, int c0, Raw<NV> (&hr)[3]) {
+    const uint16_t *base = a.state + static_cast<int64_t>(q) * a.st_slot;
+    if (a.state_vec) {
+#pragma unroll
+        for (int p = 0; p < 3; ++p) hr[p] = ld_rw<NV>(base + p * a.st_l + c0);
+    } else {
+#pragma unroll
+        for (int p = 0; p < 3; ++p) {
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                const uint32_t lo = base[(c0 + 2 * v) * a.st_c + p * a.st_l];
+                const uint32_t hi = base[(c0 + 2 * v + 1) * a.st_c + p * a.st_l];
+                hr[p].u[v] = lo | (hi << 16);
+            }
+        }
+    }
+}
+
+template <int NV>
+__device__ __forceinline__ void scatter_state(const FwdArgs &a, int q, int c0, const Raw<NV> (&fin)[3]) {
+    uint16_t *base = a.state + static_cast<int64_t>(q) * a.st_slot;
+    if (a.state_vec) {
+#pragma unroll
+        for (int p = 0; p < 3; ++p) st_plain<NV>(base + p * a.st_l + c0, fin[p]);
+    } else {
+#pragma unroll
+        for (int p = 0; p < 3; ++p) {
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                base[(c0 + 2 * v) * a.st_c + p * a.st_l] = static_cast<uint16_t>(fin[p].u[v] & 0xffffu);
+                base[(c0 + 2 * v + 1) * a.st_c + p * a.st_l] = static_cast<uint16_t>(fin[p].u[v] >> 16);
+            }
+        }
+    }
+}
+
+template <int VEC, int U>
+__global__ void __launch_bounds__(kCtaThreads, 2) fwd_kernel(const FwdArgs a) {
+    constexpr int NV = VEC / 2;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int cv = blockIdx.x * 32 + lane;
+    const bool act = cv < a.C / VEC;
+    const int c0 = act ? cv * VEC : 0;
+
+    float2 w0[NV], w1[NV], w2[NV], w3[NV], bb[NV];
+    load_taps<NV>(a.w, a.w_bf16, a.b, a.b_kind, c0, act, w0, w1, w2, w3, bb);
+
+    grid_dependency_wait();  // the chunk map, when one was built
+
+    ItemDecoder dec;
+    dec.init(a.map, a.cap, a.cu, a.N, a.rows, kFwdChunk, false, lane);
+    const int step = gridDim.y * kWarpsPerCta;
+
+    for (int it = blockIdx.y * kWarpsPerCta + warp; it < dec.total; it += step) {
+        const Item t = dec.get(it);
+        const int nr = t.nr;
+        if (nr <= 0) continue;
+        const int64_t o0 = t.r0 - t.s, L = t.e - t.s;
+        const uint16_t *xrow = a.x + t.r0 * a.xs + c0;
+        uint16_t *orow = a.out + t.r0 * a.os + c0;
+
+        int q = -2;
+        if (a.cache) q = __ldg(a.cache + t.n);
+        if (q == -1) {  // padded request: zero output, no state access
+            if (act) {
+                const Raw<NV> z = raw_zero<NV>();
+                for (int r = 0; r < nr; ++r) st_stream<NV>(orow + r * a.os, z);
+                if (o0 == 0 && a.hist)
+#pragma unroll
+                    for (int p = 0; p < 3; ++p)
+                        st_plain<NV>(a.hist + (static_cast<int64_t>(t.n) * 3 + p) * a.C + c0, z);
+            }
+            continue;
+        }
+        const bool pool = a.state != nullptr && q >= 0 && q < a.n_slots;
+
+        // The three history rows before r0 (raw BF16 bits).
+        Raw<NV> hr[3];
+#pragma unroll
+        for (int p = 0; p < 3; ++p) hr[p] = raw_zero<NV>();
+        if (o0 == 0) {
+            const bool rd = pool && a.has_init != nullptr && __ldg(a.has_init + t.n) != 0;
+            if (rd && act) gather_state<NV>(a, q, c0, hr);
+            if (a.hist && act)
+#pragma unroll
+                for (int p = 0; p < 3; ++p)
+                    st_plain<NV>(a.hist + (static_cast<int64_t>(t.n) * 3 + p) * a.C + c0, hr[p]);
+        } else if (act) {
+#pragma unroll
+            for (int p = 0; p < 3; ++p) hr[p] = ld_ro<NV>(xrow - (3 - p) * a.xs);
+        }
+        float2 h0[NV], h1[NV], h2[NV];
+        unpack<NV>(hr[0], h0);
+        unpack<NV>(hr[1], h1);
+        unpack<NV>(hr[2], h2);
+
+        for (int base = 0; base < nr; base += U) {
+            Raw<NV> cur[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                cur[u] = (act && base + u < nr) ? ld_ro<NV>(xrow + (base + u) * a.xs) : raw_zero<NV>();
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                float2 hc[NV];
+                unpack<NV>(cur[u], hc);
+                Raw<NV> y;
+#pragma unroll
+                for (int v = 0; v < NV; ++v) {
+                    float2 z = bb[v];
+                    z = __ffma2_rn(w0[v], h0[v], z);
+                    z = __ffma2_rn(w1[v], h1[v], z);
+                    z = __ffma2_rn(w2[v], h2[v], z);
+                    z = __ffma2_rn(w3[v], hc[v], z);
+                    y.u[v] = f2_to_bf2(__fmul2_rn(z, sigmoid2(z)));
+                    h0[v] = h1[v];
+                    h1[v] = h2[v];
+                    h2[v] = hc[v];
+                }
+                if (act && base + u < nr) st_stream<NV>(orow + (base + u) * a.os, y);
+            }
+        }
+
+        // Final three raw history values h[L], h[L+1], h[L+2] -> positions 0:3.
+        if (o0 == 0 && pool && L > 0 && act) {
+            Raw<NV> fin[3];
+#pragma unroll
+            for (int p = 0; p < 3; ++p) {
+                const int64_t idx = L + p;
+                // Select without indexing hr[] dynamically (keeps it in registers).
+                if (idx >= 3) {
+                    fin[p] = ld_ro<NV>(a.x + (t.s + idx - 3) * a.xs + c0);
+                } else {
+                    fin[p] = idx == 0 ? hr[0] : (idx == 1 ? hr[1] : hr[2]);
+                }
+            }
+            scatter_state<NV>(a, q, c0, fin);
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdArgs &a, int grid_y, bool pdl, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(a.C, 32 * kFwdVec)), static_cast<unsigned>(grid_y));
+    cfg.blockDim = dim3(kCtaThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    if (pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, fwd_kernel<kFwdVec, 8>, a);
+}
+
+}  // namespace ccc

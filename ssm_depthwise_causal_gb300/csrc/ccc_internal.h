@@ -1,0 +1,102 @@
+// ccc_internal.h -- launch interface between the C-ABI layer (ccc_api.cu)
+// and the kernels (ccc_chunkmap.cu, ccc_fwd.cu, ccc_bwd.cu).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace ccc {
+
+// Rows per work item.  Long enough that the 3-row halo an item re-reads
+// (forward: left; backward: left and right) is a few percent of its rows and
+// is served from L2, short enough that a lognormal mix of short sequences
+// still yields many items.
+constexpr int kFwdChunk = 64;
+constexpr int kBwdChunk = 64;
+// Above this many sequences the items come from the device chunk map.
+constexpr int kMaxInlineSeqs = 32;
+// Channels per lane.
+constexpr int kFwdVec = 8;
+constexpr int kBwdVec = 4;
+// Backward CTAs the partial-sum grid is sized for (152 SMs x 2 resident
+// CTAs).  Fixed, not queried, so the reduction order -- and with it every
+// bit of dweight / dbias -- depends only on (rows, N, C).
+constexpr int kBwdTargetCtas = 304;
+
+// Warps per CTA of the forward and backward kernels.
+constexpr int kWarpsPerCta = 8;
+
+// Upper bound on the number of work items: the sum over sequences of
+// max(1, ceil(len / B)) is at most ceil(rows / B) + N.
+inline int64_t item_capacity(int64_t rows, int64_t N, int B) { return (rows + B - 1) / B + N; }
+
+struct FwdArgs {
+    const uint16_t *x;
+    int64_t rows;
+    int C;
+    int64_t xs;
+    const void *w;
+    int w_bf16;
+    const void *b;
+    int b_kind;  // 0 none, 1 FP32, 2 BF16
+    uint16_t *state;
+    int n_slots;
+    int64_t st_slot, st_c, st_l;
+    int state_vec;  // channel axis contiguous and 16-byte aligned rows
+    const int32_t *cu;
+    int N;
+    const int32_t *cache;
+    const uint8_t *has_init;
+    uint16_t *out;
+    int64_t os;
+    uint16_t *hist;
+    const int32_t *map;  // nullptr: items derived in-kernel
+    int cap;
+};
+
+struct BwdArgs {
+    const uint16_t *x;
+    int64_t rows;
+    int C;
+    int64_t xs;
+    const void *w;
+    int w_bf16;
+    const void *b;
+    int b_kind;
+    const uint16_t *hist;
+    const int32_t *cu;
+    int N;
+    const int32_t *cache;
+    const uint8_t *has_init;
+    const uint16_t *dy;
+    int64_t dys;
+    const float *d_final;
+    uint16_t *dx;
+    int64_t dxs;
+    float *d_init;
+    float *part;  // [G][5][C]
+    const int32_t *map;
+    int cap;
+};
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Grid height of the backward (number of partial-sum groups G).
+inline int bwd_groups(int64_t rows, int N, int C) {
+    const int64_t slabs = ceil_div(C, 32 * kBwdVec);
+    const int64_t cap = ceil_div(rows, kBwdChunk) + N;
+    int64_t g = ceil_div(kBwdTargetCtas, slabs);
+    const int64_t gmax = ceil_div(cap, kWarpsPerCta);
+    if (g > gmax) g = gmax;
+    return static_cast<int>(g < 1 ? 1 : g);
+}
+
+cudaError_t launch_chunkmap(const int32_t *cu, int N, int64_t rows, int B, int empty_items,
+                            int32_t *map, int cap, cudaStream_t st);
+cudaError_t launch_fwd(const FwdArgs &a, int grid_y, bool pdl, cudaStream_t st);
+cudaError_t launch_bwd(const BwdArgs &a, int grid_y, bool pdl, cudaStream_t st);
+cudaError_t launch_reduce(const float *part, int G, int C, float *dweight, float *dbias,
+                          bool pdl, cudaStream_t st);
+
+}  // namespace ccc

@@ -1,0 +1,150 @@
+"""Host-side checks of the C ABI (no GPU needed, no kernel launched).
+
+The library must build for sm_103a, load, export every function declared in
+include/ccc.h, size its workspace by pure host arithmetic, and reject bad
+arguments with the documented status codes before touching CUDA.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import ssm_depthwise_causal_gb300 as ccc
+from ssm_depthwise_causal_gb300 import _build, _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ccc.h")
+
+OK, E_NULL, E_SHAPE, E_DTYPE, E_ALIGN, E_WS, E_ALIAS = 0, -1, -2, -3, -4, -5, -6
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return _lib.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ccc_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_function(lib):
+    names = declared_functions()
+    assert {"ccc_fwd", "ccc_bwd", "ccc_workspace_size"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in ccc.h but not exported"
+    assert set(_lib.EXPORTS) <= set(names)
+
+
+def test_status_strings(lib):
+    assert _lib.status_string(0) == "CCC_OK"
+    assert _lib.status_string(-6) == "CCC_ERR_ALIAS"
+    assert _lib.status_string(5) == "unknown"
+
+
+def test_workspace_size_rules(lib):
+    ws = ccc.ccc_workspace_size
+    # forward: no scratch up to 32 sequences (in-kernel item scan)
+    assert ws(16384, 4, 4096, False) == 0
+    assert ws(16384, 32, 4096, False) == 0
+    # forward, N > 32: 1 + 2 * (ceil(rows/64) + N) int32, rounded to 256 bytes
+    n = (1 + 2 * ((65536 + 63) // 64 + 200)) * 4
+    assert ws(65536, 200, 7168, False) == (n + 255) // 256 * 256
+    # backward always carries the FP32 partial sums
+    assert ws(16384, 4, 4096, True) > 0
+    assert ws(65536, 200, 7168, True) > ws(65536, 200, 7168, False)
+    # degenerate / invalid
+    assert ws(0, 4, 4096, True) == 0
+    assert ws(100, 0, 4096, False) == 0
+    assert ws(100, 4, 12, False) == 0
+    assert ws(-1, 4, 4096, False) == 0
+    # grows monotonically with the problem and depends only on the sizes
+    assert ws(65536, 200, 7168, True) == ws(65536, 200, 7168, True)
+
+
+P = ctypes.c_void_p
+A = 1 << 20  # fake, 16-byte aligned, never dereferenced
+
+
+def fwd_args(**kw):
+    a = dict(x=A, rows=64, C=256, xs=256, w=A * 2, wd=0, b=None, bd=-1,
+             state=None, slots=0, L=0, s0=0, s1=0, s2=0, cu=A * 3, N=4, ci=None, hi=None,
+             out=A * 4, os=256, hist=None, ws=None, wsb=0, stream=None)
+    a.update(kw)
+    return a
+
+
+def call_fwd(lib, a):
+    return lib.ccc_fwd(P(a["x"]), a["rows"], a["C"], a["xs"], P(a["w"]), a["wd"], P(a["b"]), a["bd"],
+                       P(a["state"]), a["slots"], a["L"], a["s0"], a["s1"], a["s2"], P(a["cu"]), a["N"],
+                       P(a["ci"]), P(a["hi"]), P(a["out"]), a["os"], P(a["hist"]), P(a["ws"]), a["wsb"],
+                       P(a["stream"]))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=None), E_NULL),
+    (dict(out=None), E_NULL),
+    (dict(cu=None), E_NULL),
+    (dict(w=None), E_NULL),
+    (dict(C=12, xs=16, os=16), E_SHAPE),
+    (dict(C=0), E_SHAPE),
+    (dict(xs=128), E_SHAPE),
+    (dict(xs=260), E_SHAPE),
+    (dict(rows=-1), E_SHAPE),
+    (dict(wd=7), E_DTYPE),
+    (dict(b=A * 5, bd=-1), E_DTYPE),
+    (dict(b=None, bd=0), E_DTYPE),
+    (dict(x=A + 8), E_ALIGN),
+    (dict(out=A * 4 + 2), E_ALIGN),
+    (dict(state=A * 6, slots=8, L=2, s0=1024, s1=4, s2=1, ci=A * 7), E_SHAPE),
+    (dict(state=A * 6, slots=8, L=4, s0=1024, s1=2, s2=2, ci=A * 7), E_SHAPE),
+    (dict(state=A * 6, slots=8, L=4, s0=100, s1=4, s2=1, ci=A * 7), E_SHAPE),  # slots overlap
+    (dict(state=A * 6, slots=8, L=4, s0=1024, s1=4, s2=1, ci=None), E_NULL),
+    (dict(out=A + 64 * 2), E_ALIAS),            # out overlaps x
+    (dict(hist=A + 256, N=4), E_ALIAS),         # saved_hist inside x
+    (dict(N=40, ws=None), E_WS),                # N > 32 needs the chunk map
+    (dict(N=40, ws=A * 8, wsb=16), E_WS),
+    (dict(rows=0), OK),                         # nothing to do, nothing launched
+    (dict(N=0), OK),
+])
+def test_fwd_host_checks(lib, kw, code):
+    assert call_fwd(lib, fwd_args(**kw)) == code
+
+
+def test_fwd_state_layouts_accepted_by_checks(lib):
+    # history-contiguous [slots, C, L] and channel-contiguous [slots, L, C]
+    # views pass the layout check (rows == 0 keeps the call host-only)
+    for s in ((1024, 4, 1), (1024, 1, 256), (256, 1, 256 * 8)):
+        a = fwd_args(rows=0, state=A * 6, slots=8, L=4, s0=s[0], s1=s[1], s2=s[2], ci=A * 7)
+        assert call_fwd(lib, a) == OK, s
+
+
+def call_bwd(lib, **kw):
+    a = dict(x=A, rows=64, C=256, xs=256, w=A * 2, wd=0, b=None, bd=-1, hist=None, cu=A * 3, N=4,
+             ci=None, hi=None, dy=A * 4, dys=256, df=None, dx=A * 5, dxs=256, dw=A * 6, db=None,
+             di=None, ws=A * 9, wsb=1 << 30, stream=None)
+    a.update(kw)
+    return lib.ccc_bwd(P(a["x"]), a["rows"], a["C"], a["xs"], P(a["w"]), a["wd"], P(a["b"]), a["bd"],
+                       P(a["hist"]), P(a["cu"]), a["N"], P(a["ci"]), P(a["hi"]), P(a["dy"]), a["dys"],
+                       P(a["df"]), P(a["dx"]), a["dxs"], P(a["dw"]), P(a["db"]), P(a["di"]), P(a["ws"]),
+                       a["wsb"], P(a["stream"]))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dy=None), E_NULL),
+    (dict(dx=None), E_NULL),
+    (dict(dw=None), E_NULL),
+    (dict(dx=A + 8), E_ALIGN),
+    (dict(df=A * 7 + 4), E_ALIGN),
+    (dict(dxs=8), E_SHAPE),
+    (dict(ws=None), E_WS),
+    (dict(wsb=8), E_WS),
+    (dict(dx=A + 128), E_ALIAS),          # dx overlaps x
+    (dict(dw=A * 4 + 64), E_ALIAS),       # dweight inside dy
+    (dict(di=A * 9 + 256), E_ALIAS),      # d_init inside the workspace
+])
+def test_bwd_host_checks(lib, kw, code):
+    assert call_bwd(lib, **kw) == code

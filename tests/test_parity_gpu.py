@@ -1,0 +1,211 @@
+"""GPU path (through the C ABI) against the float64 oracle.
+
+Small cases are compared element by element on every channel; the five
+workloads run at full size and are compared on a spread of channels (every
+channel slab boundary the kernels use is included) -- exact for those
+channels, since channels never interact -- plus full-size properties (state
+bits, untouched slots, -1 rows, padding, determinism, split = unsplit).
+"""
+import numpy as np
+import pytest
+import torch
+
+from ssm_depthwise_causal_gb300 import workloads
+from tests import gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+def spread_channels(C, n=48):
+    picks = set(range(0, min(C, 8))) | set(range(max(0, C - 8), C))
+    for b in (127, 128, 255, 256, 511, 512, 1023, 1024):
+        if b < C:
+            picks.add(b)
+    picks |= set(np.linspace(0, C - 1, n).round().astype(int).tolist())
+    return sorted(picks)
+
+
+def check(wl_gpu, res, *, chans=None, backward=True, d_final=None):
+    chans = list(range(wl_gpu.C)) if chans is None else chans
+    sub = H.subset(wl_gpu, chans)
+    df = None if d_final is None else d_final[:, :, chans].double().cpu()
+    ref = H.run_oracle(sub, backward=backward, d_final=df)
+    H.compare(sub, ref, H.gpu_numpy(res, chans), backward=backward)
+
+
+def test_tiny(cuda_device):
+    wl = workloads.tiny(device=cuda_device)
+    check(wl, H.run_gpu(wl))
+
+
+@pytest.mark.parametrize("layout", ["history", "channel"])
+@pytest.mark.parametrize("pad", [0, 24])
+def test_tiny_layouts_and_strides(cuda_device, layout, pad):
+    wl = workloads.tiny(seed=3, device=cuda_device)
+    res = H.run_gpu(wl, pool_layout=layout, x_pad_cols=pad)
+    if layout == "channel":  # compare in the logical [slots, C, L] view
+        res.state = res.state.contiguous()
+    check(wl, res)
+
+
+EDGE = {
+    # lengths, C, kwargs
+    "short_and_empty": ((1, 2, 3, 4, 0, 5), 8, dict(n_minus_one=1)),
+    "chunk_boundaries": ((63, 64, 65, 127, 128, 129, 0, 1), 24, dict(n_minus_one=1)),
+    "n32_inline": (tuple(range(0, 64, 2)), 264, dict(n_minus_one=3)),
+    "n33_map": (tuple(range(0, 66, 2)), 136, dict(n_minus_one=3)),
+    "n100_short_all_init": (tuple(int(v) for v in np.random.default_rng(5).integers(0, 50, 100)),
+                            40, dict(n_minus_one=10, has_init_p=1.0)),
+    "single_long_no_state": ((1000,), 520, dict(with_state=False)),
+    "bf16_w_bf16_b": ((33, 7, 90), 64, dict(w_dtype=torch.bfloat16, b_dtype=torch.bfloat16)),
+    "no_bias": ((33, 7, 90), 64, dict(b_dtype=None)),
+    "no_init": ((17, 3, 40), 32, dict(has_init_p=0.0)),
+    "all_minus_one": ((5, 9), 16, dict(n_minus_one=2)),
+    "all_empty": ((0, 0, 0), 16, dict()),
+}
+
+
+@pytest.mark.parametrize("name", sorted(EDGE))
+def test_edge_cases(cuda_device, name):
+    lengths, C, kw = EDGE[name]
+    T = sum(lengths)
+    wl = workloads.make_custom(lengths, C, rows=T + 5, seed=11, device=cuda_device, **kw)
+    check(wl, H.run_gpu(wl))
+
+
+def test_d_final_carry(cuda_device):
+    wl = workloads.make_custom((40, 2, 0, 70), 64, rows=120, seed=2, device=cuda_device,
+                               n_minus_one=0, has_init_p=0.5)
+    g = torch.Generator(device=cuda_device).manual_seed(9)
+    d_final = torch.randn((wl.n_seqs, 3, wl.C), generator=g, device=cuda_device)
+    check(wl, H.run_gpu(wl, d_final=d_final), d_final=d_final)
+
+
+def test_no_hist_no_pool_minus_one_only(cuda_device):
+    """cache_indices without a pool: only the -1 rule applies; saved_hist
+    omitted."""
+    import ssm_depthwise_causal_gb300 as ccc
+    wl = workloads.make_custom((12, 30, 5), 32, rows=50, seed=4, device=cuda_device,
+                               n_minus_one=1)
+    out = H.fill_sentinel(torch.empty_like(wl.x))
+    ccc.ccc_fwd(wl.x, wl.weight, wl.bias, None, wl.cu_seqlens, wl.cache_indices, None, out)
+    torch.cuda.synchronize()
+    sub = H.subset(wl, list(range(wl.C)))
+    sub.conv_state = None
+    ref_out, _, _ = __import__("oracle").fwd(sub.x, sub.weight, sub.bias, sub.cu_seqlens)
+    live = H.live_rows(sub)
+    o = H.bits(out)
+    H.assert_bf16_close(o[live], ref_out[live], "out")
+    m1 = H.minus_one_rows(sub)
+    assert np.all(o[m1] == 0)
+
+
+def _full_size(wl, backward=True):
+    res = H.run_gpu(wl, backward=backward)
+    check(wl, res, chans=spread_channels(wl.C), backward=backward)
+    return res
+
+
+def test_dense_full(cuda_device):
+    _full_size(workloads.dense(device=cuda_device))
+
+
+def test_packed_full_and_deterministic(cuda_device):
+    wl = workloads.packed(device=cuda_device)
+    res = _full_size(wl)
+    # ten more backward runs: dweight / dbias / dx bitwise identical
+    import ssm_depthwise_causal_gb300 as ccc
+    ws = torch.empty(ccc.ccc_workspace_size(wl.rows, wl.n_seqs, wl.C, True), dtype=torch.uint8,
+                     device=cuda_device)
+    dx = torch.empty_like(wl.x)
+    dw = torch.empty((wl.C, 4), device=cuda_device)
+    db = torch.empty((wl.C,), device=cuda_device)
+    T = wl.valid_tokens
+    for _ in range(10):
+        ccc.ccc_bwd(wl.x, wl.weight, wl.bias, res.hist, wl.cu_seqlens, None, None, wl.dy, None,
+                    dx, dw, db, None, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(dw.view(torch.int32), res.dweight.view(torch.int32))
+        assert torch.equal(db.view(torch.int32), res.dbias.view(torch.int32))
+        assert torch.equal(dx[:T].view(torch.int16), res.dx[:T].view(torch.int16))
+
+
+def test_serving_full(cuda_device):
+    wl = workloads.serving(device=cuda_device)
+    before = wl.conv_state.clone()
+    res = _full_size(wl, backward=False)
+    # full-size state properties (every channel)
+    cu = wl.cu_seqlens.cpu().tolist()
+    ci = wl.cache_indices.cpu().tolist()
+    live = set()
+    for n in range(wl.n_seqs):
+        q, s, e = ci[n], cu[n], cu[n + 1]
+        if q == -1 or e == s:
+            continue
+        live.add(q)
+        assert e - s >= 1
+        if e - s >= 3:
+            assert torch.equal(res.state[q, :, 0:3].view(torch.int16),
+                               wl.x[e - 3:e].t().contiguous().view(torch.int16)), n
+        assert torch.equal(res.state[q, :, 3:].view(torch.int16), before[q, :, 3:].view(torch.int16))
+    for q in range(wl.conv_state.shape[0]):
+        if q not in live:
+            assert torch.equal(res.state[q].view(torch.int16), before[q].view(torch.int16)), q
+
+
+def test_long_context_split_equals_unsplit(cuda_device):
+    import ssm_depthwise_causal_gb300 as ccc
+    wl = workloads.long_context(device=cuda_device)
+    dev = cuda_device
+    T, C, F = wl.rows, wl.C, wl.fragments
+    L = T // F
+    # unsplit, one call each way
+    out_u = torch.empty_like(wl.x)
+    ccc.ccc_fwd(wl.x, wl.weight, None, None, wl.cu_seqlens, None, None, out_u)
+    dx_u = torch.empty_like(wl.x)
+    dw_u = torch.empty((C, 4), device=dev)
+    ws = torch.empty(ccc.ccc_workspace_size(T, 1, C, True), dtype=torch.uint8, device=dev)
+    ccc.ccc_bwd(wl.x, wl.weight, None, None, wl.cu_seqlens, None, None, wl.dy, None, dx_u, dw_u,
+                None, None, ws)
+    # split: fragments chained through a one-slot pool, backward in reverse
+    pool = torch.zeros((1, C, 4), dtype=torch.bfloat16, device=dev)
+    cache = torch.zeros(1, dtype=torch.int32, device=dev)
+    cu_f = torch.tensor([0, L], dtype=torch.int32, device=dev)
+    out_s = torch.empty_like(wl.x)
+    hists = []
+    for k in range(F):
+        hist = torch.empty((1, 3, C), dtype=torch.bfloat16, device=dev)
+        hi = torch.tensor([k > 0], device=dev)
+        ccc.ccc_fwd(wl.x[k * L:(k + 1) * L], wl.weight, None, pool, cu_f, cache, hi,
+                    out_s[k * L:(k + 1) * L], hist)
+        hists.append((hist, hi))
+    dx_s = torch.empty_like(wl.x)
+    wsf = torch.empty(ccc.ccc_workspace_size(L, 1, C, True), dtype=torch.uint8, device=dev)
+    d_carry = None
+    dw_s = torch.zeros((C, 4), dtype=torch.float64, device=dev)
+    for k in reversed(range(F)):
+        hist, hi = hists[k]
+        dwk = torch.empty((C, 4), device=dev)
+        d_init = torch.empty((1, 3, C), device=dev)
+        ccc.ccc_bwd(wl.x[k * L:(k + 1) * L], wl.weight, None, hist, cu_f, cache, hi,
+                    wl.dy[k * L:(k + 1) * L], d_carry, dx_s[k * L:(k + 1) * L], dwk, None, d_init,
+                    wsf)
+        dw_s += dwk.double()
+        d_carry = d_init
+    torch.cuda.synchronize()
+    assert torch.equal(out_s.view(torch.int16), out_u.view(torch.int16)), "split fwd != unsplit"
+    assert torch.equal(dx_s.view(torch.int16), dx_u.view(torch.int16)), "split dx != unsplit"
+    assert torch.equal(pool[0, :, 0:3].view(torch.int16), wl.x[T - 3:T].t().contiguous().view(torch.int16))
+    assert torch.all(d_carry == 0), "the first fragment read no state: d_init must be 0"
+    # unsplit vs the oracle on a channel subset
+    chans = spread_channels(C, n=24)
+    sub = H.subset(wl, chans)
+    ref = H.run_oracle(sub)
+    res = H.GpuResult(out=out_u, state=None, hist=H.fill_sentinel(torch.empty((1, 3, C), dtype=torch.bfloat16, device=dev)),
+                      dx=dx_u, dweight=dw_u, dbias=None, d_init=None)
+    g = H.gpu_numpy(res, chans)
+    g["hist"] = ref["hist"]  # no history was saved in the unsplit call
+    H.compare(sub, ref, g)
+    # fragment-summed dweight within the reduction tolerance of the oracle
+    H.assert_reduction_close(dw_s[chans].cpu().numpy(), ref["dweight"], ref["abs_dweight"],
+                             "split dweight")
