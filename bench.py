@@ -424,7 +424,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", action="store_true",
                     help="run warm-up + one step of --workload only (for ncu captures)")
-    ap.add_argument("--workload", default="packed", choices=["tiny", "dense", "packed", "serving", "long"])
+    ap.add_argument("--workload", default="packed", choices=["tiny", "dense", "packed", "packed_small", "serving", "long"])
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     ws, rank, local = dist_env()

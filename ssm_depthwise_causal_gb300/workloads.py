@@ -254,10 +254,18 @@ def long_context(seed=0, device="cpu", C=4096, T=1 << 20, fragments=8) -> Worklo
                     dy=dy, fragments=fragments)
 
 
+def packed_small(seed=0, device="cpu") -> Workload:
+    """The packed workload at a quarter of the rows (16384 rows, 50
+    sequences): each tensor is 235 MB, still larger than L2, for profiler
+    captures that replay the kernel many times."""
+    return packed(seed, device, rows=16384, N=50)
+
+
 WORKLOADS = {
     "tiny": tiny,
     "dense": dense,
     "packed": packed,
+    "packed_small": packed_small,
     "serving": serving,
     "long": long_context,
 }
