@@ -57,6 +57,21 @@ def init_dist(ws, backend):
     return None
 
 
+def job_max(value: float, dist, device) -> float:
+    """Max of a per-rank number over all ranks (the job's time is its slowest
+    rank's); identity on one process."""
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world_size: int, tokens_per_rank: int, ms_per_step: float) -> float:
+    """Whole-job tokens/s: every rank is a replica processing its own batch."""
+    return world_size * tokens_per_rank / (ms_per_step / 1e3)
+
+
 def measured_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -290,16 +305,12 @@ def run_ours(args, ws, rank, local):
     clk = clocks.stop()
     if dist:
         dist.barrier()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if dist:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = job_max(t_start.elapsed_time(t_end), dist, dev)
     gpu_launches = launches["n"]
     fwd_ms = statistics.mean(ev[k][0].elapsed_time(ev[k][1]) for k in range(K))
     bwd_ms = statistics.mean(ev[k][1].elapsed_time(ev[k][2]) for k in range(K))
     ms_step = elapsed_ms / K
-    value = ws * T / (ms_step / 1e3)
+    value = job_throughput(ws, T, ms_step)
     fb, bb = algorithmic_bytes(wl)
     peak, peak_kind = measured_peak()
     eff_gbs = (fb + bb) / (ms_step / 1e3) / 1e9
@@ -342,12 +353,8 @@ def run_ours(args, ws, rank, local):
             e2e_step()
         e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_val = ws * T / (e2e_ms / 1e3)
+    e2e_ms = job_max(e0.elapsed_time(e1) / e2e_steps, dist, dev)
+    e2e_val = job_throughput(ws, T, e2e_ms)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
