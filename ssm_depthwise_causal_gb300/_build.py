@@ -52,8 +52,8 @@ def _stamp(src: str, extra: list[str]) -> str:
     return h.hexdigest()
 
 
-def _compile(src: str, extra: list[str], verbose: bool) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+def _compile(src: str, extra: list[str], verbose: bool, build_dir: str = BUILD) -> str:
+    obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
     stamp_path = obj + ".stamp"
     stamp = _stamp(src, extra)
     if os.path.exists(obj) and os.path.exists(stamp_path) and open(stamp_path).read() == stamp:
@@ -71,24 +71,29 @@ def _compile(src: str, extra: list[str], verbose: bool) -> str:
     return obj
 
 
-def build(verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    """Compile every CUDA unit and link libccc.so; returns its path."""
+def build(verbose: bool = False, extra_flags: list[str] | None = None, lib_path: str = LIB,
+          build_dir: str = BUILD) -> str:
+    """Compile every CUDA unit and link the library (by default
+    ssm_depthwise_causal_gb300/libccc.so); returns its path.  `extra_flags`
+    (e.g. -DCCC_BWD_UNROLL=8) with another `lib_path` / `build_dir` builds a
+    variant beside the default one."""
     extra = list(extra_flags or [])
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra, verbose), srcs))
+        objs = list(ex.map(lambda s: _compile(s, extra, verbose, build_dir), srcs))
     newest = max(os.path.getmtime(o) for o in objs)
-    if not os.path.exists(LIB) or os.path.getmtime(LIB) < newest:
-        tmp = LIB + f".tmp{os.getpid()}"
+    LIB_OUT = lib_path
+    if not os.path.exists(LIB_OUT) or os.path.getmtime(LIB_OUT) < newest:
+        tmp = LIB_OUT + f".tmp{os.getpid()}"
         cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs
         if verbose:
             print(" ".join(cmd), flush=True)
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link of libccc.so failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, LIB_OUT)
+    return LIB_OUT
 
 
 if __name__ == "__main__":

@@ -203,7 +203,7 @@ int ccc_fwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
         pdl = true;
     }
     const int64_t slabs = ceil_div(C, 32 * ccc::kFwdVec);
-    const int64_t want = ceil_div(static_cast<int64_t>(sm_count()) * 2 * 2, slabs);  // 2 waves of 2 CTAs/SM
+    const int64_t want = ceil_div(static_cast<int64_t>(sm_count()) * ccc::kFwdCtasPerSm, slabs);
     const int64_t gy = std::max<int64_t>(1, std::min<int64_t>(want, ceil_div(a.cap, ccc::kWarpsPerCta)));
     if (ccc::launch_fwd(a, static_cast<int>(gy), pdl, st) != cudaSuccess) return CCC_ERR_CUDA;
     ++launches;

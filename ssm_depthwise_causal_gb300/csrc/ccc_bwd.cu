@@ -20,17 +20,20 @@
 // backward is chained through d_init_state -> d_final_state gives the
 // unsplit dx and d_init_state bit for bit.
 //
-// Mapping.  As in the forward: a warp owns (item, 32*VEC-channel slab), a
-// lane owns VEC channels.  For an item of nr rows starting at sequence offset
-// o0 the lane walks i = o0 .. o0+nr+2: it needs x rows o0-3 .. o0+nr+2 and dy
-// rows o0 .. o0+nr+2 (a 3-row halo on each side, served by L2), keeps a
-// sliding window of 3 history rows and 3 past dz values in registers, emits
-// dx for row i-3 once dz_i is known, and accumulates dz_j * h[j+k] and dz_j
-// of its own rows into 5*VEC FP32 registers.
+// Mapping.  As in the forward: a warp owns a 32*VEC-channel slab, a lane
+// owns VEC channels, and each warp walks a contiguous run of work items.
+// Along consecutive items of one sequence the lane walks i = o0, o0+1, ...
+// without a break: it keeps a sliding window of 3 history rows and the 3
+// previous dz values in registers, emits dx for row i-3 once dz_i is known,
+// and accumulates dz_j * h[j+k] and dz_j of its own rows into 5*VEC FP32
+// registers.  Only where a walk starts inside a sequence does it re-read the
+// 3 rows before it, and only where it stops before the sequence end does it
+// read 3 rows past it (both from L2: the neighbouring warp's run).
 //
 // Determinism.  The grid is (slabs, G) with G fixed by (rows, N, C) only;
-// warp w of CTA (x, y) takes items y*8+w, y*8+w+8G, ... in order, so every
-// partial sum has a fixed operand order.  At the end each CTA folds its 8
+// warp w of CTA (x, y) takes the item run [v*total/W, (v+1)*total/W) with
+// v = 8y + w and W = 8G, in order, so every partial sum has a fixed operand
+// order.  At the end each CTA folds its 8
 // warps in shared memory in warp order and writes partial[y][k][c]; the
 // reduce kernel then sums the G partials of every (k, c) in order y = 0..G-1.
 #include "ccc_device.cuh"
@@ -40,10 +43,18 @@ namespace ccc {
 
 namespace {
 
-template <int VEC, int U>
-__global__ void __launch_bounds__(kCtaThreads, 2) bwd_kernel(const BwdArgs a) {
+// P = 0: each lane loads its U rows of x and dy straight into registers.
+// P > 0: each lane streams the rows of its walk through a P-stage ring of
+// U-row batches in shared memory (cp.async), keeping up to P-1 batches in
+// flight ahead of the math.
+template <int VEC, int U, int P>
+__global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const BwdArgs a) {
     constexpr int NV = VEC / 2;
     constexpr int SLAB = 32 * VEC;
+    constexpr int VB = VEC * 2;                         // bytes per lane per row
+    constexpr int RING_WARP = P * U * 2 * 32 * VB;      // ring bytes per warp
+    static_assert(P == 0 || kBwdChunk % U == 0, "items must be whole batches");
+    extern __shared__ __align__(16) unsigned char dyn_smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int cv = blockIdx.x * 32 + lane;
     const bool act = cv < a.C / VEC;
@@ -58,21 +69,70 @@ __global__ void __launch_bounds__(kCtaThreads, 2) bwd_kernel(const BwdArgs a) {
 
     grid_dependency_wait();  // the chunk map, when one was built
 
-    ItemDecoder dec;
-    dec.init(a.map, a.cap, a.cu, a.N, a.rows, kBwdChunk, true, lane);
-    const int step = gridDim.y * kWarpsPerCta;
+    ItemDecoder<kBwdChunk> dec;
+    dec.init(a.map, a.cap, a.cu, a.N, a.rows, true, lane);
 
-    for (int it = blockIdx.y * kWarpsPerCta + warp; it < dec.total; it += step) {
-        const Item t = dec.get(it);
+    // This warp's run: a contiguous, fixed range of items (same for every
+    // slab), so the operand order of every partial sum is fixed.
+    const int64_t wi = static_cast<int64_t>(blockIdx.y) * kWarpsPerCta + warp;
+    const int64_t nw = static_cast<int64_t>(gridDim.y) * kWarpsPerCta;
+    const int lo = static_cast<int>(wi * dec.total / nw);
+    const int hi = static_cast<int>((wi + 1) * dec.total / nw);
+
+    // The run's last item (sequence, row after it): where its final walk
+    // stops reading ahead.
+    int last_n = -1, last_end = 0;
+    if (lo < hi) {
+        const Item l = dec.get(hi - 1, a.map, a.cu, a.rows);
+        last_n = l.n;
+        last_end = l.r0 + l.nr;
+    }
+
+    // Sliding windows, carried from one item to the next when the next item
+    // continues the same sequence: history rows h[i..i+2] and dz_{i-1..i-3}.
+    float2 h0[NV], h1[NV], h2[NV], d1[NV], d2[NV], d3[NV];
+    int prev_n = -1, prev_end = -1;
+
+    // Ring state (P > 0): batch b of the current walk holds rows
+    // [walk start + b*U, ... + U) of x and dy, in stage b % P.
+    const uint32_t ring = smem_addr(dyn_smem + warp * RING_WARP) + lane * VB;
+    const unsigned char *ring_p = dyn_smem + warp * RING_WARP + lane * VB;
+    int p_row = 0, p_end = 0, issued = 0, consumed = 0;
+    auto issue = [&]() {
+        const int st = issued % P;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int row = p_row + u;
+            const bool ok = act && row < p_end;
+            const uint32_t off = static_cast<uint32_t>(((st * U + u) * 2) * 32 * VB);
+            cp_async<VB>(ring + off, ok ? a.x + static_cast<int64_t>(row) * a.xs + c0 : a.x, ok);
+            cp_async<VB>(ring + off + 32 * VB, ok ? a.dy + static_cast<int64_t>(row) * a.dys + c0 : a.dy, ok);
+        }
+        cp_async_commit();
+        ++issued;
+        p_row += U;
+    };
+
+    for (int it = lo; it < hi; ++it) {
+        const Item t = dec.get(it, a.map, a.cu, a.rows);
+        bool next_cont = false;
+        if (it + 1 < hi) {
+            int nn, nr0;
+            dec.head(it + 1, a.map, nn, nr0);
+            next_cont = nn == t.n && nr0 == t.r0 + t.nr;
+        }
+        const bool cont = t.n == prev_n && t.r0 == prev_end;
+        prev_n = t.n;
+        prev_end = t.r0 + t.nr;
         const int nr = t.nr;
-        const int64_t o0 = t.r0 - t.s, L = t.e - t.s;
+        const int o0 = t.r0 - t.s, L = t.e - t.s;
         const bool live = !(a.cache && __ldg(a.cache + t.n) == -1);
         float *dinit = a.d_init ? a.d_init + static_cast<int64_t>(t.n) * 3 * a.C + c0 : nullptr;
 
         if (!live || L == 0) {  // zero gradient, no contribution
             if (act) {
                 const Raw<NV> z = raw_zero<NV>();
-                for (int r = 0; r < nr; ++r) st_stream<NV>(a.dx + (t.r0 + r) * a.dxs + c0, z);
+                for (int r = 0; r < nr; ++r) st_stream<NV>(a.dx + static_cast<int64_t>(t.r0 + r) * a.dxs + c0, z);
                 if (o0 == 0 && dinit)
 #pragma unroll
                     for (int p = 0; p < 3; ++p)
@@ -84,16 +144,27 @@ __global__ void __launch_bounds__(kCtaThreads, 2) bwd_kernel(const BwdArgs a) {
         }
         const bool read_state = a.has_init != nullptr && __ldg(a.has_init + t.n) != 0;
 
-        // History rows o0-3 .. o0-1 (initial history for the first item).
-        float2 h0[NV], h1[NV], h2[NV];
-        {
+        if constexpr (P > 0) {
+            if (!cont) {
+                // A new walk: the rows it will load are [t.r0, p_end) -- to the
+                // end of the sequence, or for the run's last sequence to 3 rows
+                // past the run (within the sequence).
+                cp_async_wait(0);
+                p_row = t.r0;
+                p_end = t.n == last_n ? min(last_end + 3, t.e) : t.e;
+                issued = consumed = 0;
+                while (issued < P - 1 && p_row < p_end) issue();
+            }
+        }
+        if (!cont) {
+            // History rows o0-3 .. o0-1 (the initial history for a first item).
             Raw<NV> hr[3];
 #pragma unroll
             for (int p = 0; p < 3; ++p) hr[p] = raw_zero<NV>();
             if (act) {
                 if (o0 > 0) {
 #pragma unroll
-                    for (int p = 0; p < 3; ++p) hr[p] = ld_ro<NV>(a.x + (t.r0 - 3 + p) * a.xs + c0);
+                    for (int p = 0; p < 3; ++p) hr[p] = ld_ro<NV>(a.x + static_cast<int64_t>(t.r0 - 3 + p) * a.xs + c0);
                 } else if (a.hist) {
 #pragma unroll
                     for (int p = 0; p < 3; ++p)
@@ -103,26 +174,47 @@ __global__ void __launch_bounds__(kCtaThreads, 2) bwd_kernel(const BwdArgs a) {
             unpack<NV>(hr[0], h0);
             unpack<NV>(hr[1], h1);
             unpack<NV>(hr[2], h2);
-        }
-        float2 d1[NV], d2[NV], d3[NV];  // dz_{i-1}, dz_{i-2}, dz_{i-3}
 #pragma unroll
-        for (int v = 0; v < NV; ++v) d1[v] = d2[v] = d3[v] = f2_zero();
+            for (int v = 0; v < NV; ++v) d1[v] = d2[v] = d3[v] = f2_zero();
+        }
 
-        const int iters = nr + 3;                                       // i = o0 .. o0+nr+2
-        const int nload = static_cast<int>(L - o0 < iters ? L - o0 : iters);  // rows with i < L
+        // i = o0 + k.  Rows k < nr are this item's; when the next item does
+        // not continue the walk, 3 more steps finish dx of the last 3 rows
+        // (loading x / dy past the item while still inside the sequence).
+        const int iters = nr + (next_cont ? 0 : 3);
+        const int nload = L - o0 < iters ? L - o0 : iters;  // steps with i < L
         for (int base = 0; base < iters; base += U) {
             Raw<NV> xr[U], gr[U];
+            if constexpr (P == 0) {
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const bool ld = act && base + u < nload;
-                xr[u] = ld ? ld_ro<NV>(a.x + (t.r0 + base + u) * a.xs + c0) : raw_zero<NV>();
-                gr[u] = ld ? ld_ro<NV>(a.dy + (t.r0 + base + u) * a.dys + c0) : raw_zero<NV>();
+                for (int u = 0; u < U; ++u) {
+                    const bool ld = act && base + u < nload;
+                    xr[u] = ld ? ld_ro<NV>(a.x + static_cast<int64_t>(t.r0 + base + u) * a.xs + c0)
+                               : raw_zero<NV>();
+                    gr[u] = ld ? ld_ro<NV>(a.dy + static_cast<int64_t>(t.r0 + base + u) * a.dys + c0)
+                               : raw_zero<NV>();
+                }
+            } else {
+                if (base < nload) {  // the next batch of the walk (zero-filled past p_end)
+                    cp_async_wait(issued - consumed - 1);
+                    const unsigned char *src = ring_p + (consumed % P) * U * 2 * 32 * VB;
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        xr[u] = ld_shared<NV>(src + (u * 2) * 32 * VB);
+                        gr[u] = ld_shared<NV>(src + (u * 2 + 1) * 32 * VB);
+                    }
+                    ++consumed;
+                    if (p_row < p_end) issue();
+                } else {
+#pragma unroll
+                    for (int u = 0; u < U; ++u) xr[u] = gr[u] = raw_zero<NV>();
+                }
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int k = base + u;
                 if (k >= iters) break;
-                const int64_t i = o0 + k;
+                const int i = o0 + k;
                 float2 hc[NV], dz[NV];
                 unpack<NV>(xr[u], hc);
                 if (k < nload) {
@@ -154,8 +246,12 @@ __global__ void __launch_bounds__(kCtaThreads, 2) bwd_kernel(const BwdArgs a) {
                         gb[v] = __fadd2_rn(gb[v], dz[v]);
                     }
                 }
-                const bool emit_dx = k >= 3;
-                const bool emit_init = o0 == 0 && k < 3 && dinit != nullptr;
+                // dH[i] is complete now.  i < 3: an initial-history gradient.
+                // Otherwise it is dx of row i-3, ours unless this is the first
+                // step of a walk that starts inside a sequence (then the
+                // previous item's owner finished that row).
+                const bool emit_init = i < 3 && dinit != nullptr;
+                const bool emit_dx = i >= 3 && (cont || k >= 3);
                 if (emit_dx || emit_init) {
                     const bool carry = i >= L && a.d_final != nullptr;
                     const float2 *cp = carry ? reinterpret_cast<const float2 *>(
@@ -176,9 +272,9 @@ __global__ void __launch_bounds__(kCtaThreads, 2) bwd_kernel(const BwdArgs a) {
                             Raw<NV> o;
 #pragma unroll
                             for (int v = 0; v < NV; ++v) o.u[v] = f2_to_bf2(acc[v]);
-                            st_stream<NV>(a.dx + (t.r0 + k - 3) * a.dxs + c0, o);
+                            st_stream<NV>(a.dx + static_cast<int64_t>(t.s + i - 3) * a.dxs + c0, o);
                         } else {
-                            float2 *dp = reinterpret_cast<float2 *>(dinit + i * a.C);
+                            float2 *dp = reinterpret_cast<float2 *>(dinit + static_cast<int64_t>(i) * a.C);
 #pragma unroll
                             for (int v = 0; v < NV; ++v) dp[v] = read_state ? acc[v] : f2_zero();
                         }
@@ -224,15 +320,18 @@ __global__ void __launch_bounds__(kCtaThreads, 2) bwd_kernel(const BwdArgs a) {
 
 // dweight[c][k] = sum_{g=0..G-1} part[g][k][c] (k < 4), dbias[c] likewise
 // with k = 4: one thread per output, fixed order.
-__global__ void __launch_bounds__(256) reduce_kernel(const float *__restrict__ part, int G, int C,
-                                                     float *__restrict__ dweight, float *__restrict__ dbias) {
+// The partials are written by the backward grid, which may still be running
+// when this grid becomes resident (programmatic dependent launch): they are
+// read with L2-coherent loads, not through the read-only path.
+__global__ void __launch_bounds__(256) reduce_kernel(const float *part, int G, int C, float *dweight,
+                                                     float *dbias) {
     grid_dependency_wait();  // the backward's partials
     const int idx = blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= 5 * C) return;
     const int k = idx / C, c = idx % C;
     const float *p = part + static_cast<int64_t>(k) * C + c;
-    float s = p[0];
-    for (int g = 1; g < G; ++g) s += p[static_cast<int64_t>(g) * 5 * C];
+    float s = __ldcg(p);
+    for (int g = 1; g < G; ++g) s += __ldcg(p + static_cast<int64_t>(g) * 5 * C);
     if (k < 4) {
         dweight[4 * c + k] = s;
     } else if (dbias) {
@@ -254,7 +353,20 @@ cudaError_t launch_bwd(const BwdArgs &a, int grid_y, bool pdl, cudaStream_t st) 
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, bwd_kernel<kBwdVec, 4>, a);
+    constexpr int P = kBwdRing;
+    constexpr size_t ring_bytes = static_cast<size_t>(P) * kBwdUnroll * 2 * 32 * kBwdVec * 2 * kWarpsPerCta;
+    auto kern = bwd_kernel<kBwdVec, kBwdUnroll, P>;
+    if (ring_bytes > 48 * 1024) {
+        static bool attr_set = false;  // once per process (the attribute is per function)
+        if (!attr_set) {
+            const cudaError_t e =
+                cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ring_bytes));
+            if (e != cudaSuccess) return e;
+            attr_set = true;
+        }
+    }
+    cfg.dynamicSmemBytes = ring_bytes;
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 cudaError_t launch_reduce(const float *part, int G, int C, float *dweight, float *dbias, bool pdl,

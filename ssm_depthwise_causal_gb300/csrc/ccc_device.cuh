@@ -104,6 +104,58 @@ __device__ __forceinline__ void unpack(const Raw<NV> &r, float2 (&f)[NV]) {
     for (int i = 0; i < NV; ++i) f[i] = bf2_to_f2(r.u[i]);
 }
 
+// ------------------------------------------------- asynchronous copies --
+//
+// Per-lane global -> shared copies (PTX cp.async): the bytes land in shared
+// memory without passing through registers, so a lane can keep several rows
+// in flight while it computes on earlier ones.  `valid == false` zero-fills
+// the destination without reading global memory.
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+template <int BYTES>
+__device__ __forceinline__ void cp_async(uint32_t dst, const void *src, bool valid) {
+    const int n = valid ? BYTES : 0;
+    if constexpr (BYTES == 16) {
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
+    } else {
+        asm volatile("cp.async.ca.shared.global [%0], [%1], %2, %3;" ::"r"(dst), "l"(src), "n"(BYTES), "r"(n)
+                     : "memory");
+    }
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Wait until at most `pending` of this thread's committed copy groups are
+// still in flight (pending is a small runtime value < 8).
+__device__ __forceinline__ void cp_async_wait(int pending) {
+    switch (pending) {
+        case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+        case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+        case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+        case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+        case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+        case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
+        case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
+        default: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
+    }
+}
+
+template <int NV>
+__device__ __forceinline__ Raw<NV> ld_shared(const unsigned char *p) {
+    Raw<NV> r;
+    if constexpr (NV == 4) {
+        const uint4 t = *reinterpret_cast<const uint4 *>(p);
+        r.u[0] = t.x; r.u[1] = t.y; r.u[2] = t.z; r.u[3] = t.w;
+    } else {
+        const uint2 t = *reinterpret_cast<const uint2 *>(p);
+        r.u[0] = t.x; r.u[1] = t.y;
+    }
+    return r;
+}
+
 // ------------------------------------------------------------------ math --
 
 // Documented PTX approximations (PTX ISA: ex2.approx.ftz.f32, rcp.approx.ftz.f32).
@@ -182,36 +234,43 @@ __device__ __forceinline__ void load_taps(const void *w, int w_bf16, const void 
 // `empty_items` gives each empty sequence one zero-row item (the backward
 // needs one to zero that sequence's d_init_state).
 
+// Row indices fit in 32 bits (the host rejects rows > INT32_MAX: cu_seqlens
+// is int32); every address is formed in 64 bits from them.
 struct Item {
     int n;
-    int64_t s, e, r0;
+    int s, e, r0;
     int nr;
 };
 
+// The decoder keeps three registers per lane for the in-kernel numbering
+// (lane n < N holds sequence n's clamped start, end and inclusive item
+// prefix); the chunk map, offsets and sizes are read from the kernel
+// parameters at each call, so they cost no registers across the loop.
+template <int B>
 struct ItemDecoder {
-    const int32_t *map;
-    const int32_t *cu;
-    int64_t rows;
-    int B;
+    int ls, le, lincl;  // register scan state (no map)
     int total;
-    // register-scan state (map == nullptr)
-    int lane_s, lane_e, lane_excl, lane_incl;
 
-    __device__ __forceinline__ void init(const int32_t *map_, int cap, const int32_t *cu_, int N,
-                                         int64_t rows_, int B_, bool empty_items, int lane) {
-        map = map_;
-        cu = cu_;
-        rows = rows_;
-        B = B_;
+    __device__ __forceinline__ static int clamp_row(int v, int64_t rows) {
+        return v < 0 ? 0 : (v > rows ? static_cast<int>(rows) : v);
+    }
+
+    // The map is written by the chunk-map kernel while this grid may already
+    // be resident (programmatic dependent launch), so it is not read-only over
+    // this kernel's lifetime: it is read with L2-coherent loads (ld.global.cg),
+    // never through the non-coherent read-only path.
+    __device__ __forceinline__ void init(const int32_t *map, int cap, const int32_t *cu, int N, int64_t rows,
+                                         bool empty_items, int lane) {
         if (map) {
-            const int cnt = __ldg(map);
+            const int cnt = __ldcg(map);
             total = cnt < cap ? cnt : cap;
+            ls = le = lincl = 0;
             return;
         }
         int s = 0, e = 0, ni = 0;
         if (lane < N) {
-            s = clamp_row(__ldg(cu + lane));
-            e = clamp_row(__ldg(cu + lane + 1));
+            s = clamp_row(__ldg(cu + lane), rows);
+            e = clamp_row(__ldg(cu + lane + 1), rows);
             if (e < s) e = s;
             ni = (e - s + B - 1) / B;
             if (empty_items && ni == 0) ni = 1;
@@ -222,40 +281,41 @@ struct ItemDecoder {
             const int t = __shfl_up_sync(kFull, incl, off);
             if (lane >= off) incl += t;
         }
-        lane_s = s;
-        lane_e = e;
-        lane_excl = incl - ni;
-        lane_incl = incl;
+        ls = s;
+        le = e;
+        lincl = incl;
         total = __shfl_sync(kFull, incl, 31);
     }
 
-    __device__ __forceinline__ int clamp_row(int v) const {
-        return v < 0 ? 0 : (v > rows ? static_cast<int>(rows) : v);
-    }
-
-    // Must be called by all 32 lanes with the same `it`.
-    __device__ __forceinline__ Item get(int it) const {
-        Item t;
+    // Sequence and first row of item `it` (all 32 lanes, same `it`).
+    __device__ __forceinline__ void head(int it, const int32_t *map, int &n, int &r0) const {
         if (map) {
-            t.n = __ldg(map + 1 + 2 * it);
-            const int r0 = __ldg(map + 2 + 2 * it);
-            int s = clamp_row(__ldg(cu + t.n));
-            int e = clamp_row(__ldg(cu + t.n + 1));
-            if (e < s) e = s;
-            t.s = s;
-            t.e = e;
-            t.r0 = r0 < s ? s : (r0 > e ? e : r0);
+            n = __ldcg(map + 1 + 2 * it);
+            r0 = __ldcg(map + 2 + 2 * it);
         } else {
             // Sequences whose items all precede `it` form a lane prefix.
-            const unsigned m = __ballot_sync(kFull, lane_incl <= it);
-            t.n = __popc(m);
-            t.s = __shfl_sync(kFull, lane_s, t.n);
-            t.e = __shfl_sync(kFull, lane_e, t.n);
-            const int ex = __shfl_sync(kFull, lane_excl, t.n);
-            t.r0 = t.s + static_cast<int64_t>(it - ex) * B;
+            n = __popc(__ballot_sync(kFull, lincl <= it));
+            const int s = __shfl_sync(kFull, ls, n), e = __shfl_sync(kFull, le, n);
+            const int incl = __shfl_sync(kFull, lincl, n);
+            const int ni = max((e - s + B - 1) / B, 1);
+            r0 = s + (it - (incl - ni)) * B;
         }
-        const int64_t left = t.e - t.r0;
-        t.nr = static_cast<int>(left < B ? left : B);
+    }
+
+    __device__ __forceinline__ Item get(int it, const int32_t *map, const int32_t *cu, int64_t rows) const {
+        Item t;
+        head(it, map, t.n, t.r0);
+        if (map) {
+            t.s = clamp_row(__ldg(cu + t.n), rows);
+            t.e = clamp_row(__ldg(cu + t.n + 1), rows);
+            if (t.e < t.s) t.e = t.s;
+            t.r0 = t.r0 < t.s ? t.s : (t.r0 > t.e ? t.e : t.r0);
+        } else {
+            t.s = __shfl_sync(kFull, ls, t.n);
+            t.e = __shfl_sync(kFull, le, t.n);
+        }
+        const int left = t.e - t.r0;
+        t.nr = left < B ? left : B;
         return t;
     }
 };

@@ -13,18 +13,19 @@
 // of one sequence.  Lane l holds channels [c0, c0+VEC) with c0 = (slab*32 +
 // l)*VEC, keeps the three previous rows in registers as FP32 pairs, and
 // streams its rows U at a time (U independent 16-byte loads in flight per
-// lane before any math).  The three rows before an item come from x (an L2
-// hit: the previous item of the same sequence has just read them) or, for a
-// sequence's first item, from the state slot.  The warp that runs a
+// lane before any math).  The three rows before a sequence's first item come
+// from the state slot (or are zeros).  The warp that runs a
 // sequence's first item is the only one that touches that slot: it reads the
 // initial history and, after its own rows, writes the final three values (for
 // len >= 3 these are x's last three rows, re-read from global; for shorter
 // sequences they mix the initial history and x), so the read always precedes
 // the write in program order and no other warp can race with it.
 //
-// The grid is persistent: (slabs, G) CTAs of 8 warps, each warp striding
-// over items.  Consecutive items sit in the same CTA, so an item's halo rows
-// are read while the neighbouring warp still has them in L1/L2.
+// The grid is persistent: (slabs, G) CTAs of 8 warps; each warp walks a
+// contiguous run of items and carries its 3-row window from one item to the
+// next when they continue the same sequence, so the 3 rows before a walk are
+// re-read (from L2: the neighbouring warp's run) only where a run starts
+// inside a sequence.
 #include "ccc_device.cuh"
 #include "ccc_internal.h"
 
@@ -70,7 +71,7 @@ __device__ __forceinline__ void scatter_state(const FwdArgs &a, int q, int c0, c
 }
 
 template <int VEC, int U>
-__global__ void __launch_bounds__(kCtaThreads, 2) fwd_kernel(const FwdArgs a) {
+__global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const FwdArgs a) {
     constexpr int NV = VEC / 2;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int cv = blockIdx.x * 32 + lane;
@@ -82,24 +83,35 @@ __global__ void __launch_bounds__(kCtaThreads, 2) fwd_kernel(const FwdArgs a) {
 
     grid_dependency_wait();  // the chunk map, when one was built
 
-    ItemDecoder dec;
-    dec.init(a.map, a.cap, a.cu, a.N, a.rows, kFwdChunk, false, lane);
-    const int step = gridDim.y * kWarpsPerCta;
+    ItemDecoder<kFwdChunk> dec;
+    dec.init(a.map, a.cap, a.cu, a.N, a.rows, false, lane);
 
-    for (int it = blockIdx.y * kWarpsPerCta + warp; it < dec.total; it += step) {
-        const Item t = dec.get(it);
+    // This warp's run of consecutive items (the same rows for every slab).
+    const int64_t wi = static_cast<int64_t>(blockIdx.y) * kWarpsPerCta + warp;
+    const int64_t nw = static_cast<int64_t>(gridDim.y) * kWarpsPerCta;
+    const int lo = static_cast<int>(wi * dec.total / nw);
+    const int hi = static_cast<int>((wi + 1) * dec.total / nw);
+
+    float2 h0[NV], h1[NV], h2[NV];  // the three rows before the current one
+    int prev_n = -1, prev_end = -1;
+
+    for (int it = lo; it < hi; ++it) {
+        const Item t = dec.get(it, a.map, a.cu, a.rows);
+        const bool cont = t.n == prev_n && t.r0 == prev_end;  // window carried over
+        prev_n = t.n;
+        prev_end = t.r0 + t.nr;
         const int nr = t.nr;
         if (nr <= 0) continue;
-        const int64_t o0 = t.r0 - t.s, L = t.e - t.s;
-        const uint16_t *xrow = a.x + t.r0 * a.xs + c0;
-        uint16_t *orow = a.out + t.r0 * a.os + c0;
+        const int o0 = t.r0 - t.s, L = t.e - t.s;
+        const uint16_t *xrow = a.x + static_cast<int64_t>(t.r0) * a.xs + c0;
+        uint16_t *orow = a.out + static_cast<int64_t>(t.r0) * a.os + c0;
 
         int q = -2;
         if (a.cache) q = __ldg(a.cache + t.n);
         if (q == -1) {  // padded request: zero output, no state access
             if (act) {
                 const Raw<NV> z = raw_zero<NV>();
-                for (int r = 0; r < nr; ++r) st_stream<NV>(orow + r * a.os, z);
+                for (int r = 0; r < nr; ++r) st_stream<NV>(orow + static_cast<int64_t>(r) * a.os, z);
                 if (o0 == 0 && a.hist)
 #pragma unroll
                     for (int p = 0; p < 3; ++p)
@@ -108,34 +120,38 @@ __global__ void __launch_bounds__(kCtaThreads, 2) fwd_kernel(const FwdArgs a) {
             continue;
         }
         const bool pool = a.state != nullptr && q >= 0 && q < a.n_slots;
+        const bool rd = o0 == 0 && pool && a.has_init != nullptr && __ldg(a.has_init + t.n) != 0;
 
-        // The three history rows before r0 (raw BF16 bits).
-        Raw<NV> hr[3];
+        if (!cont) {
+            // The three history rows before r0 (raw BF16 bits): the initial
+            // state (or zeros) for a sequence's first item, else x rows.
+            Raw<NV> hr[3];
 #pragma unroll
-        for (int p = 0; p < 3; ++p) hr[p] = raw_zero<NV>();
-        if (o0 == 0) {
-            const bool rd = pool && a.has_init != nullptr && __ldg(a.has_init + t.n) != 0;
-            if (rd && act) gather_state<NV>(a, q, c0, hr);
-            if (a.hist && act)
+            for (int p = 0; p < 3; ++p) hr[p] = raw_zero<NV>();
+            if (o0 == 0) {
+                if (rd && act) gather_state<NV>(a, q, c0, hr);
+                if (a.hist && act)
 #pragma unroll
-                for (int p = 0; p < 3; ++p)
-                    st_plain<NV>(a.hist + (static_cast<int64_t>(t.n) * 3 + p) * a.C + c0, hr[p]);
-        } else if (act) {
+                    for (int p = 0; p < 3; ++p)
+                        st_plain<NV>(a.hist + (static_cast<int64_t>(t.n) * 3 + p) * a.C + c0, hr[p]);
+            } else if (act) {
 #pragma unroll
-            for (int p = 0; p < 3; ++p) hr[p] = ld_ro<NV>(xrow - (3 - p) * a.xs);
+                for (int p = 0; p < 3; ++p) hr[p] = ld_ro<NV>(xrow - static_cast<int64_t>(3 - p) * a.xs);
+            }
+            unpack<NV>(hr[0], h0);
+            unpack<NV>(hr[1], h1);
+            unpack<NV>(hr[2], h2);
         }
-        float2 h0[NV], h1[NV], h2[NV];
-        unpack<NV>(hr[0], h0);
-        unpack<NV>(hr[1], h1);
-        unpack<NV>(hr[2], h2);
 
         for (int base = 0; base < nr; base += U) {
             Raw<NV> cur[U];
 #pragma unroll
             for (int u = 0; u < U; ++u)
-                cur[u] = (act && base + u < nr) ? ld_ro<NV>(xrow + (base + u) * a.xs) : raw_zero<NV>();
+                cur[u] = (act && base + u < nr) ? ld_ro<NV>(xrow + static_cast<int64_t>(base + u) * a.xs)
+                                                : raw_zero<NV>();
 #pragma unroll
             for (int u = 0; u < U; ++u) {
+                if (base + u >= nr) break;
                 float2 hc[NV];
                 unpack<NV>(cur[u], hc);
                 Raw<NV> y;
@@ -151,21 +167,25 @@ __global__ void __launch_bounds__(kCtaThreads, 2) fwd_kernel(const FwdArgs a) {
                     h1[v] = h2[v];
                     h2[v] = hc[v];
                 }
-                if (act && base + u < nr) st_stream<NV>(orow + (base + u) * a.os, y);
+                if (act) st_stream<NV>(orow + static_cast<int64_t>(base + u) * a.os, y);
             }
         }
 
-        // Final three raw history values h[L], h[L+1], h[L+2] -> positions 0:3.
+        // Final three raw history values h[L], h[L+1], h[L+2] -> positions
+        // 0:3, by the warp that read the initial ones (read before write).
         if (o0 == 0 && pool && L > 0 && act) {
+            Raw<NV> init[3];
+#pragma unroll
+            for (int p = 0; p < 3; ++p) init[p] = raw_zero<NV>();
+            if (rd && L < 3) gather_state<NV>(a, q, c0, init);  // still unwritten
             Raw<NV> fin[3];
 #pragma unroll
             for (int p = 0; p < 3; ++p) {
-                const int64_t idx = L + p;
-                // Select without indexing hr[] dynamically (keeps it in registers).
+                const int idx = L + p;
                 if (idx >= 3) {
-                    fin[p] = ld_ro<NV>(a.x + (t.s + idx - 3) * a.xs + c0);
+                    fin[p] = ld_ro<NV>(a.x + static_cast<int64_t>(t.s + idx - 3) * a.xs + c0);
                 } else {
-                    fin[p] = idx == 0 ? hr[0] : (idx == 1 ? hr[1] : hr[2]);
+                    fin[p] = idx == 0 ? init[0] : (idx == 1 ? init[1] : init[2]);
                 }
             }
             scatter_state<NV>(a, q, c0, fin);
@@ -187,7 +207,7 @@ cudaError_t launch_fwd(const FwdArgs &a, int grid_y, bool pdl, cudaStream_t st) 
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, fwd_kernel<kFwdVec, 8>, a);
+    return cudaLaunchKernelEx(&cfg, fwd_kernel<kFwdVec, kFwdUnroll>, a);
 }
 
 }  // namespace ccc

@@ -8,21 +8,70 @@
 
 namespace ccc {
 
+// Tuning constants.  Each can be overridden at compile time (-DCCC_...) for
+// sweeps; the defaults are the measured choice on GB300.
+#ifndef CCC_FWD_CHUNK
+#define CCC_FWD_CHUNK 64
+#endif
+#ifndef CCC_BWD_CHUNK
+#define CCC_BWD_CHUNK 64
+#endif
+#ifndef CCC_FWD_VEC
+#define CCC_FWD_VEC 8
+#endif
+#ifndef CCC_BWD_VEC
+#define CCC_BWD_VEC 4
+#endif
+#ifndef CCC_FWD_UNROLL
+#define CCC_FWD_UNROLL 8
+#endif
+#ifndef CCC_BWD_UNROLL
+#define CCC_BWD_UNROLL 4
+#endif
+#ifndef CCC_FWD_MIN_BLOCKS
+#define CCC_FWD_MIN_BLOCKS 2
+#endif
+#ifndef CCC_BWD_MIN_BLOCKS
+#define CCC_BWD_MIN_BLOCKS 2
+#endif
+#ifndef CCC_BWD_TARGET_CTAS
+#define CCC_BWD_TARGET_CTAS 304
+#endif
+#ifndef CCC_BWD_RING
+#define CCC_BWD_RING 0
+#endif
+#ifndef CCC_FWD_CTAS_PER_SM
+#define CCC_FWD_CTAS_PER_SM 4
+#endif
+
 // Rows per work item.  Long enough that the 3-row halo an item re-reads
 // (forward: left; backward: left and right) is a few percent of its rows and
 // is served from L2, short enough that a lognormal mix of short sequences
 // still yields many items.
-constexpr int kFwdChunk = 64;
-constexpr int kBwdChunk = 64;
+constexpr int kFwdChunk = CCC_FWD_CHUNK;
+constexpr int kBwdChunk = CCC_BWD_CHUNK;
 // Above this many sequences the items come from the device chunk map.
 constexpr int kMaxInlineSeqs = 32;
-// Channels per lane.
-constexpr int kFwdVec = 8;
-constexpr int kBwdVec = 4;
+// Channels per lane (8: one 16-byte vector per row; 4: 8 bytes, which keeps
+// the backward's per-channel state -- taps, windows, partial sums -- within
+// 128 registers).
+constexpr int kFwdVec = CCC_FWD_VEC;
+constexpr int kBwdVec = CCC_BWD_VEC;
+// Rows loaded ahead per lane before the math (independent loads in flight).
+constexpr int kFwdUnroll = CCC_FWD_UNROLL;
+constexpr int kBwdUnroll = CCC_BWD_UNROLL;
+// Resident CTAs per SM the register budget is sized for.
+constexpr int kFwdMinBlocks = CCC_FWD_MIN_BLOCKS;
+constexpr int kBwdMinBlocks = CCC_BWD_MIN_BLOCKS;
+// Backward: stages of the per-lane shared-memory ring (0 = load rows
+// straight into registers).
+constexpr int kBwdRing = CCC_BWD_RING;
+// Forward grid: CTAs per SM (times the SM count) the persistent grid aims at.
+constexpr int kFwdCtasPerSm = CCC_FWD_CTAS_PER_SM;
 // Backward CTAs the partial-sum grid is sized for (152 SMs x 2 resident
 // CTAs).  Fixed, not queried, so the reduction order -- and with it every
 // bit of dweight / dbias -- depends only on (rows, N, C).
-constexpr int kBwdTargetCtas = 304;
+constexpr int kBwdTargetCtas = CCC_BWD_TARGET_CTAS;
 
 // Warps per CTA of the forward and backward kernels.
 constexpr int kWarpsPerCta = 8;

@@ -132,16 +132,26 @@ def minus_one_rows(wl) -> np.ndarray:
     return m
 
 
-def assert_bf16_close(gpu_bits: np.ndarray, ref64: np.ndarray, what: str):
+def assert_bf16_close(gpu_bits: np.ndarray, ref64: np.ndarray, what: str, rows=None, chans=None):
+    """`rows` / `chans` (optional) map array indices back to absolute row and
+    channel numbers for the failure message."""
     got = (gpu_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     r32 = ref64.astype(np.float32).astype(np.float64)
     err = np.abs(got - r32)
     tol = 2.0 ** -7 * np.abs(r32) + 1e-3
     bad = ~(err <= tol)
     if bad.any():
-        i = np.argwhere(bad)[0]
-        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} elements out of tolerance; "
-                             f"first at {tuple(i)}: gpu {got[tuple(i)]!r} ref {r32[tuple(i)]!r}")
+        idx = np.argwhere(bad)
+        i = tuple(idx[0])
+        where = i
+        if rows is not None and len(i) == 2:
+            where = (int(rows[i[0]]), int(chans[i[1]]) if chans is not None else int(i[1]))
+        bad_rows = np.unique(idx[:, 0])
+        abs_rows = rows[bad_rows] if rows is not None else bad_rows
+        raise AssertionError(
+            f"{what}: {int(bad.sum())} of {bad.size} elements out of tolerance in {len(bad_rows)} rows "
+            f"(rows {abs_rows[:8].tolist()}...); first at row/channel {where}: gpu {got[i]!r} "
+            f"(bits {int(gpu_bits[i]):#06x}) ref {r32[i]!r}")
 
 
 def assert_reduction_close(gpu: np.ndarray, ref: np.ndarray, abs_terms: np.ndarray, what: str):
@@ -154,14 +164,14 @@ def assert_reduction_close(gpu: np.ndarray, ref: np.ndarray, abs_terms: np.ndarr
                              f"sum|terms| {abs_terms[tuple(i)]!r}")
 
 
-def compare(wl_cpu, ref, gpu: dict, *, backward=True, rows_checked=None):
+def compare(wl_cpu, ref, gpu: dict, *, backward=True, rows_checked=None, chans=None):
     """Compare GPU results (numpy, same channel subset) against the oracle."""
     T = int(wl_cpu.cu_seqlens[-1])
     live = live_rows(wl_cpu)
     m1 = minus_one_rows(wl_cpu)
     rows = np.arange(wl_cpu.rows) if rows_checked is None else rows_checked
     lv = rows[live[rows]]
-    assert_bf16_close(gpu["out"][lv], ref["out"][lv], "out")
+    assert_bf16_close(gpu["out"][lv], ref["out"][lv], "out", lv, chans)
     mo = rows[m1[rows]]
     assert np.all(gpu["out"][mo] == 0), "-1 rows of out must be +0"
     pad = rows[rows >= T]
@@ -174,7 +184,7 @@ def compare(wl_cpu, ref, gpu: dict, *, backward=True, rows_checked=None):
     assert np.all(gpu["hist"][~ne] == SENTINEL), "saved_hist rows of empty sequences were written"
     if not backward:
         return
-    assert_bf16_close(gpu["dx"][lv], ref["dx"][lv], "dx")
+    assert_bf16_close(gpu["dx"][lv], ref["dx"][lv], "dx", lv, chans)
     assert np.all(gpu["dx"][mo] == 0), "-1 rows of dx must be +0"
     assert np.all(gpu["dx"][pad] == SENTINEL), "padding rows of dx were written"
     assert_reduction_close(gpu["dweight"], ref["dweight"], ref["abs_dweight"], "dweight")

@@ -30,7 +30,7 @@ def check(wl_gpu, res, *, chans=None, backward=True, d_final=None):
     sub = H.subset(wl_gpu, chans)
     df = None if d_final is None else d_final[:, :, chans].double().cpu()
     ref = H.run_oracle(sub, backward=backward, d_final=df)
-    H.compare(sub, ref, H.gpu_numpy(res, chans), backward=backward)
+    H.compare(sub, ref, H.gpu_numpy(res, chans), backward=backward, chans=chans)
 
 
 def test_tiny(cuda_device):
