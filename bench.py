@@ -191,27 +191,33 @@ def oracle_sample(wl, chans):
     return x, dy, w, b, wl.cu_seqlens.cpu()
 
 
-def time_oracle(wl, target_s=12.0, max_chans=None):
+def time_oracle(wl, target_s=12.0):
+    """Time the float64 oracle (as it stands) on a bounded sample of the
+    workload: all rows and sequences, the first `chans` channels, repeated
+    `reps` times, sized to about `target_s` seconds of CPU work.  Returns
+    (tokens/s scaled to the full channel count, threads, sample text, s)."""
     import oracle
     oracle.build()
     C = wl.C
-    chans = 8
+    chans = min(C, 64)
     x, dy, w, b, cu = oracle_sample(wl, chans)
     t0 = time.perf_counter()
     _, _, hist = oracle.fwd(x, w, b, cu)
     oracle.bwd(x, w, b, cu, dy, hist)
-    dt = time.perf_counter() - t0
-    # grow the sample to about target_s of CPU work
-    chans = int(min(C if max_chans is None else max_chans, max(8, chans * target_s / max(dt, 1e-3))))
+    probe = max(time.perf_counter() - t0, 1e-3)
+    per_chan = probe / chans
+    chans = int(min(C, max(8, target_s / per_chan)))
     chans = max(8, chans - chans % 8)
+    reps = max(1, int(round(target_s / (per_chan * chans))))
     x, dy, w, b, cu = oracle_sample(wl, chans)
     t0 = time.perf_counter()
-    _, _, hist = oracle.fwd(x, w, b, cu)
-    oracle.bwd(x, w, b, cu, dy, hist)
+    for _ in range(reps):
+        _, _, hist = oracle.fwd(x, w, b, cu)
+        oracle.bwd(x, w, b, cu, dy, hist)
     dt = time.perf_counter() - t0
-    tok_s = wl.valid_tokens * (chans / C) / dt
-    sample = (f"all {wl.valid_tokens} valid tokens of the workload, first {chans} of {C} channels "
-              f"(fwd+bwd, {dt:.2f} s); tokens/s scaled by {chans}/{C}")
+    tok_s = reps * wl.valid_tokens * (chans / C) / dt
+    sample = (f"{reps} x fwd+bwd over all {wl.valid_tokens} valid tokens, first {chans} of {C} "
+              f"channels ({dt:.1f} s); tokens/s scaled by {chans}/{C}")
     return tok_s, oracle.threads(), sample, dt
 
 

@@ -72,16 +72,29 @@ bool state_layout_ok(int n_slots, int C, int L, int64_t s_slot, int64_t s_c, int
     return true;
 }
 
-int sm_count() {
-    static int cached[64] = {0};
+// Per-device launch facts, queried once per device (host calls, no sync).
+struct DeviceFacts {
+    int sms = 0;
+    int fwd_ctas = 0;
+};
+
+const DeviceFacts &device_facts() {
+    static DeviceFacts cached[64];
+    static const DeviceFacts fallback{152, ccc::kFwdMinBlocks};
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 152;
-    if (dev < 64 && cached[dev]) return cached[dev];
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
-    if (dev < 64) cached[dev] = n;
-    return n;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fallback;
+    DeviceFacts &f = cached[dev];
+    if (f.sms == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+        f.fwd_ctas = ccc::fwd_ctas_per_sm();
+        f.sms = n;
+    }
+    return f;
 }
+
+int sm_count() { return device_facts().sms; }
+int fwd_ctas() { return device_facts().fwd_ctas; }
 
 }  // namespace
 
@@ -92,8 +105,8 @@ size_t ccc_workspace_size(int64_t rows, int32_t n_seqs, int32_t channels, int32_
     if (rows == 0 || n_seqs == 0) return 0;
     if (!for_bwd) return map_bytes(rows, n_seqs, ccc::kFwdChunk);
     const size_t mb = map_bytes(rows, n_seqs, ccc::kBwdChunk);
-    const int G = ccc::bwd_groups(rows, n_seqs, channels);
-    return mb + round_up(static_cast<size_t>(G) * 5 * channels * sizeof(float), kAlignWs);
+    const int R = ccc::bwd_runs(rows, n_seqs, channels);
+    return mb + round_up(static_cast<size_t>(R) * 5 * channels * sizeof(float), kAlignWs);
 }
 
 const char *ccc_status_string(int status) {
@@ -202,10 +215,9 @@ int ccc_fwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
         a.map = map;
         pdl = true;
     }
-    const int64_t slabs = ceil_div(C, 32 * ccc::kFwdVec);
-    const int64_t want = ceil_div(static_cast<int64_t>(sm_count()) * ccc::kFwdCtasPerSm, slabs);
-    const int64_t gy = std::max<int64_t>(1, std::min<int64_t>(want, ceil_div(a.cap, ccc::kWarpsPerCta)));
-    if (ccc::launch_fwd(a, static_cast<int>(gy), pdl, st) != cudaSuccess) return CCC_ERR_CUDA;
+    a.slabs = ccc::slabs_of(C, ccc::kFwdVec);
+    a.runs = ccc::runs_per_slab(static_cast<int64_t>(sm_count()) * fwd_ctas() * ccc::kWarpsPerCta, a.slabs, a.cap);
+    if (ccc::launch_fwd(a, pdl, st) != cudaSuccess) return CCC_ERR_CUDA;
     ++launches;
     g_last_launches = launches;
     return CCC_OK;
@@ -305,10 +317,11 @@ int ccc_bwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
         a.map = map;
         pdl = true;
     }
-    const int G = ccc::bwd_groups(rows, N, C);
-    if (ccc::launch_bwd(a, G, pdl, st) != cudaSuccess) return CCC_ERR_CUDA;
+    a.slabs = ccc::slabs_of(C, ccc::kBwdVec);
+    a.runs = ccc::bwd_runs(rows, N, C);
+    if (ccc::launch_bwd(a, pdl, st) != cudaSuccess) return CCC_ERR_CUDA;
     ++launches;
-    if (ccc::launch_reduce(a.part, G, C, dweight, dbias, true, st) != cudaSuccess) return CCC_ERR_CUDA;
+    if (ccc::launch_reduce(a.part, a.runs, C, dweight, dbias, true, st) != cudaSuccess) return CCC_ERR_CUDA;
     ++launches;
     g_last_launches = launches;
     return CCC_OK;

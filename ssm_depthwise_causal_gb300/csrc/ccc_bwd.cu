@@ -30,18 +30,32 @@
 // 3 rows before it, and only where it stops before the sequence end does it
 // read 3 rows past it (both from L2: the neighbouring warp's run).
 //
-// Determinism.  The grid is (slabs, G) with G fixed by (rows, N, C) only;
-// warp w of CTA (x, y) takes the item run [v*total/W, (v+1)*total/W) with
-// v = 8y + w and W = 8G, in order, so every partial sum has a fixed operand
-// order.  At the end each CTA folds its 8
-// warps in shared memory in warp order and writes partial[y][k][c]; the
-// reduce kernel then sums the G partials of every (k, c) in order y = 0..G-1.
+// Determinism.  The number of runs per slab R is fixed by (rows, N, C) only;
+// the warp with task (slab, run r) walks items [r*total/R, (r+1)*total/R) in
+// order and writes partial[r][k][c] for its channels, so every partial sum
+// has a fixed operand order; the reduce kernel then sums the R partials of
+// every (k, c) in order r = 0..R-1.
 #include "ccc_device.cuh"
 #include "ccc_internal.h"
 
 namespace ccc {
 
 namespace {
+
+// dz = dy * s * (1 + z * (1 - s)), s = sigmoid(z), for the recomputed
+// pre-activation z = b + w0 h0 + w1 h1 + w2 h2 + w3 hc (bias first, then the
+// four FMAs in tap order, exactly as the forward).
+__device__ __forceinline__ float2 silu_grad(float2 b, float2 w0, float2 w1, float2 w2, float2 w3, float2 h0,
+                                            float2 h1, float2 h2, float2 hc, float2 gy) {
+    float2 z = __ffma2_rn(w0, h0, b);
+    z = __ffma2_rn(w1, h1, z);
+    z = __ffma2_rn(w2, h2, z);
+    z = __ffma2_rn(w3, hc, z);
+    const float2 s = sigmoid2(z);
+    const float2 oms = __fadd2_rn(make_float2(1.0f, 1.0f), make_float2(-s.x, -s.y));
+    const float2 f = __ffma2_rn(z, oms, make_float2(1.0f, 1.0f));
+    return __fmul2_rn(gy, __fmul2_rn(s, f));
+}
 
 // P = 0: each lane loads its U rows of x and dy straight into registers.
 // P > 0: each lane streams the rows of its walk through a P-stage ring of
@@ -50,13 +64,15 @@ namespace {
 template <int VEC, int U, int P>
 __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const BwdArgs a) {
     constexpr int NV = VEC / 2;
-    constexpr int SLAB = 32 * VEC;
     constexpr int VB = VEC * 2;                         // bytes per lane per row
     constexpr int RING_WARP = P * U * 2 * 32 * VB;      // ring bytes per warp
     static_assert(P == 0 || kBwdChunk % U == 0, "items must be whole batches");
     extern __shared__ __align__(16) unsigned char dyn_smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int cv = blockIdx.x * 32 + lane;
+    const int gw = blockIdx.x * kWarpsPerCta + warp;  // this warp's task
+    if (gw >= a.slabs * a.runs) return;               // (whole warp) no task in the last CTA
+    const int slab = gw % a.slabs, run = gw / a.slabs;
+    const int cv = slab * 32 + lane;
     const bool act = cv < a.C / VEC;
     const int c0 = act ? cv * VEC : 0;
 
@@ -74,10 +90,8 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
 
     // This warp's run: a contiguous, fixed range of items (same for every
     // slab), so the operand order of every partial sum is fixed.
-    const int64_t wi = static_cast<int64_t>(blockIdx.y) * kWarpsPerCta + warp;
-    const int64_t nw = static_cast<int64_t>(gridDim.y) * kWarpsPerCta;
-    const int lo = static_cast<int>(wi * dec.total / nw);
-    const int hi = static_cast<int>((wi + 1) * dec.total / nw);
+    const int lo = static_cast<int>(static_cast<int64_t>(run) * dec.total / a.runs);
+    const int hi = static_cast<int>(static_cast<int64_t>(run + 1) * dec.total / a.runs);
 
     // The run's last item (sequence, row after it): where its final walk
     // stops reading ahead.
@@ -184,15 +198,20 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
         const int iters = nr + (next_cont ? 0 : 3);
         const int nload = L - o0 < iters ? L - o0 : iters;  // steps with i < L
         for (int base = 0; base < iters; base += U) {
+            // Steady state: every step of the batch loads a row, is one of
+            // this item's tokens and emits dx of the row 3 back (no carry:
+            // all i < L).  Such batches run guard-free; the first batch of a
+            // walk and the tail take the general path.
+            const bool fast = (cont || base >= 3) && base + U <= nload && base + U <= nr;
             Raw<NV> xr[U], gr[U];
             if constexpr (P == 0) {
+                const uint16_t *xp = a.x + static_cast<int64_t>(t.r0 + base) * a.xs + c0;
+                const uint16_t *gp = a.dy + static_cast<int64_t>(t.r0 + base) * a.dys + c0;
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    const bool ld = act && base + u < nload;
-                    xr[u] = ld ? ld_ro<NV>(a.x + static_cast<int64_t>(t.r0 + base + u) * a.xs + c0)
-                               : raw_zero<NV>();
-                    gr[u] = ld ? ld_ro<NV>(a.dy + static_cast<int64_t>(t.r0 + base + u) * a.dys + c0)
-                               : raw_zero<NV>();
+                    const bool ld = act && (fast || base + u < nload);
+                    xr[u] = ld ? ld_ro<NV>(xp + static_cast<int64_t>(u) * a.xs) : raw_zero<NV>();
+                    gr[u] = ld ? ld_ro<NV>(gp + static_cast<int64_t>(u) * a.dys) : raw_zero<NV>();
                 }
             } else {
                 if (base < nload) {  // the next batch of the walk (zero-filled past p_end)
@@ -210,6 +229,40 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
                     for (int u = 0; u < U; ++u) xr[u] = gr[u] = raw_zero<NV>();
                 }
             }
+
+            if (fast) {
+                uint16_t *dxp = a.dx + static_cast<int64_t>(t.r0 + base - 3) * a.dxs + c0;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    float2 hc[NV], gy[NV], dz[NV];
+                    unpack<NV>(xr[u], hc);
+                    unpack<NV>(gr[u], gy);
+                    Raw<NV> o;
+#pragma unroll
+                    for (int v = 0; v < NV; ++v) {
+                        dz[v] = silu_grad(bb[v], w0[v], w1[v], w2[v], w3[v], h0[v], h1[v], h2[v], hc[v], gy[v]);
+                        g0[v] = __ffma2_rn(dz[v], h0[v], g0[v]);
+                        g1[v] = __ffma2_rn(dz[v], h1[v], g1[v]);
+                        g2[v] = __ffma2_rn(dz[v], h2[v], g2[v]);
+                        g3[v] = __ffma2_rn(dz[v], hc[v], g3[v]);
+                        gb[v] = __fadd2_rn(gb[v], dz[v]);
+                        float2 c = __ffma2_rn(w0[v], dz[v], f2_zero());  // no carry (same op as the general path)
+                        c = __ffma2_rn(w1[v], d1[v], c);
+                        c = __ffma2_rn(w2[v], d2[v], c);
+                        c = __ffma2_rn(w3[v], d3[v], c);
+                        o.u[v] = f2_to_bf2(c);
+                        d3[v] = d2[v];
+                        d2[v] = d1[v];
+                        d1[v] = dz[v];
+                        h0[v] = h1[v];
+                        h1[v] = h2[v];
+                        h2[v] = hc[v];
+                    }
+                    if (act) st_stream<NV>(dxp + static_cast<int64_t>(u) * a.dxs, o);
+                }
+                continue;
+            }
+
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int k = base + u;
@@ -221,17 +274,8 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
                     float2 gy[NV];
                     unpack<NV>(gr[u], gy);
 #pragma unroll
-                    for (int v = 0; v < NV; ++v) {
-                        float2 z = bb[v];
-                        z = __ffma2_rn(w0[v], h0[v], z);
-                        z = __ffma2_rn(w1[v], h1[v], z);
-                        z = __ffma2_rn(w2[v], h2[v], z);
-                        z = __ffma2_rn(w3[v], hc[v], z);
-                        const float2 s = sigmoid2(z);
-                        const float2 oms = __fadd2_rn(make_float2(1.0f, 1.0f), make_float2(-s.x, -s.y));
-                        const float2 f = __ffma2_rn(z, oms, make_float2(1.0f, 1.0f));
-                        dz[v] = __fmul2_rn(gy[v], __fmul2_rn(s, f));
-                    }
+                    for (int v = 0; v < NV; ++v)
+                        dz[v] = silu_grad(bb[v], w0[v], w1[v], w2[v], w3[v], h0[v], h1[v], h2[v], hc[v], gy[v]);
                 } else {
 #pragma unroll
                     for (int v = 0; v < NV; ++v) dz[v] = f2_zero();
@@ -293,32 +337,24 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
         }
     }
 
-    // Let the reduce kernel get scheduled while this CTA folds its warps.
+    // Let the reduce kernel get scheduled while this warp stores its sums.
     grid_dependents_launch();
 
-    // Fold the 8 warps' partials in warp order, write partial[y][k][c].
-    __shared__ float red[kWarpsPerCta][5][SLAB];
+    // partial[run][k][c0 .. c0+VEC) for k = 0..3 (taps) and 4 (bias).
+    if (act) {
+        float *pp = a.part + static_cast<int64_t>(run) * 5 * a.C + c0;
 #pragma unroll
-    for (int v = 0; v < NV; ++v) {
-        const int cl = lane * VEC + 2 * v;
-        red[warp][0][cl] = g0[v].x; red[warp][0][cl + 1] = g0[v].y;
-        red[warp][1][cl] = g1[v].x; red[warp][1][cl + 1] = g1[v].y;
-        red[warp][2][cl] = g2[v].x; red[warp][2][cl + 1] = g2[v].y;
-        red[warp][3][cl] = g3[v].x; red[warp][3][cl + 1] = g3[v].y;
-        red[warp][4][cl] = gb[v].x; red[warp][4][cl + 1] = gb[v].y;
-    }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < 5 * SLAB; idx += kCtaThreads) {
-        const int k = idx / SLAB, cl = idx % SLAB;
-        float s = red[0][k][cl];
-#pragma unroll
-        for (int w = 1; w < kWarpsPerCta; ++w) s += red[w][k][cl];
-        const int c = blockIdx.x * SLAB + cl;
-        if (c < a.C) a.part[(static_cast<int64_t>(blockIdx.y) * 5 + k) * a.C + c] = s;
+        for (int v = 0; v < NV; ++v) {
+            reinterpret_cast<float2 *>(pp + 0 * a.C)[v] = g0[v];
+            reinterpret_cast<float2 *>(pp + 1 * a.C)[v] = g1[v];
+            reinterpret_cast<float2 *>(pp + 2 * a.C)[v] = g2[v];
+            reinterpret_cast<float2 *>(pp + 3 * a.C)[v] = g3[v];
+            reinterpret_cast<float2 *>(pp + 4 * a.C)[v] = gb[v];
+        }
     }
 }
 
-// dweight[c][k] = sum_{g=0..G-1} part[g][k][c] (k < 4), dbias[c] likewise
+// dweight[c][k] = sum_{r=0..runs-1} part[r][k][c] (k < 4), dbias[c] likewise
 // with k = 4: one thread per output, fixed order.
 // The partials are written by the backward grid, which may still be running
 // when this grid becomes resident (programmatic dependent launch): they are
@@ -341,9 +377,9 @@ __global__ void __launch_bounds__(256) reduce_kernel(const float *part, int G, i
 
 }  // namespace
 
-cudaError_t launch_bwd(const BwdArgs &a, int grid_y, bool pdl, cudaStream_t st) {
+cudaError_t launch_bwd(const BwdArgs &a, bool pdl, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(a.C, 32 * kBwdVec)), static_cast<unsigned>(grid_y));
+    cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(static_cast<int64_t>(a.slabs) * a.runs, kWarpsPerCta)));
     cfg.blockDim = dim3(kCtaThreads);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -357,12 +393,15 @@ cudaError_t launch_bwd(const BwdArgs &a, int grid_y, bool pdl, cudaStream_t st) 
     constexpr size_t ring_bytes = static_cast<size_t>(P) * kBwdUnroll * 2 * 32 * kBwdVec * 2 * kWarpsPerCta;
     auto kern = bwd_kernel<kBwdVec, kBwdUnroll, P>;
     if (ring_bytes > 48 * 1024) {
-        static bool attr_set = false;  // once per process (the attribute is per function)
-        if (!attr_set) {
-            const cudaError_t e =
-                cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ring_bytes));
+        // Opt in to more than 48 KB of dynamic shared memory, once per device.
+        static bool attr_set[64] = {};
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ring_bytes));
             if (e != cudaSuccess) return e;
-            attr_set = true;
+            if (dev >= 0 && dev < 64) attr_set[dev] = true;
         }
     }
     cfg.dynamicSmemBytes = ring_bytes;

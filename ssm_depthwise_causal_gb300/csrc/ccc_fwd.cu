@@ -21,7 +21,8 @@
 // sequences they mix the initial history and x), so the read always precedes
 // the write in program order and no other warp can race with it.
 //
-// The grid is persistent: (slabs, G) CTAs of 8 warps; each warp walks a
+// The grid is one resident wave of CTAs of 8 warps; each warp owns a
+// (slab, item run) task (ccc_internal.h, runs_per_slab) and walks its
 // contiguous run of items and carries its 3-row window from one item to the
 // next when they continue the same sequence, so the 3 rows before a walk are
 // re-read (from L2: the neighbouring warp's run) only where a run starts
@@ -74,7 +75,10 @@ template <int VEC, int U>
 __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const FwdArgs a) {
     constexpr int NV = VEC / 2;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int cv = blockIdx.x * 32 + lane;
+    const int gw = blockIdx.x * kWarpsPerCta + warp;  // this warp's task
+    if (gw >= a.slabs * a.runs) return;               // (whole warp) no task in the last CTA
+    const int slab = gw % a.slabs, run = gw / a.slabs;
+    const int cv = slab * 32 + lane;
     const bool act = cv < a.C / VEC;
     const int c0 = act ? cv * VEC : 0;
 
@@ -87,10 +91,8 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
     dec.init(a.map, a.cap, a.cu, a.N, a.rows, false, lane);
 
     // This warp's run of consecutive items (the same rows for every slab).
-    const int64_t wi = static_cast<int64_t>(blockIdx.y) * kWarpsPerCta + warp;
-    const int64_t nw = static_cast<int64_t>(gridDim.y) * kWarpsPerCta;
-    const int lo = static_cast<int>(wi * dec.total / nw);
-    const int hi = static_cast<int>((wi + 1) * dec.total / nw);
+    const int lo = static_cast<int>(static_cast<int64_t>(run) * dec.total / a.runs);
+    const int hi = static_cast<int>(static_cast<int64_t>(run + 1) * dec.total / a.runs);
 
     float2 h0[NV], h1[NV], h2[NV];  // the three rows before the current one
     int prev_n = -1, prev_end = -1;
@@ -195,9 +197,18 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
 
 }  // namespace
 
-cudaError_t launch_fwd(const FwdArgs &a, int grid_y, bool pdl, cudaStream_t st) {
+int fwd_ctas_per_sm() {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_kernel<kFwdVec, kFwdUnroll>, kCtaThreads, 0) !=
+            cudaSuccess ||
+        n < 1)
+        n = kFwdMinBlocks;
+    return n;
+}
+
+cudaError_t launch_fwd(const FwdArgs &a, bool pdl, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(a.C, 32 * kFwdVec)), static_cast<unsigned>(grid_y));
+    cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(static_cast<int64_t>(a.slabs) * a.runs, kWarpsPerCta)));
     cfg.blockDim = dim3(kCtaThreads);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];

@@ -34,14 +34,11 @@ namespace ccc {
 #ifndef CCC_BWD_MIN_BLOCKS
 #define CCC_BWD_MIN_BLOCKS 2
 #endif
-#ifndef CCC_BWD_TARGET_CTAS
-#define CCC_BWD_TARGET_CTAS 304
+#ifndef CCC_BWD_TARGET_WARPS
+#define CCC_BWD_TARGET_WARPS 2432
 #endif
 #ifndef CCC_BWD_RING
 #define CCC_BWD_RING 0
-#endif
-#ifndef CCC_FWD_CTAS_PER_SM
-#define CCC_FWD_CTAS_PER_SM 4
 #endif
 
 // Rows per work item.  Long enough that the 3-row halo an item re-reads
@@ -66,12 +63,11 @@ constexpr int kBwdMinBlocks = CCC_BWD_MIN_BLOCKS;
 // Backward: stages of the per-lane shared-memory ring (0 = load rows
 // straight into registers).
 constexpr int kBwdRing = CCC_BWD_RING;
-// Forward grid: CTAs per SM (times the SM count) the persistent grid aims at.
-constexpr int kFwdCtasPerSm = CCC_FWD_CTAS_PER_SM;
-// Backward CTAs the partial-sum grid is sized for (152 SMs x 2 resident
-// CTAs).  Fixed, not queried, so the reduction order -- and with it every
-// bit of dweight / dbias -- depends only on (rows, N, C).
-constexpr int kBwdTargetCtas = CCC_BWD_TARGET_CTAS;
+// Backward warps the work split is sized for: 152 SMs x 2 resident CTAs x 8
+// warps, i.e. one full wave on GB300.  Fixed, not queried, so the reduction
+// order -- and with it every bit of dweight / dbias -- depends only on
+// (rows, N, C).
+constexpr int kBwdTargetWarps = CCC_BWD_TARGET_WARPS;
 
 // Warps per CTA of the forward and backward kernels.
 constexpr int kWarpsPerCta = 8;
@@ -102,6 +98,7 @@ struct FwdArgs {
     uint16_t *hist;
     const int32_t *map;  // nullptr: items derived in-kernel
     int cap;
+    int slabs, runs;     // work split (see runs_per_slab)
 };
 
 struct BwdArgs {
@@ -124,27 +121,39 @@ struct BwdArgs {
     uint16_t *dx;
     int64_t dxs;
     float *d_init;
-    float *part;  // [G][5][C]
+    float *part;  // [runs][5][C]
     const int32_t *map;
     int cap;
+    int slabs, runs;
 };
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Grid height of the backward (number of partial-sum groups G).
-inline int bwd_groups(int64_t rows, int N, int C) {
-    const int64_t slabs = ceil_div(C, 32 * kBwdVec);
-    const int64_t cap = ceil_div(rows, kBwdChunk) + N;
-    int64_t g = ceil_div(kBwdTargetCtas, slabs);
-    const int64_t gmax = ceil_div(cap, kWarpsPerCta);
-    if (g > gmax) g = gmax;
-    return static_cast<int>(g < 1 ? 1 : g);
+// Work split of both kernels.  Every warp owns one task: a 32*VEC-channel
+// slab and a run of consecutive items, runs_per_slab runs per slab; warp g
+// (global index) takes slab g % slabs and run g / slabs, so the 8 warps of a
+// CTA cover neighbouring slabs of the same rows.  The grid is
+// ceil(slabs * runs / 8) CTAs -- sized to one resident wave, so no CTA waits
+// for a second wave with a whole run of work.
+inline int slabs_of(int C, int vec) { return static_cast<int>(ceil_div(C, 32 * vec)); }
+
+inline int runs_per_slab(int64_t target_warps, int slabs, int64_t cap) {
+    int64_t r = target_warps / slabs;
+    if (r > cap) r = cap;
+    return static_cast<int>(r < 1 ? 1 : r);
+}
+
+// Backward runs per slab; also the number of FP32 partial rows per channel.
+inline int bwd_runs(int64_t rows, int N, int C) {
+    return runs_per_slab(kBwdTargetWarps, slabs_of(C, kBwdVec), item_capacity(rows, N, kBwdChunk));
 }
 
 cudaError_t launch_chunkmap(const int32_t *cu, int N, int64_t rows, int B, int empty_items,
                             int32_t *map, int cap, cudaStream_t st);
-cudaError_t launch_fwd(const FwdArgs &a, int grid_y, bool pdl, cudaStream_t st);
-cudaError_t launch_bwd(const BwdArgs &a, int grid_y, bool pdl, cudaStream_t st);
+cudaError_t launch_fwd(const FwdArgs &a, bool pdl, cudaStream_t st);
+cudaError_t launch_bwd(const BwdArgs &a, bool pdl, cudaStream_t st);
+// Resident forward CTAs per SM on the current device (occupancy query).
+int fwd_ctas_per_sm();
 cudaError_t launch_reduce(const float *part, int G, int C, float *dweight, float *dbias,
                           bool pdl, cudaStream_t st);
 
