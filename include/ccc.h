@@ -164,6 +164,39 @@ int ccc_bwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
             float *dweight, float *dbias, float *d_init_state,
             void *workspace, size_t workspace_bytes, void *cuda_stream);
 
+/*
+ * Backward without a workspace argument, for callers that cannot allocate
+ * device memory (a host framework whose memory pool they cannot reach, a
+ * plugin host that forbids device allocation after start-up, a latency-
+ * critical path that cannot pay for cudaMalloc's possible device-wide
+ * synchronization).  The pages have no counterpart: this is a library
+ * convenience, not part of the method.
+ *
+ * Arguments, results and checks are those of ccc_bwd without `workspace` /
+ * `workspace_bytes`.  The scratch is a fixed array of
+ * CCC_NOALLOC_SCRATCH_BYTES compiled into the library, held by every GPU the
+ * library is loaded on until the process exits; a shape whose
+ * ccc_workspace_size(rows, N, C, 1) exceeds it returns CCC_ERR_WORKSPACE with
+ * nothing enqueued.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) and caches it; make that first call before
+ * any stream capture on the device.  All calls share the array, so calls
+ * whose GPU work overlaps (other streams, other host threads on the same
+ * device) race and must be serialized by the caller.  Nothing is allocated
+ * and no allocating routine is called.
+ */
+#define CCC_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+int ccc_bwd_noalloc(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
+                    const void *weight, int32_t w_dtype, const void *bias, int32_t b_dtype,
+                    const void *saved_hist,
+                    const int32_t *cu_seqlens, int32_t N,
+                    const int32_t *cache_indices, const uint8_t *has_initial_state,
+                    const void *dy, int64_t dy_row_stride,
+                    const float *d_final_state,
+                    void *dx, int64_t dx_row_stride,
+                    float *dweight, float *dbias, float *d_init_state,
+                    void *cuda_stream);
+
 /* Name of a ccc_status value ("CCC_OK", ...); "unknown" otherwise. */
 const char *ccc_status_string(int status);
 

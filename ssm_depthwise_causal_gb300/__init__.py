@@ -30,7 +30,8 @@ from . import _lib
 
 CCC_F32, CCC_BF16, CCC_NONE = 0, 1, -1
 
-__all__ = ["ccc_workspace_size", "ccc_fwd", "ccc_bwd", "causal_conv1d_fn", "causal_conv1d_bwd",
+__all__ = ["ccc_workspace_size", "ccc_fwd", "ccc_bwd", "ccc_bwd_noalloc", "causal_conv1d_fn",
+           "causal_conv1d_bwd",
            "CCCError", "library_path", "last_launch_count"]
 
 
@@ -127,6 +128,28 @@ def ccc_bwd(x, weight, bias, saved_hist, cu_seqlens, cache_indices, has_initial_
         _ptr(d_init_state), _ptr(workspace), ws_bytes, _stream(stream))
     if rc != 0:
         raise CCCError(rc, "ccc_bwd")
+
+
+def ccc_bwd_noalloc(x, weight, bias, saved_hist, cu_seqlens, cache_indices, has_initial_state, dy,
+                    d_final_state, dx, dweight, dbias, d_init_state, stream=None) -> None:
+    """ccc_bwd for callers that cannot allocate device memory: the library
+    uses its own fixed scratch array (``_lib.NOALLOC_SCRATCH_BYTES``) instead
+    of a workspace.  Shapes needing more scratch raise CCCError
+    (CCC_ERR_WORKSPACE).  Calls share that array: serialize calls whose GPU
+    work could overlap."""
+    x2, rows, C, xs = _rows_view(x, "x")
+    g2, grows, gC, gs = _rows_view(dy, "dy")
+    d2, drows, dC, ds = _rows_view(dx, "dx")
+    if (grows, gC) != (rows, C) or (drows, dC) != (rows, C):
+        raise ValueError("dy and dx must match x")
+    N = cu_seqlens.numel() - 1
+    rc = _lib.lib().ccc_bwd_noalloc(
+        _ptr(x2), rows, C, xs, _ptr(weight), _dtype_code(weight), _ptr(bias), _dtype_code(bias),
+        _ptr(saved_hist), _ptr(cu_seqlens), N, _ptr(cache_indices), _ptr(has_initial_state),
+        _ptr(g2), gs, _ptr(d_final_state), _ptr(d2), ds, _ptr(dweight), _ptr(dbias),
+        _ptr(d_init_state), _stream(stream))
+    if rc != 0:
+        raise CCCError(rc, "ccc_bwd_noalloc")
 
 
 def _workspace(rows, N, C, for_bwd, device, given):

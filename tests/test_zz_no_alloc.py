@@ -1,0 +1,96 @@
+"""ccc_bwd_noalloc: the backward for callers that cannot allocate device
+memory (it runs on a fixed scratch array inside the library instead of a
+caller-supplied workspace).
+
+This file is collected last on purpose, so that a run stopping at its first
+failure has already run every other test.  Each case makes two calls in a row
+-- the scratch array keeps the previous call's contents -- and compares them
+with the ordinary ccc_bwd on the same inputs, with the tolerances used by the
+other GPU tests.
+"""
+import numpy as np
+import pytest
+import torch
+
+import ssm_depthwise_causal_gb300 as ccc
+from ssm_depthwise_causal_gb300 import _lib, workloads
+from tests import gpu_helpers as H
+
+
+def _forward(wl):
+    out = torch.empty_like(wl.x)
+    hist = torch.empty((wl.n_seqs, 3, wl.C), dtype=torch.bfloat16, device=wl.x.device)
+    ccc.causal_conv1d_fn(wl.x, wl.weight, wl.conv_state, wl.cu_seqlens, wl.cache_indices,
+                         wl.has_initial_state, bias=wl.bias, out=out, saved_hist=hist)
+    return hist
+
+
+def _grads(wl, hist, noalloc):
+    dev = wl.x.device
+    dx = H.fill_sentinel(torch.empty_like(wl.x))
+    dw = torch.full((wl.C, 4), float("nan"), device=dev)
+    db = torch.full((wl.C,), float("nan"), device=dev) if wl.bias is not None else None
+    di = torch.full((wl.n_seqs, 3, wl.C), float("nan"), device=dev)
+    args = (wl.x, wl.weight, wl.bias, hist, wl.cu_seqlens, wl.cache_indices, wl.has_initial_state,
+            wl.dy, None, dx, dw, db, di)
+    if noalloc:
+        ccc.ccc_bwd_noalloc(*args)
+    else:
+        ws = torch.empty(ccc.ccc_workspace_size(wl.rows, wl.n_seqs, wl.C, True), dtype=torch.uint8,
+                         device=dev)
+        ccc.ccc_bwd(*args, ws)
+    torch.cuda.synchronize()
+    return dx, dw, db, di
+
+
+def _as_f64(bf16_bits):
+    return (bf16_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _check_same(wl, got, want):
+    T = wl.valid_tokens
+    gdx, gdw, gdb, gdi = got
+    wdx, wdw, wdb, wdi = want
+    H.assert_bf16_close(H.bits(gdx[:T]), _as_f64(H.bits(wdx[:T])), "dx (noalloc vs workspace)")
+    assert np.all(H.bits(gdx[T:]) == H.SENTINEL), "padding rows of dx were written"
+    for g, w, what in ((gdw, wdw, "dweight"), (gdb, wdb, "dbias"), (gdi, wdi, "d_init_state")):
+        if w is None:
+            continue
+        g64, w64 = g.double().cpu().numpy(), w.double().cpu().numpy()
+        assert np.all(np.abs(g64 - w64) <= 1e-4 * np.abs(w64) + 1e-6 * np.abs(w64).max()), what
+    # same kernels, same partial-sum grid: the reduction is bitwise identical
+    assert torch.equal(gdw.view(torch.int32), wdw.view(torch.int32))
+
+
+@pytest.mark.gpu
+def test_noalloc_matches_workspace_backward_two_calls(cuda_device):
+    # call 1: 200 packed sequences (chunk-map path); call 2: 4 sequences with a
+    # pool (in-kernel item path) -- the second call runs on whatever the first
+    # left in the shared scratch
+    first = workloads.make_custom(workloads.packed_lengths(seed=3, N=200, rows=16384), 1024,
+                                  rows=16384, seed=3, device=cuda_device, with_state=False)
+    second = workloads.make_custom((300, 0, 17, 1200), 512, rows=1600, seed=4, device=cuda_device,
+                                   n_minus_one=1)
+    for wl in (first, second):
+        need = ccc.ccc_workspace_size(wl.rows, wl.n_seqs, wl.C, True)
+        assert 0 < need <= _lib.NOALLOC_SCRATCH_BYTES
+        hist = _forward(wl)
+        want = _grads(wl, hist, noalloc=False)
+        got = _grads(wl, hist, noalloc=True)
+        _check_same(wl, got, want)
+
+
+@pytest.mark.gpu
+def test_noalloc_rejects_oversized_shapes(cuda_device):
+    # two million sequences: the chunk map alone needs more than the fixed
+    # scratch array, so the call is refused before anything is read or run
+    rows, N, C = 1 << 24, 2_000_000, 1024
+    assert ccc.ccc_workspace_size(rows, N, C, True) > _lib.NOALLOC_SCRATCH_BYTES
+    x = torch.empty((8, C), dtype=torch.bfloat16, device=cuda_device)
+    big = x.as_strided((rows, C), (0, 1))  # never read: the size check comes first
+    cu = torch.zeros(N + 1, dtype=torch.int32, device=cuda_device)
+    w = torch.zeros((C, 4), device=cuda_device)
+    dw = torch.empty((C, 4), device=cuda_device)
+    with pytest.raises(ccc.CCCError) as e:
+        ccc.ccc_bwd_noalloc(big, w, None, None, cu, None, None, big, None, big, dw, None, None)
+    assert e.value.status == -5  # CCC_ERR_WORKSPACE
