@@ -78,6 +78,9 @@ def build(verbose: bool = False, extra_flags: list[str] | None = None, lib_path:
     (e.g. -DCCC_BWD_UNROLL=8) with another `lib_path` / `build_dir` builds a
     variant beside the default one."""
     extra = list(extra_flags or [])
+    # Optional extra defines for experiments, e.g.
+    # CCC_EXTRA_NVCC_FLAGS="-DCCC_BWD_UNROLL=2"; unset in normal builds.
+    extra += os.environ.get("CCC_EXTRA_NVCC_FLAGS", "").split()
     os.makedirs(build_dir, exist_ok=True)
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:

@@ -138,6 +138,7 @@ int ccc_fwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
     if (rows < 0 || N < 0 || C <= 0 || C % 8 != 0) return CCC_ERR_SHAPE;
     if (rows > INT32_MAX) return CCC_ERR_SHAPE;  // cu_seqlens is int32
     if (x_row_stride < C || out_row_stride < C || x_row_stride % 8 || out_row_stride % 8) return CCC_ERR_SHAPE;
+    if (x_row_stride > INT32_MAX || out_row_stride > INT32_MAX) return CCC_ERR_SHAPE;
     if (w_dtype != CCC_F32 && w_dtype != CCC_BF16) return CCC_ERR_DTYPE;
     if (bias ? (b_dtype != CCC_F32 && b_dtype != CCC_BF16) : (b_dtype != CCC_NONE)) return CCC_ERR_DTYPE;
     if (conv_state) {
@@ -184,7 +185,7 @@ int ccc_fwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
     a.x = static_cast<const uint16_t *>(x);
     a.rows = rows;
     a.C = C;
-    a.xs = x_row_stride;
+    a.xs = static_cast<int>(x_row_stride);
     a.w = weight;
     a.w_bf16 = w_dtype == CCC_BF16;
     a.b = bias;
@@ -200,7 +201,7 @@ int ccc_fwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
     a.cache = cache_indices;
     a.has_init = has_initial_state;
     a.out = static_cast<uint16_t *>(out);
-    a.os = out_row_stride;
+    a.os = static_cast<int>(out_row_stride);
     a.hist = static_cast<uint16_t *>(saved_hist);
     a.cap = static_cast<int>(std::min<int64_t>(ccc::item_capacity(rows, N, ccc::kFwdChunk), INT32_MAX));
     a.map = nullptr;
@@ -238,6 +239,7 @@ int ccc_bwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
     if (x_row_stride < C || dy_row_stride < C || dx_row_stride < C || x_row_stride % 8 || dy_row_stride % 8 ||
         dx_row_stride % 8)
         return CCC_ERR_SHAPE;
+    if (x_row_stride > INT32_MAX || dy_row_stride > INT32_MAX || dx_row_stride > INT32_MAX) return CCC_ERR_SHAPE;
     if (w_dtype != CCC_F32 && w_dtype != CCC_BF16) return CCC_ERR_DTYPE;
     if (bias ? (b_dtype != CCC_F32 && b_dtype != CCC_BF16) : (b_dtype != CCC_NONE)) return CCC_ERR_DTYPE;
     if (!x || !weight || !cu_seqlens || !dy || !dx || !dweight) return CCC_ERR_NULL;
@@ -286,7 +288,7 @@ int ccc_bwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
     a.x = static_cast<const uint16_t *>(x);
     a.rows = rows;
     a.C = C;
-    a.xs = x_row_stride;
+    a.xs = static_cast<int>(x_row_stride);
     a.w = weight;
     a.w_bf16 = w_dtype == CCC_BF16;
     a.b = bias;
@@ -297,10 +299,10 @@ int ccc_bwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
     a.cache = cache_indices;
     a.has_init = has_initial_state;
     a.dy = static_cast<const uint16_t *>(dy);
-    a.dys = dy_row_stride;
+    a.dys = static_cast<int>(dy_row_stride);
     a.d_final = d_final_state;
     a.dx = static_cast<uint16_t *>(dx);
-    a.dxs = dx_row_stride;
+    a.dxs = static_cast<int>(dx_row_stride);
     a.d_init = d_init_state;
     a.cap = static_cast<int>(std::min<int64_t>(ccc::item_capacity(rows, N, ccc::kBwdChunk), INT32_MAX));
     const size_t mb = map_bytes(rows, N, ccc::kBwdChunk);
@@ -317,9 +319,10 @@ int ccc_bwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
         a.map = map;
         pdl = true;
     }
-    a.slabs = ccc::slabs_of(C, ccc::kBwdVec);
+    a.slabs = ccc::bwd_columns(C);
     a.runs = ccc::bwd_runs(rows, N, C);
-    if (ccc::launch_bwd(a, pdl, st) != cudaSuccess) return CCC_ERR_CUDA;
+    if ((ccc::kBwdTma ? ccc::launch_bwd_tma(a, pdl, st) : ccc::launch_bwd(a, pdl, st)) != cudaSuccess)
+        return CCC_ERR_CUDA;
     ++launches;
     if (ccc::launch_reduce(a.part, a.runs, C, dweight, dbias, true, st) != cudaSuccess) return CCC_ERR_CUDA;
     ++launches;

@@ -42,21 +42,6 @@ namespace ccc {
 
 namespace {
 
-// dz = dy * s * (1 + z * (1 - s)), s = sigmoid(z), for the recomputed
-// pre-activation z = b + w0 h0 + w1 h1 + w2 h2 + w3 hc (bias first, then the
-// four FMAs in tap order, exactly as the forward).
-__device__ __forceinline__ float2 silu_grad(float2 b, float2 w0, float2 w1, float2 w2, float2 w3, float2 h0,
-                                            float2 h1, float2 h2, float2 hc, float2 gy) {
-    float2 z = __ffma2_rn(w0, h0, b);
-    z = __ffma2_rn(w1, h1, z);
-    z = __ffma2_rn(w2, h2, z);
-    z = __ffma2_rn(w3, hc, z);
-    const float2 s = sigmoid2(z);
-    const float2 oms = __fadd2_rn(make_float2(1.0f, 1.0f), make_float2(-s.x, -s.y));
-    const float2 f = __ffma2_rn(z, oms, make_float2(1.0f, 1.0f));
-    return __fmul2_rn(gy, __fmul2_rn(s, f));
-}
-
 // P = 0: each lane loads its U rows of x and dy straight into registers.
 // P > 0: each lane streams the rows of its walk through a P-stage ring of
 // U-row batches in shared memory (cp.async), keeping up to P-1 batches in
@@ -74,6 +59,7 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
     const int slab = gw % a.slabs, run = gw / a.slabs;
     const int cv = slab * 32 + lane;
     const bool act = cv < a.C / VEC;
+    const bool full = (slab + 1) * 32 * VEC <= a.C;  // warp-uniform: all lanes have channels
     const int c0 = act ? cv * VEC : 0;
 
     float2 w0[NV], w1[NV], w2[NV], w3[NV], bb[NV];
@@ -113,7 +99,7 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
     const unsigned char *ring_p = dyn_smem + warp * RING_WARP + lane * VB;
     int p_row = 0, p_end = 0, issued = 0, consumed = 0;
     auto issue = [&]() {
-        const int st = issued % P;
+        const int st = issued % (P > 0 ? P : 1);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int row = p_row + u;
@@ -202,16 +188,27 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
             // this item's tokens and emits dx of the row 3 back (no carry:
             // all i < L).  Such batches run guard-free; the first batch of a
             // walk and the tail take the general path.
-            const bool fast = (cont || base >= 3) && base + U <= nload && base + U <= nr;
+            const bool fast = full && (cont || base >= 3) && base + U <= nload && base + U <= nr;
             Raw<NV> xr[U], gr[U];
             if constexpr (P == 0) {
-                const uint16_t *xp = a.x + static_cast<int64_t>(t.r0 + base) * a.xs + c0;
-                const uint16_t *gp = a.dy + static_cast<int64_t>(t.r0 + base) * a.dys + c0;
+                if (fast) {  // all lanes, all rows: unconditional loads, stepping row pointers
+                    const uint16_t *xp = a.x + static_cast<int64_t>(t.r0 + base) * a.xs + c0;
+                    const uint16_t *gp = a.dy + static_cast<int64_t>(t.r0 + base) * a.dys + c0;
 #pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const bool ld = act && (fast || base + u < nload);
-                    xr[u] = ld ? ld_ro<NV>(xp + static_cast<int64_t>(u) * a.xs) : raw_zero<NV>();
-                    gr[u] = ld ? ld_ro<NV>(gp + static_cast<int64_t>(u) * a.dys) : raw_zero<NV>();
+                    for (int u = 0; u < U; ++u) {
+                        xr[u] = ld_ro<NV>(xp);
+                        gr[u] = ld_ro<NV>(gp);
+                        xp += a.xs;
+                        gp += a.dys;
+                    }
+                } else {
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const bool ld = act && base + u < nload;
+                        const int row = t.r0 + base + u;
+                        xr[u] = ld ? ld_ro<NV>(a.x + static_cast<int64_t>(row) * a.xs + c0) : raw_zero<NV>();
+                        gr[u] = ld ? ld_ro<NV>(a.dy + static_cast<int64_t>(row) * a.dys + c0) : raw_zero<NV>();
+                    }
                 }
             } else {
                 if (base < nload) {  // the next batch of the walk (zero-filled past p_end)
@@ -258,7 +255,8 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
                         h1[v] = h2[v];
                         h2[v] = hc[v];
                     }
-                    if (act) st_stream<NV>(dxp + static_cast<int64_t>(u) * a.dxs, o);
+                    st_stream<NV>(dxp, o);
+                    dxp += a.dxs;
                 }
                 continue;
             }

@@ -28,6 +28,10 @@ __device__ __forceinline__ int row_clamp(int v, int64_t rows) {
     return v < 0 ? 0 : (v > rows ? static_cast<int>(rows) : v);
 }
 
+// Offsets of up to kSmemSeqs sequences are staged in shared memory with one
+// coalesced pass, so the scan and the item writes read no global memory.
+constexpr int kSmemSeqs = 8192;
+
 __global__ void __launch_bounds__(kMapThreads) chunkmap_kernel(const int32_t *__restrict__ cu, int N,
                                                                int64_t rows, int B, int empty_items,
                                                                int32_t *__restrict__ map, int cap) {
@@ -36,12 +40,20 @@ __global__ void __launch_bounds__(kMapThreads) chunkmap_kernel(const int32_t *__
     grid_dependents_launch();
 
     __shared__ int warp_tot[32];
+    __shared__ int s_cu[kSmemSeqs + 1];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool staged = N <= kSmemSeqs;
+    if (staged) {
+        for (int i = tid; i <= N; i += kMapThreads) s_cu[i] = row_clamp(__ldg(cu + i), rows);
+        __syncthreads();
+    }
+    auto off_of = [&](int n) { return staged ? s_cu[n] : row_clamp(__ldg(cu + n), rows); };
+
     const int per = (N + kMapThreads - 1) / kMapThreads;
     const int n0 = min(tid * per, N), n1 = min(n0 + per, N);
 
     auto items_of = [&](int n) {
-        int s = row_clamp(__ldg(cu + n), rows), e = row_clamp(__ldg(cu + n + 1), rows);
+        const int s = off_of(n), e = off_of(n + 1);
         const int len = e > s ? e - s : 0;
         int ni = (len + B - 1) / B;
         if (empty_items && ni == 0) ni = 1;
@@ -78,7 +90,7 @@ __global__ void __launch_bounds__(kMapThreads) chunkmap_kernel(const int32_t *__
         int off = __shfl_sync(kFull, base, owner);
         const int on0 = __shfl_sync(kFull, n0, owner), on1 = __shfl_sync(kFull, n1, owner);
         for (int n = on0; n < on1; ++n) {
-            const int s = row_clamp(__ldg(cu + n), rows);
+            const int s = off_of(n);
             const int ni = items_of(n);
             for (int i = lane; i < ni; i += 32) {
                 const int idx = off + i;

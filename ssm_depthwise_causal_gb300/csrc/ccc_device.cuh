@@ -183,6 +183,23 @@ __device__ __forceinline__ float2 sigmoid2(float2 z) {
 
 __device__ __forceinline__ float2 f2_zero() { return make_float2(0.0f, 0.0f); }
 
+// dz = dy * s * (1 + z * (1 - s)), s = sigmoid(z), for the recomputed
+// pre-activation z = b + w0 h0 + w1 h1 + w2 h2 + w3 hc (bias first, then the
+// four FMAs in tap order, exactly as the forward).
+__device__ __forceinline__ float2 silu_grad(float2 b, float2 w0, float2 w1, float2 w2, float2 w3, float2 h0,
+                                            float2 h1, float2 h2, float2 hc, float2 gy) {
+    float2 z = __ffma2_rn(w0, h0, b);
+    z = __ffma2_rn(w1, h1, z);
+    z = __ffma2_rn(w2, h2, z);
+    z = __ffma2_rn(w3, hc, z);
+    const float2 s = sigmoid2(z);
+    const float2 one = make_float2(1.0f, 1.0f);
+    const float2 oms = __ffma2_rn(s, make_float2(-1.0f, -1.0f), one);  // 1 - s
+    const float2 f = __ffma2_rn(z, oms, one);
+    return __fmul2_rn(gy, __fmul2_rn(s, f));
+}
+
+
 // ------------------------------------------------------ taps and bias --
 
 // Weights [C][4] FP32 or BF16 and bias [C] FP32 / BF16 / none, read once per
@@ -319,6 +336,62 @@ struct ItemDecoder {
         return t;
     }
 };
+
+// ------------------------------------------------ mbarrier + bulk copies --
+//
+// Shared-memory mbarriers (PTX mbarrier.*) and the bulk-copy engine
+// (cp.async.bulk, global -> shared, completion counted in bytes on an
+// mbarrier).  Every wait is bounded: after kSpinLimit polls (each one a
+// try_wait that may suspend for up to kSuspendNs) it gives up and returns
+// false, so a broken handshake ends the kernel instead of hanging the GPU.
+
+constexpr int kSpinLimit = 1 << 22;
+constexpr uint32_t kSuspendNs = 1000;
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Make initialised barriers visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// true once the barrier phase with this parity has completed.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(kSuspendNs)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    for (int i = 0; i < kSpinLimit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// One bulk copy global -> shared; `bytes` and both addresses are multiples of
+// 16.  Completion is reported to `bar` as `bytes` transaction bytes.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
 
 // ------------------------------------------------- programmatic launch --
 

@@ -71,6 +71,17 @@ __device__ __forceinline__ void scatter_state(const FwdArgs &a, int q, int c0, c
     }
 }
 
+// SiLU(z) for z = b + w0 h0 + w1 h1 + w2 h2 + w3 hc (bias first, then the four
+// FMAs in tap order), on a pair of channels.
+__device__ __forceinline__ float2 silu_pre(float2 b, float2 w0, float2 w1, float2 w2, float2 w3, float2 h0,
+                                           float2 h1, float2 h2, float2 hc) {
+    float2 z = __ffma2_rn(w0, h0, b);
+    z = __ffma2_rn(w1, h1, z);
+    z = __ffma2_rn(w2, h2, z);
+    z = __ffma2_rn(w3, hc, z);
+    return __fmul2_rn(z, sigmoid2(z));
+}
+
 template <int VEC, int U>
 __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const FwdArgs a) {
     constexpr int NV = VEC / 2;
@@ -80,6 +91,7 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
     const int slab = gw % a.slabs, run = gw / a.slabs;
     const int cv = slab * 32 + lane;
     const bool act = cv < a.C / VEC;
+    const bool full = (slab + 1) * 32 * VEC <= a.C;  // warp-uniform: all lanes have channels
     const int c0 = act ? cv * VEC : 0;
 
     float2 w0[NV], w1[NV], w2[NV], w3[NV], bb[NV];
@@ -145,7 +157,38 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
             unpack<NV>(hr[2], h2);
         }
 
-        for (int base = 0; base < nr; base += U) {
+        int base = 0;
+        if (full) {
+            // Every lane active and the batch inside the item: no guards.
+            const uint16_t *xp = xrow;
+            uint16_t *op = orow;
+            for (; base + U <= nr; base += U) {
+                Raw<NV> cur[U];
+                const uint16_t *lp = xp;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    cur[u] = ld_ro<NV>(lp);
+                    lp += a.xs;
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    float2 hc[NV];
+                    unpack<NV>(cur[u], hc);
+                    Raw<NV> y;
+#pragma unroll
+                    for (int v = 0; v < NV; ++v) {
+                        y.u[v] = f2_to_bf2(silu_pre(bb[v], w0[v], w1[v], w2[v], w3[v], h0[v], h1[v], h2[v], hc[v]));
+                        h0[v] = h1[v];
+                        h1[v] = h2[v];
+                        h2[v] = hc[v];
+                    }
+                    st_stream<NV>(op, y);
+                    op += a.os;
+                }
+                xp = lp;
+            }
+        }
+        for (; base < nr; base += U) {  // remainder, or a partly filled slab
             Raw<NV> cur[U];
 #pragma unroll
             for (int u = 0; u < U; ++u)
@@ -159,12 +202,7 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
                 Raw<NV> y;
 #pragma unroll
                 for (int v = 0; v < NV; ++v) {
-                    float2 z = bb[v];
-                    z = __ffma2_rn(w0[v], h0[v], z);
-                    z = __ffma2_rn(w1[v], h1[v], z);
-                    z = __ffma2_rn(w2[v], h2[v], z);
-                    z = __ffma2_rn(w3[v], hc[v], z);
-                    y.u[v] = f2_to_bf2(__fmul2_rn(z, sigmoid2(z)));
+                    y.u[v] = f2_to_bf2(silu_pre(bb[v], w0[v], w1[v], w2[v], w3[v], h0[v], h1[v], h2[v], hc[v]));
                     h0[v] = h1[v];
                     h1[v] = h2[v];
                     h2[v] = hc[v];

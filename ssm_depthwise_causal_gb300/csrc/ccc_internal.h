@@ -40,6 +40,21 @@ namespace ccc {
 #ifndef CCC_BWD_RING
 #define CCC_BWD_RING 0
 #endif
+#ifndef CCC_BWD_TMA
+#define CCC_BWD_TMA 0
+#endif
+#ifndef CCC_BWD_TMA_WARPS
+#define CCC_BWD_TMA_WARPS 4
+#endif
+#ifndef CCC_BWD_TMA_ROWS
+#define CCC_BWD_TMA_ROWS 16
+#endif
+#ifndef CCC_BWD_TMA_STAGES
+#define CCC_BWD_TMA_STAGES 3
+#endif
+#ifndef CCC_BWD_TMA_MIN_BLOCKS
+#define CCC_BWD_TMA_MIN_BLOCKS 2
+#endif
 
 // Rows per work item.  Long enough that the 3-row halo an item re-reads
 // (forward: left; backward: left and right) is a few percent of its rows and
@@ -63,6 +78,14 @@ constexpr int kBwdMinBlocks = CCC_BWD_MIN_BLOCKS;
 // Backward: stages of the per-lane shared-memory ring (0 = load rows
 // straight into registers).
 constexpr int kBwdRing = CCC_BWD_RING;
+// Backward fed by a bulk-copy producer warp (ccc_bwd_tma.cu): consumer
+// warps per CTA (128 channels each), rows per shared-memory stage, stages,
+// resident CTAs per SM.
+constexpr bool kBwdTma = CCC_BWD_TMA != 0;
+constexpr int kBwdTmaWarps = CCC_BWD_TMA_WARPS;
+constexpr int kBwdTmaRows = CCC_BWD_TMA_ROWS;
+constexpr int kBwdTmaStages = CCC_BWD_TMA_STAGES;
+constexpr int kBwdTmaMinBlocks = CCC_BWD_TMA_MIN_BLOCKS;
 // Backward warps the work split is sized for: 152 SMs x 2 resident CTAs x 8
 // warps, i.e. one full wave on GB300.  Fixed, not queried, so the reduction
 // order -- and with it every bit of dweight / dbias -- depends only on
@@ -80,7 +103,7 @@ struct FwdArgs {
     const uint16_t *x;
     int64_t rows;
     int C;
-    int64_t xs;
+    int xs;  // row strides in elements (host-checked < 2^31)
     const void *w;
     int w_bf16;
     const void *b;
@@ -94,7 +117,7 @@ struct FwdArgs {
     const int32_t *cache;
     const uint8_t *has_init;
     uint16_t *out;
-    int64_t os;
+    int os;
     uint16_t *hist;
     const int32_t *map;  // nullptr: items derived in-kernel
     int cap;
@@ -105,7 +128,7 @@ struct BwdArgs {
     const uint16_t *x;
     int64_t rows;
     int C;
-    int64_t xs;
+    int xs;  // row strides in elements (host-checked < 2^31)
     const void *w;
     int w_bf16;
     const void *b;
@@ -116,10 +139,10 @@ struct BwdArgs {
     const int32_t *cache;
     const uint8_t *has_init;
     const uint16_t *dy;
-    int64_t dys;
+    int dys;
     const float *d_final;
     uint16_t *dx;
-    int64_t dxs;
+    int dxs;
     float *d_init;
     float *part;  // [runs][5][C]
     const int32_t *map;
@@ -143,15 +166,22 @@ inline int runs_per_slab(int64_t target_warps, int slabs, int64_t cap) {
     return static_cast<int>(r < 1 ? 1 : r);
 }
 
-// Backward runs per slab; also the number of FP32 partial rows per channel.
+// Backward task split: `slabs` task columns (a slab of 32*VEC channels per
+// warp, or a column of kBwdTmaWarps*128 channels per CTA for the bulk-copy
+// kernel) times `runs` runs per column; runs is also the number of FP32
+// partial rows per channel.  Both depend only on (rows, N, C).
+inline int bwd_columns(int C) { return kBwdTma ? static_cast<int>(ceil_div(C, kBwdTmaWarps * 128)) : slabs_of(C, kBwdVec); }
+
 inline int bwd_runs(int64_t rows, int N, int C) {
-    return runs_per_slab(kBwdTargetWarps, slabs_of(C, kBwdVec), item_capacity(rows, N, kBwdChunk));
+    const int64_t target = kBwdTma ? int64_t{152} * kBwdTmaMinBlocks : kBwdTargetWarps;
+    return runs_per_slab(target, bwd_columns(C), item_capacity(rows, N, kBwdChunk));
 }
 
 cudaError_t launch_chunkmap(const int32_t *cu, int N, int64_t rows, int B, int empty_items,
                             int32_t *map, int cap, cudaStream_t st);
 cudaError_t launch_fwd(const FwdArgs &a, bool pdl, cudaStream_t st);
 cudaError_t launch_bwd(const BwdArgs &a, bool pdl, cudaStream_t st);
+cudaError_t launch_bwd_tma(const BwdArgs &a, bool pdl, cudaStream_t st);
 // Resident forward CTAs per SM on the current device (occupancy query).
 int fwd_ctas_per_sm();
 cudaError_t launch_reduce(const float *part, int G, int C, float *dweight, float *dbias,
