@@ -15,8 +15,10 @@ Entry points (same names as the C ABI):
 * ``ccc_bwd(...)``  -- fused dx + deterministic FP32 dweight/dbias
   (``cake_causal_conv1d_kcp``, Returns)
 
-and the allocating conveniences ``causal_conv1d_fn`` / ``causal_conv1d_bwd``,
-which create ``out`` / ``dx`` / the workspace when they are not given.
+the allocating conveniences ``causal_conv1d_fn`` / ``causal_conv1d_bwd``,
+which create ``out`` / ``dx`` / the workspace when they are not given,
+``recompute_fwd`` (bitwise re-run of a forward from its saved history) and the
+autograd wrapper ``causal_conv1d`` / ``CausalConv1dFn``.
 """
 from __future__ import annotations
 
@@ -31,7 +33,7 @@ from . import _lib
 CCC_F32, CCC_BF16, CCC_NONE = 0, 1, -1
 
 __all__ = ["ccc_workspace_size", "ccc_fwd", "ccc_bwd", "ccc_bwd_noalloc", "causal_conv1d_fn",
-           "causal_conv1d_bwd",
+           "causal_conv1d_bwd", "recompute_fwd", "CausalConv1dFn", "causal_conv1d",
            "CCCError", "library_path", "last_launch_count"]
 
 
@@ -193,3 +195,75 @@ def causal_conv1d_bwd(x, weight, dy, cu_seqlens, *, bias=None, saved_hist=None,
     ccc_bwd(x, weight, bias, saved_hist, cu_seqlens, cache_indices, has_initial_state, dy,
             d_final_state, dx, dweight, dbias, d_init, workspace, stream)
     return dx, dweight, dbias, d_init
+
+
+def recompute_fwd(x, weight, saved_hist, cu_seqlens, cache_indices=None, *, bias=None, out=None,
+                  workspace=None, stream=None) -> torch.Tensor:
+    """Re-run the forward from the history a previous ccc_fwd saved.
+
+    ``saved_hist`` [N, 3, C] is read as a pool of N slots (slot n = sequence
+    n, positions along dim 1), so the recomputed output is bit for bit the
+    original one even though the real conv_state was updated in place since
+    (the checkpoint recompute of ``cake_causal_conv1d_kcp``, recompute_handle).
+    ``saved_hist`` itself is not modified: the final state is written into a
+    scratch copy."""
+    x2, rows, C, _ = _rows_view(x, "x")
+    N = cu_seqlens.numel() - 1
+    pool = saved_hist.clone().transpose(1, 2)     # [N, C, 3] view, channel axis contiguous
+    slots = torch.arange(N, dtype=torch.int32, device=x.device)
+    if cache_indices is not None:  # -1 requests stay -1 (zero output)
+        slots = torch.where(cache_indices == -1, cache_indices, slots)
+    every = torch.ones(N, dtype=torch.bool, device=x.device)
+    return causal_conv1d_fn(x, weight, pool, cu_seqlens, slots, every, bias=bias, out=out,
+                            workspace=workspace, stream=stream)
+
+
+class CausalConv1dFn(torch.autograd.Function):
+    """Autograd wrapper: forward = ccc_fwd (saving the initial history),
+    backward = ccc_bwd.  The backward recomputes the pre-activations from x
+    and the saved history, so nothing of the forward output is kept.
+
+    Gradients flow to x, weight and bias; conv_state is an in-place
+    serving buffer and gets none (use ccc_bwd's d_init_state /
+    d_final_state directly to chain fragments)."""
+
+    @staticmethod
+    def forward(ctx, x, weight, bias, cu_seqlens, conv_state, cache_indices, has_initial_state):
+        x2, rows, C, _ = _rows_view(x, "x")
+        N = cu_seqlens.numel() - 1
+        hist = torch.empty((N, 3, C), dtype=torch.bfloat16, device=x.device)
+        out = causal_conv1d_fn(x, weight, conv_state, cu_seqlens, cache_indices, has_initial_state,
+                               bias=bias, saved_hist=hist)
+        ctx.save_for_backward(x, weight, bias if bias is not None else torch.empty(0, device=x.device),
+                              cu_seqlens, hist,
+                              cache_indices if cache_indices is not None else torch.empty(0, device=x.device),
+                              has_initial_state if has_initial_state is not None else
+                              torch.empty(0, device=x.device))
+        ctx.has_bias = bias is not None
+        ctx.has_cache = cache_indices is not None
+        ctx.has_init = has_initial_state is not None
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        x, weight, bias, cu_seqlens, hist, cache, has_init = ctx.saved_tensors
+        bias = bias if ctx.has_bias else None
+        cache = cache if ctx.has_cache else None
+        has_init = has_init if ctx.has_init else None
+        dout = dout.contiguous() if dout.stride(-1) != 1 else dout
+        # rows past cu_seqlens[-1] are not written by the kernel: start from 0
+        dx = torch.zeros_like(x)
+        dx, dw, db, _ = causal_conv1d_bwd(x, weight, dout, cu_seqlens, bias=bias, saved_hist=hist,
+                                          cache_indices=cache, has_initial_state=has_init, dx=dx)
+        dw = dw.to(weight.dtype)
+        db = None if db is None else db.to(bias.dtype)
+        return dx, dw, db, None, None, None, None
+
+
+def causal_conv1d(x, weight, bias=None, cu_seqlens=None, conv_state=None, cache_indices=None,
+                  has_initial_state=None) -> torch.Tensor:
+    """Differentiable packed causal Conv1d + SiLU (see CausalConv1dFn)."""
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, x.shape[-2]], dtype=torch.int32, device=x.device)
+    return CausalConv1dFn.apply(x, weight, bias, cu_seqlens, conv_state, cache_indices,
+                                has_initial_state)

@@ -156,6 +156,69 @@ __device__ __forceinline__ Raw<NV> ld_shared(const unsigned char *p) {
     return r;
 }
 
+// Per-lane ring over a contiguous row stream [S0, S1) of NT tensors: stage k
+// holds rows S0 + k*U .. S0 + k*U + U-1 (zero-filled past S1) in slot k % P.
+// Each lane copies -- and later reads -- only its own VB bytes of a row, so
+// in-order completion of its cp.async groups is all the synchronisation
+// needed: no barrier, no cross-lane wait.  `src[t]` points at the lane's
+// bytes of row 0 of tensor t, `stride[t]` is that tensor's row stride in
+// elements.  Shared layout per warp: [P][U][NT][32 lanes][VB].
+template <int NV, int U, int P, int NT>
+struct LaneRing {
+    static constexpr int VB = NV * 4;
+    static constexpr int kWarpBytes = P * U * NT * 32 * VB;
+    uint32_t base;  // shared address of this lane's bytes in stage 0, row 0, tensor 0
+    int S0, S1;
+    int issued;     // stages issued so far
+    const uint16_t *src[NT];
+    int stride[NT];
+
+    __device__ __forceinline__ void start(int s0, int s1) {
+        cp_async_wait(0);  // nothing of a previous stream may still land
+        S0 = s0;
+        S1 = s1;
+        issued = 0;
+    }
+
+    __device__ __forceinline__ void issue(bool act) {
+        const int slot = issued % P;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int r = S0 + issued * U + u;
+            const bool ok = act && r < S1;
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                const uint32_t dst = base + static_cast<uint32_t>(((slot * U + u) * NT + t) * 32 * VB);
+                cp_async<VB>(dst, ok ? src[t] + static_cast<int64_t>(r) * stride[t] : src[t], ok);
+            }
+        }
+        cp_async_commit();
+        ++issued;
+    }
+
+    // Keep the stages from the one holding row r on issued, P deep.
+    __device__ __forceinline__ void top_up(int r, bool act) {
+        const int k = (r - S0) / U;
+        while (issued < k + P && S0 + issued * U < S1) issue(act);
+    }
+
+    // Row r of tensor t (r in [S0, S1), stage already issued).
+    __device__ __forceinline__ Raw<NV> get(int r, int t) const {
+        const int j = r - S0, k = j / U;
+        cp_async_wait(issued - 1 - k);
+        const uint32_t addr = base + static_cast<uint32_t>((((k % P) * U + j % U) * NT + t) * 32 * VB);
+        Raw<NV> v;
+        if constexpr (NV == 4) {
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v.u[0]), "=r"(v.u[1]), "=r"(v.u[2]), "=r"(v.u[3])
+                         : "r"(addr));
+        } else {
+            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.u[0]), "=r"(v.u[1]) : "r"(addr));
+        }
+        return v;
+    }
+};
+
 // ------------------------------------------------------------------ math --
 
 // Documented PTX approximations (PTX ISA: ex2.approx.ftz.f32, rcp.approx.ftz.f32).

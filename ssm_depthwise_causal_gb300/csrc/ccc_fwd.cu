@@ -82,9 +82,13 @@ __device__ __forceinline__ float2 silu_pre(float2 b, float2 w0, float2 w1, float
     return __fmul2_rn(z, sigmoid2(z));
 }
 
-template <int VEC, int U>
+// P = 0: rows are loaded straight into registers, U per batch.  P > 0: each
+// lane streams its run's rows through a P-stage shared-memory ring
+// (LaneRing, cp.async), so loads run ahead of the math.
+template <int VEC, int U, int P>
 __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const FwdArgs a) {
     constexpr int NV = VEC / 2;
+    extern __shared__ __align__(16) unsigned char fwd_smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int gw = blockIdx.x * kWarpsPerCta + warp;  // this warp's task
     if (gw >= a.slabs * a.runs) return;               // (whole warp) no task in the last CTA
@@ -108,6 +112,23 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
 
     float2 h0[NV], h1[NV], h2[NV];  // the three rows before the current one
     int prev_n = -1, prev_end = -1;
+
+    using Ring = LaneRing<NV, U, (P > 0 ? P : 1), 1>;
+    Ring ring;
+    if constexpr (P > 0) {
+        ring.base = smem_addr(fwd_smem + warp * Ring::kWarpBytes) + lane * Ring::VB;
+        ring.src[0] = a.x + c0;
+        ring.stride[0] = a.xs;
+        if (lo < hi) {
+            // The run's rows: from its first item (and the 3 rows before it
+            // when it starts inside a sequence) to the end of its last item.
+            const Item f = dec.get(lo, a.map, a.cu, a.rows);
+            const Item l = dec.get(hi - 1, a.map, a.cu, a.rows);
+            ring.start(f.r0 > f.s ? f.r0 - 3 : f.r0, l.r0 + l.nr);
+        } else {
+            ring.start(0, 0);
+        }
+    }
 
     for (int it = lo; it < hi; ++it) {
         const Item t = dec.get(it, a.map, a.cu, a.rows);
@@ -148,6 +169,10 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
 #pragma unroll
                     for (int p = 0; p < 3; ++p)
                         st_plain<NV>(a.hist + (static_cast<int64_t>(t.n) * 3 + p) * a.C + c0, hr[p]);
+            } else if constexpr (P > 0) {
+                ring.top_up(t.r0 - 3, act);
+#pragma unroll
+                for (int p = 0; p < 3; ++p) hr[p] = ring.get(t.r0 - 3 + p, 0);
             } else if (act) {
 #pragma unroll
                 for (int p = 0; p < 3; ++p) hr[p] = ld_ro<NV>(xrow - static_cast<int64_t>(3 - p) * a.xs);
@@ -158,7 +183,30 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
         }
 
         int base = 0;
-        if (full) {
+        if constexpr (P > 0) {
+            for (; base < nr; base += U) {
+                ring.top_up(t.r0 + base, act);
+                Raw<NV> cur[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) cur[u] = base + u < nr ? ring.get(t.r0 + base + u, 0) : raw_zero<NV>();
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    if (base + u >= nr) break;
+                    float2 hc[NV];
+                    unpack<NV>(cur[u], hc);
+                    Raw<NV> y;
+#pragma unroll
+                    for (int v = 0; v < NV; ++v) {
+                        y.u[v] = f2_to_bf2(silu_pre(bb[v], w0[v], w1[v], w2[v], w3[v], h0[v], h1[v], h2[v], hc[v]));
+                        h0[v] = h1[v];
+                        h1[v] = h2[v];
+                        h2[v] = hc[v];
+                    }
+                    if (act) st_stream<NV>(orow + static_cast<int64_t>(base + u) * a.os, y);
+                }
+            }
+        }
+        if (full && P == 0) {
             // Every lane active and the batch inside the item: no guards.
             const uint16_t *xp = xrow;
             uint16_t *op = orow;
@@ -235,10 +283,30 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
 
 }  // namespace
 
+constexpr size_t kFwdRingBytes =
+    kFwdRing > 0 ? static_cast<size_t>(LaneRing<kFwdVec / 2, kFwdUnroll, (kFwdRing > 0 ? kFwdRing : 1), 1>::kWarpBytes) *
+                       kWarpsPerCta
+                 : 0;
+
+// Opt in to more than 48 KB of dynamic shared memory, once per device.
+cudaError_t fwd_prepare() {
+    if (kFwdRingBytes <= 48 * 1024) return cudaSuccess;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && attr_set[dev]) return cudaSuccess;
+    e = cudaFuncSetAttribute(fwd_kernel<kFwdVec, kFwdUnroll, kFwdRing>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kFwdRingBytes));
+    if (e == cudaSuccess && dev >= 0 && dev < 64) attr_set[dev] = true;
+    return e;
+}
+
 int fwd_ctas_per_sm() {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_kernel<kFwdVec, kFwdUnroll>, kCtaThreads, 0) !=
-            cudaSuccess ||
+    if (fwd_prepare() != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_kernel<kFwdVec, kFwdUnroll, kFwdRing>, kCtaThreads,
+                                                      kFwdRingBytes) != cudaSuccess ||
         n < 1)
         n = kFwdMinBlocks;
     return n;
@@ -248,7 +316,9 @@ cudaError_t launch_fwd(const FwdArgs &a, bool pdl, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(static_cast<int64_t>(a.slabs) * a.runs, kWarpsPerCta)));
     cfg.blockDim = dim3(kCtaThreads);
+    cfg.dynamicSmemBytes = kFwdRingBytes;
     cfg.stream = st;
+    if (const cudaError_t e = fwd_prepare(); e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
     if (pdl) {
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -256,7 +326,7 @@ cudaError_t launch_fwd(const FwdArgs &a, bool pdl, cudaStream_t st) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, fwd_kernel<kFwdVec, kFwdUnroll>, a);
+    return cudaLaunchKernelEx(&cfg, fwd_kernel<kFwdVec, kFwdUnroll, kFwdRing>, a);
 }
 
 }  // namespace ccc

@@ -20,7 +20,7 @@ namespace ccc {
 #define CCC_FWD_VEC 8
 #endif
 #ifndef CCC_BWD_VEC
-#define CCC_BWD_VEC 4
+#define CCC_BWD_VEC 8
 #endif
 #ifndef CCC_FWD_UNROLL
 #define CCC_FWD_UNROLL 8
@@ -32,16 +32,19 @@ namespace ccc {
 #define CCC_FWD_MIN_BLOCKS 2
 #endif
 #ifndef CCC_BWD_MIN_BLOCKS
-#define CCC_BWD_MIN_BLOCKS 2
+#define CCC_BWD_MIN_BLOCKS 1
 #endif
 #ifndef CCC_BWD_TARGET_WARPS
-#define CCC_BWD_TARGET_WARPS 2432
+#define CCC_BWD_TARGET_WARPS 1216
 #endif
 #ifndef CCC_BWD_RING
-#define CCC_BWD_RING 0
+#define CCC_BWD_RING 3
 #endif
 #ifndef CCC_BWD_TMA
 #define CCC_BWD_TMA 0
+#endif
+#ifndef CCC_FWD_RING
+#define CCC_FWD_RING 0
 #endif
 #ifndef CCC_BWD_TMA_WARPS
 #define CCC_BWD_TMA_WARPS 4
@@ -64,9 +67,11 @@ constexpr int kFwdChunk = CCC_FWD_CHUNK;
 constexpr int kBwdChunk = CCC_BWD_CHUNK;
 // Above this many sequences the items come from the device chunk map.
 constexpr int kMaxInlineSeqs = 32;
-// Channels per lane (8: one 16-byte vector per row; 4: 8 bytes, which keeps
-// the backward's per-channel state -- taps, windows, partial sums -- within
-// 128 registers).
+// Channels per lane (8: one 16-byte vector per row).  The backward's
+// per-lane state (taps, bias, two sliding windows, five partial sums) then
+// needs ~200 registers, so it runs one 256-thread CTA per SM and takes its
+// memory-level parallelism from the shared-memory ring below instead of from
+// more warps.
 constexpr int kFwdVec = CCC_FWD_VEC;
 constexpr int kBwdVec = CCC_BWD_VEC;
 // Rows loaded ahead per lane before the math (independent loads in flight).
@@ -75,6 +80,9 @@ constexpr int kBwdUnroll = CCC_BWD_UNROLL;
 // Resident CTAs per SM the register budget is sized for.
 constexpr int kFwdMinBlocks = CCC_FWD_MIN_BLOCKS;
 constexpr int kBwdMinBlocks = CCC_BWD_MIN_BLOCKS;
+// Forward: stages of the per-lane shared-memory ring (0 = load rows straight
+// into registers).
+constexpr int kFwdRing = CCC_FWD_RING;
 // Backward: stages of the per-lane shared-memory ring (0 = load rows
 // straight into registers).
 constexpr int kBwdRing = CCC_BWD_RING;
@@ -86,7 +94,7 @@ constexpr int kBwdTmaWarps = CCC_BWD_TMA_WARPS;
 constexpr int kBwdTmaRows = CCC_BWD_TMA_ROWS;
 constexpr int kBwdTmaStages = CCC_BWD_TMA_STAGES;
 constexpr int kBwdTmaMinBlocks = CCC_BWD_TMA_MIN_BLOCKS;
-// Backward warps the work split is sized for: 152 SMs x 2 resident CTAs x 8
+// Backward warps the work split is sized for: 152 SMs x 1 resident CTA x 8
 // warps, i.e. one full wave on GB300.  Fixed, not queried, so the reduction
 // order -- and with it every bit of dweight / dbias -- depends only on
 // (rows, N, C).
