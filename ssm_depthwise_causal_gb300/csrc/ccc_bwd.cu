@@ -91,7 +91,8 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
     // Sliding windows, carried from one item to the next when the next item
     // continues the same sequence: history rows h[i..i+2] and dz_{i-1..i-3}.
     float2 h0[NV], h1[NV], h2[NV], d1[NV], d2[NV], d3[NV];
-    int prev_n = -1, prev_end = -1;
+    Item cur = {};
+    bool live = true, read_state = false;
 
     // Ring state (P > 0): batch b of the current walk holds rows
     // [walk start + b*U, ... + U) of x and dy, in stage b % P.
@@ -114,19 +115,21 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
     };
 
     for (int it = lo; it < hi; ++it) {
-        const Item t = dec.get(it, a.map, a.cu, a.rows);
-        bool next_cont = false;
-        if (it + 1 < hi) {
-            int nn, nr0;
-            dec.head(it + 1, a.map, nn, nr0);
-            next_cont = nn == t.n && nr0 == t.r0 + t.nr;
+        // The next item of the same sequence is the next B rows: only a new
+        // sequence needs the chunk map / offsets (and its flags) again.
+        const bool cont = it > lo && cur.r0 + cur.nr < cur.e;
+        if (cont) {
+            cur.r0 += cur.nr;
+            cur.nr = min(kBwdChunk, cur.e - cur.r0);
+        } else {
+            cur = dec.get(it, a.map, a.cu, a.rows);
+            live = !(a.cache && __ldg(a.cache + cur.n) == -1);
+            read_state = a.has_init != nullptr && __ldg(a.has_init + cur.n) != 0;
         }
-        const bool cont = t.n == prev_n && t.r0 == prev_end;
-        prev_n = t.n;
-        prev_end = t.r0 + t.nr;
+        const Item t = cur;
+        const bool next_cont = it + 1 < hi && t.r0 + t.nr < t.e;
         const int nr = t.nr;
         const int o0 = t.r0 - t.s, L = t.e - t.s;
-        const bool live = !(a.cache && __ldg(a.cache + t.n) == -1);
         float *dinit = a.d_init ? a.d_init + static_cast<int64_t>(t.n) * 3 * a.C + c0 : nullptr;
 
         if (!live || L == 0) {  // zero gradient, no contribution
@@ -142,7 +145,6 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
             }
             continue;
         }
-        const bool read_state = a.has_init != nullptr && __ldg(a.has_init + t.n) != 0;
 
         if constexpr (P > 0) {
             if (!cont) {

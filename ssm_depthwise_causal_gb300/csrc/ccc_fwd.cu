@@ -111,7 +111,6 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
     const int hi = static_cast<int>(static_cast<int64_t>(run + 1) * dec.total / a.runs);
 
     float2 h0[NV], h1[NV], h2[NV];  // the three rows before the current one
-    int prev_n = -1, prev_end = -1;
 
     using Ring = LaneRing<NV, U, (P > 0 ? P : 1), 1>;
     Ring ring;
@@ -130,19 +129,28 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
         }
     }
 
+    Item cur = {};
+    int q = -2;
+    bool has_init_n = false;
     for (int it = lo; it < hi; ++it) {
-        const Item t = dec.get(it, a.map, a.cu, a.rows);
-        const bool cont = t.n == prev_n && t.r0 == prev_end;  // window carried over
-        prev_n = t.n;
-        prev_end = t.r0 + t.nr;
+        // The next item of the same sequence is the next B rows: only a new
+        // sequence needs the chunk map / offsets (and its slot) again.
+        const bool cont = it > lo && cur.r0 + cur.nr < cur.e;
+        if (cont) {
+            cur.r0 += cur.nr;
+            cur.nr = min(kFwdChunk, cur.e - cur.r0);
+        } else {
+            cur = dec.get(it, a.map, a.cu, a.rows);
+            q = a.cache ? __ldg(a.cache + cur.n) : -2;
+            has_init_n = a.has_init != nullptr && __ldg(a.has_init + cur.n) != 0;
+        }
+        const Item t = cur;
         const int nr = t.nr;
         if (nr <= 0) continue;
         const int o0 = t.r0 - t.s, L = t.e - t.s;
         const uint16_t *xrow = a.x + static_cast<int64_t>(t.r0) * a.xs + c0;
         uint16_t *orow = a.out + static_cast<int64_t>(t.r0) * a.os + c0;
 
-        int q = -2;
-        if (a.cache) q = __ldg(a.cache + t.n);
         if (q == -1) {  // padded request: zero output, no state access
             if (act) {
                 const Raw<NV> z = raw_zero<NV>();
@@ -155,7 +163,7 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
             continue;
         }
         const bool pool = a.state != nullptr && q >= 0 && q < a.n_slots;
-        const bool rd = o0 == 0 && pool && a.has_init != nullptr && __ldg(a.has_init + t.n) != 0;
+        const bool rd = o0 == 0 && pool && has_init_n;
 
         if (!cont) {
             // The three history rows before r0 (raw BF16 bits): the initial
