@@ -100,6 +100,15 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
     const unsigned char *ring_p = dyn_smem + warp * RING_WARP + lane * VB;
     int p_row = 0, p_end = 0, issued = 0, consumed = 0;
     auto issue = [&]() {
+        if constexpr (kBwdPrefetch > 0) {
+            // lanes 0..2U-1: the warp's slab of x / dy rows PF ahead into L2
+            const int pr = p_row + kBwdPrefetch + (lane >> 1);
+            if (full && lane < 2 * U && pr < p_end) {
+                const uint16_t *base_ptr = (lane & 1) ? a.dy + static_cast<int64_t>(pr) * a.dys
+                                                      : a.x + static_cast<int64_t>(pr) * a.xs;
+                prefetch_l2(base_ptr + slab * 32 * VEC, 32 * VEC * 2);
+            }
+        }
         const int st = issued % (P > 0 ? P : 1);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -194,6 +203,15 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
             Raw<NV> xr[U], gr[U];
             if constexpr (P == 0) {
                 if (fast) {  // all lanes, all rows: unconditional loads, stepping row pointers
+                    if constexpr (kBwdPrefetch > 0) {
+                        // lanes 0..2U-1: the warp's slab of x / dy rows PF ahead into L2
+                        const int pr = t.r0 + base + kBwdPrefetch + (lane >> 1);
+                        if (lane < 2 * U && pr < t.e) {
+                            const uint16_t *pp = (lane & 1) ? a.dy + static_cast<int64_t>(pr) * a.dys
+                                                            : a.x + static_cast<int64_t>(pr) * a.xs;
+                            prefetch_l2(pp + slab * 32 * VEC, 32 * VEC * 2);
+                        }
+                    }
                     const uint16_t *xp = a.x + static_cast<int64_t>(t.r0 + base) * a.xs + c0;
                     const uint16_t *gp = a.dy + static_cast<int64_t>(t.r0 + base) * a.dys + c0;
 #pragma unroll

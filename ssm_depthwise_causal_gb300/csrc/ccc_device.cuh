@@ -456,6 +456,12 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
                  : "memory");
 }
 
+// Ask the bulk-copy engine to bring `bytes` (a multiple of 16, 16-byte
+// aligned) into L2; nothing is written to shared memory and nothing waits.
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ------------------------------------------------- programmatic launch --
 
 // Wait until the preceding kernel in the stream has finished and its writes

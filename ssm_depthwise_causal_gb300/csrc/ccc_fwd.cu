@@ -219,6 +219,12 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
             const uint16_t *xp = xrow;
             uint16_t *op = orow;
             for (; base + U <= nr; base += U) {
+                if constexpr (kFwdPrefetch > 0) {
+                    // lanes 0..U-1: the warp's slab of row r0+base+PF+lane into L2
+                    const int pr = t.r0 + base + kFwdPrefetch + lane;
+                    if (lane < U && pr < a.rows)
+                        prefetch_l2(a.x + static_cast<int64_t>(pr) * a.xs + slab * 32 * VEC, 32 * VEC * 2);
+                }
                 Raw<NV> cur[U];
                 const uint16_t *lp = xp;
 #pragma unroll

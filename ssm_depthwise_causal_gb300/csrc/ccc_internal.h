@@ -23,7 +23,7 @@ namespace ccc {
 #define CCC_BWD_VEC 8
 #endif
 #ifndef CCC_FWD_UNROLL
-#define CCC_FWD_UNROLL 8
+#define CCC_FWD_UNROLL 4
 #endif
 #ifndef CCC_BWD_UNROLL
 #define CCC_BWD_UNROLL 4
@@ -45,6 +45,12 @@ namespace ccc {
 #endif
 #ifndef CCC_FWD_RING
 #define CCC_FWD_RING 0
+#endif
+#ifndef CCC_FWD_PREFETCH
+#define CCC_FWD_PREFETCH 4
+#endif
+#ifndef CCC_BWD_PREFETCH
+#define CCC_BWD_PREFETCH 0
 #endif
 #ifndef CCC_BWD_TMA_WARPS
 #define CCC_BWD_TMA_WARPS 4
@@ -83,6 +89,10 @@ constexpr int kBwdMinBlocks = CCC_BWD_MIN_BLOCKS;
 // Forward: stages of the per-lane shared-memory ring (0 = load rows straight
 // into registers).
 constexpr int kFwdRing = CCC_FWD_RING;
+// Rows ahead of the current batch whose slabs the kernels ask to be brought
+// into L2 (cp.async.bulk.prefetch.L2, one row slab per lane); 0 = off.
+constexpr int kFwdPrefetch = CCC_FWD_PREFETCH;
+constexpr int kBwdPrefetch = CCC_BWD_PREFETCH;
 // Backward: stages of the per-lane shared-memory ring (0 = load rows
 // straight into registers).
 constexpr int kBwdRing = CCC_BWD_RING;
