@@ -159,12 +159,17 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- traffic --
 
+# The sources that decide what the backward launch does (kernel, helpers,
+# launch configuration): a change to any of them makes recorded counters stale.
+BWD_SOURCES = ("ccc_bwd.cu", "ccc_bwd_tma.cu", "ccc_device.cuh", "ccc_internal.h", "ccc_api.cu",
+               "ccc_chunkmap.cu")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ssm_depthwise_causal_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in BWD_SOURCES:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()
 
 
