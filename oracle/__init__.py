@@ -1,4 +1,4 @@
-"""float64 CPU oracle of the packed width-4 causal depthwise Conv1d + SiLU.
+"""float64 CPU oracle of the packed depthwise causal Conv1d (+ SiLU).
 
 TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` may import this package.  The product path
@@ -52,11 +52,13 @@ def _bind(path: str):
     lib = ctypes.CDLL(path)
     P = ctypes.c_void_p
     i64, i32 = ctypes.c_int64, ctypes.c_int32
-    lib.oracle_fwd.argtypes = [P, i64, i32, i64, P, P, P, i32, i32, P, i32, P, P, P, i64, P]
+    lib.oracle_fwd.argtypes = [P, i64, i32, i64, P, i32, P, i32, P, i32, i32, P, i32, P, P, P, i64, P]
     lib.oracle_fwd.restype = ctypes.c_int
-    lib.oracle_bwd.argtypes = [P, i64, i32, i64, P, P, P, P, i32, P, P, P, i64,
+    lib.oracle_bwd.argtypes = [P, i64, i32, i64, P, i32, P, i32, P, P, i32, P, P, P, i64,
                                P, P, i64, P, P, P, P, P]
     lib.oracle_bwd.restype = ctypes.c_int
+    lib.oracle_update.argtypes = [P, i64, i32, i64, P, i32, P, i32, P, i32, i32, P, i32, P, P, P, i64]
+    lib.oracle_update.restype = ctypes.c_int
     return lib
 
 
@@ -108,14 +110,19 @@ class Oracle:
         self.lib = _bind(path)
 
     def fwd(self, x, weight, bias, cu_seqlens, conv_state=None, cache_indices=None,
-            has_initial_state=None):
+            has_initial_state=None, activation="silu"):
         return _fwd(self.lib, x, weight, bias, cu_seqlens, conv_state, cache_indices,
-                    has_initial_state)
+                    has_initial_state, activation)
 
     def bwd(self, x, weight, bias, cu_seqlens, dy, hist=None, cache_indices=None,
-            has_initial_state=None, d_final_state=None, want_d_init=True):
+            has_initial_state=None, d_final_state=None, want_d_init=True, activation="silu"):
         return _bwd(self.lib, x, weight, bias, cu_seqlens, dy, hist, cache_indices,
-                    has_initial_state, d_final_state, want_d_init)
+                    has_initial_state, d_final_state, want_d_init, activation)
+
+    def update(self, x, weight, bias, cu_seqlens, conv_state, cache_indices, accepted=None,
+               activation="silu"):
+        return _update(self.lib, x, weight, bias, cu_seqlens, conv_state, cache_indices, accepted,
+                       activation)
 
 
 def default() -> Oracle:
@@ -127,30 +134,56 @@ def default() -> Oracle:
 
 
 def fwd(x, weight, bias, cu_seqlens, conv_state=None, cache_indices=None,
-        has_initial_state=None):
+        has_initial_state=None, activation="silu"):
     """See ``_fwd``."""
     return default().fwd(x, weight, bias, cu_seqlens, conv_state, cache_indices,
-                         has_initial_state)
+                         has_initial_state, activation)
 
 
 def bwd(x, weight, bias, cu_seqlens, dy, hist=None, cache_indices=None,
-        has_initial_state=None, d_final_state=None, want_d_init=True):
+        has_initial_state=None, d_final_state=None, want_d_init=True, activation="silu"):
     """See ``_bwd``."""
     return default().bwd(x, weight, bias, cu_seqlens, dy, hist, cache_indices,
-                         has_initial_state, d_final_state, want_d_init)
+                         has_initial_state, d_final_state, want_d_init, activation)
 
 
-def _fwd(lib, x, weight, bias, cu_seqlens, conv_state, cache_indices, has_initial_state):
-    """Forward of the oracle.
+def _act(activation) -> int:
+    """1 for SiLU (Megatron-Core causal_conv1d_cp, activation: "silu" or
+    "swish"), 0 for none."""
+    if activation is None:
+        return 0
+    if activation in ("silu", "swish"):
+        return 1
+    raise ValueError(f"unsupported activation {activation!r}")
+
+
+def _taps(weight):
+    """Weights as float64 [C, W] and the width W."""
+    w = _f64(weight)
+    if w.ndim != 2:
+        raise ValueError("weight must be [C, W]")
+    return np.ascontiguousarray(w), int(w.shape[1])
+
+
+def update(x, weight, bias, cu_seqlens, conv_state, cache_indices, accepted=None,
+           activation="silu"):
+    """See ``_update``."""
+    return default().update(x, weight, bias, cu_seqlens, conv_state, cache_indices, accepted,
+                            activation)
+
+
+def _fwd(lib, x, weight, bias, cu_seqlens, conv_state, cache_indices, has_initial_state,
+         activation):
+    """Forward of the oracle (width W = weight.shape[1]).
 
     Returns ``(out, state, hist)``: ``out`` float64 ``[rows, C]`` with NaN in
     every row the method does not write; ``state`` the updated pool (a copy,
-    uint16 bits ``[slots, C, L]``) or None; ``hist`` uint16 ``[N, 3, C]``, the
-    initial history each nonempty sequence used (rows of empty sequences are
-    left as 0xFFFF)."""
+    uint16 bits ``[slots, C, L]``) or None; ``hist`` uint16 ``[N, W-1, C]``,
+    the initial history each nonempty sequence used (rows of empty sequences
+    are left as 0xFFFF)."""
     xb = _bits(x)
     rows, C = xb.shape
-    w = _f64(weight).reshape(C, 4)
+    w, W = _taps(weight)
     b = _f64(bias)
     cu = _i32(cu_seqlens)
     N = cu.shape[0] - 1
@@ -159,26 +192,26 @@ def _fwd(lib, x, weight, bias, cu_seqlens, conv_state, cache_indices, has_initia
     cache = _i32(cache_indices)
     hi = _u8(has_initial_state)
     out = np.full((rows, C), np.nan)
-    hist = np.full((N, 3, C), 0xFFFF, dtype=np.uint16)
-    rc = lib.oracle_fwd(_ptr(xb), rows, C, C, _ptr(w), _ptr(b), _ptr(st), slots, L,
-                        _ptr(cu), N, _ptr(cache), _ptr(hi), _ptr(out), C, _ptr(hist))
+    hist = np.full((N, W - 1, C), 0xFFFF, dtype=np.uint16)
+    rc = lib.oracle_fwd(_ptr(xb), rows, C, C, _ptr(w), W, _ptr(b), _act(activation), _ptr(st),
+                        slots, L, _ptr(cu), N, _ptr(cache), _ptr(hi), _ptr(out), C, _ptr(hist))
     if rc != 0:
         raise ValueError(f"oracle_fwd rejected its arguments ({rc})")
     return out, st, hist
 
 
 def _bwd(lib, x, weight, bias, cu_seqlens, dy, hist, cache_indices,
-         has_initial_state, d_final_state, want_d_init):
-    """Backward of the oracle.
+         has_initial_state, d_final_state, want_d_init, activation):
+    """Backward of the oracle (width W = weight.shape[1]).
 
-    ``hist`` is the ``[N, 3, C]`` BF16 initial history (None: zeros).
+    ``hist`` is the ``[N, W-1, C]`` BF16 initial history (None: zeros).
     Returns a dict with ``dx`` (float64 ``[rows, C]``, NaN in rows not
-    written), ``dweight`` ``[C, 4]``, ``dbias`` ``[C]``, ``d_init``
-    ``[N, 3, C]`` (or None), and ``abs_dweight`` / ``abs_dbias``, the sums of
-    the absolute values of the reduced terms."""
+    written), ``dweight`` ``[C, W]``, ``dbias`` ``[C]``, ``d_init``
+    ``[N, W-1, C]`` (or None), and ``abs_dweight`` / ``abs_dbias``, the sums
+    of the absolute values of the reduced terms."""
     xb = _bits(x)
     rows, C = xb.shape
-    w = _f64(weight).reshape(C, 4)
+    w, W = _taps(weight)
     b = _f64(bias)
     cu = _i32(cu_seqlens)
     N = cu.shape[0] - 1
@@ -188,18 +221,43 @@ def _bwd(lib, x, weight, bias, cu_seqlens, dy, hist, cache_indices,
     dyb = _bits(dy)
     dfin = _f64(d_final_state)
     dx = np.full((rows, C), np.nan)
-    dweight = np.zeros((C, 4))
+    dweight = np.zeros((C, W))
     dbias = np.zeros(C)
-    d_init = np.full((N, 3, C), np.nan) if want_d_init else None
-    adw = np.zeros((C, 4))
+    d_init = np.full((N, W - 1, C), np.nan) if want_d_init else None
+    adw = np.zeros((C, W))
     adb = np.zeros(C)
-    rc = lib.oracle_bwd(_ptr(xb), rows, C, C, _ptr(w), _ptr(b), _ptr(h), _ptr(cu), N,
-                        _ptr(cache), _ptr(hi), _ptr(dyb), C, _ptr(dfin), _ptr(dx), C,
+    rc = lib.oracle_bwd(_ptr(xb), rows, C, C, _ptr(w), W, _ptr(b), _act(activation), _ptr(h),
+                        _ptr(cu), N, _ptr(cache), _ptr(hi), _ptr(dyb), C, _ptr(dfin), _ptr(dx), C,
                         _ptr(dweight), _ptr(dbias), _ptr(d_init), _ptr(adw), _ptr(adb))
     if rc != 0:
-        raise MemoryError("oracle_bwd could not allocate its scratch")
+        raise ValueError(f"oracle_bwd rejected its arguments or could not allocate ({rc})")
     return dict(dx=dx, dweight=dweight, dbias=dbias, d_init=d_init,
                 abs_dweight=adw, abs_dbias=adb)
+
+
+def _update(lib, x, weight, bias, cu_seqlens, conv_state, cache_indices, accepted, activation):
+    """Speculative / single-token state update of the oracle (width W =
+    weight.shape[1]).
+
+    Returns ``(out, state)``: ``out`` float64 ``[rows, C]`` with NaN in every
+    row not written, ``state`` the updated pool (a copy, uint16 bits
+    ``[slots, C, L]``).  ``accepted`` None means 1 for every sequence."""
+    xb = _bits(x)
+    rows, C = xb.shape
+    w, W = _taps(weight)
+    b = _f64(bias)
+    cu = _i32(cu_seqlens)
+    N = cu.shape[0] - 1
+    st = _bits(conv_state).copy()
+    slots, L = st.shape[0], st.shape[2]
+    cache = _i32(cache_indices)
+    acc = _i32(accepted)
+    out = np.full((rows, C), np.nan)
+    rc = lib.oracle_update(_ptr(xb), rows, C, C, _ptr(w), W, _ptr(b), _act(activation), _ptr(st),
+                           slots, L, _ptr(cu), N, _ptr(cache), _ptr(acc), _ptr(out), C)
+    if rc != 0:
+        raise ValueError(f"oracle_update rejected its arguments ({rc})")
+    return out, st
 
 
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:

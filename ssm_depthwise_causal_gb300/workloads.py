@@ -43,7 +43,7 @@ class Workload:
     lengths: np.ndarray            # int64 [N]
     cu_seqlens: torch.Tensor       # int32 [N+1]
     x: torch.Tensor                # bf16 [rows, C]
-    weight: torch.Tensor           # fp32 / bf16 [C, 4]
+    weight: torch.Tensor           # fp32 / bf16 [C, W] (W = 4 unless stated)
     bias: Optional[torch.Tensor]   # fp32 / bf16 [C] or None
     conv_state: Optional[torch.Tensor] = None      # bf16 [slots, C, L]
     cache_indices: Optional[torch.Tensor] = None   # int32 [N]
@@ -51,6 +51,11 @@ class Workload:
     dy: Optional[torch.Tensor] = None              # bf16 [rows, C]
     fragments: int = 1             # >1: process as consecutive fragments
     training: bool = True          # forward + backward
+    activation: Optional[str] = "silu"  # "silu" or None
+
+    @property
+    def width(self) -> int:
+        return int(self.weight.shape[1])
 
     @property
     def n_seqs(self) -> int:
@@ -107,11 +112,13 @@ def cu_from_lengths(lengths: np.ndarray) -> torch.Tensor:
 def make_custom(lengths, C, rows=None, *, seed=0, device="cpu",
                 w_dtype=torch.float32, b_dtype=torch.float32,
                 slots=None, state_len=4, n_minus_one=0, has_init_p=0.5,
-                with_state=True, training=True, x_std=1.0) -> Workload:
+                with_state=True, training=True, x_std=1.0, width=4,
+                activation="silu") -> Workload:
     """A general packed workload: given lengths, draw slots, flags and tensors.
 
     Draw order: slots, flags, x, weight, bias, state, dy (lengths are given).
-    ``b_dtype=None`` gives no bias; ``with_state=False`` gives no pool."""
+    ``b_dtype=None`` gives no bias; ``with_state=False`` gives no pool;
+    ``width`` is the number of taps W (weight [C, W])."""
     rng = np.random.default_rng(seed)
     lengths = np.asarray(lengths, dtype=np.int64)
     N = len(lengths)
@@ -130,7 +137,7 @@ def make_custom(lengths, C, rows=None, *, seed=0, device="cpu",
         has_init = torch.from_numpy(hi_np)
     g = _gen(seed, device)
     x = normal_bf16((rows, C), g, device, std=x_std)
-    weight = uniform((C, 4), g, device, -0.5, 0.5, w_dtype)
+    weight = uniform((C, width), g, device, -0.5, 0.5, w_dtype)
     bias = None
     if b_dtype is not None:
         bias = (torch.randn((C,), generator=g, device=device) * 0.1).to(b_dtype)
@@ -144,7 +151,7 @@ def make_custom(lengths, C, rows=None, *, seed=0, device="cpu",
         bias=bias, conv_state=state,
         cache_indices=None if cache is None else cache.to(device),
         has_initial_state=None if has_init is None else has_init.to(device),
-        dy=dy, training=training)
+        dy=dy, training=training, activation=activation)
 
 
 # --------------------------------------------------------------------------

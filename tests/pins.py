@@ -4,8 +4,9 @@ Each ``check_*`` takes a loaded oracle (``oracle.Oracle``) and raises
 ``AssertionError`` when the oracle disagrees with:
 
 * a library routine: ``torch.nn.functional.conv1d`` (depthwise, groups=C)
-  followed by ``torch.nn.functional.silu`` in float64 for the forward, and
-  torch autograd of that same composition for every gradient;
+  followed by ``torch.nn.functional.silu`` (or nothing, for the
+  no-activation variant) in float64 for the forward, and torch autograd of
+  that same composition for every gradient, at widths W = 2, 3, 4;
 * finite differences of the oracle's own forward for dweight / dbias;
 * closed forms: the impulse response of each tap and the zero-weight case;
 * the contract of FlashInfer ``flashinfer.mamba.causal_conv1d_fn``
@@ -13,7 +14,10 @@ Each ``check_*`` takes a loaded oracle (``oracle.Oracle``) and raises
   empty sequences, has_initial_state omitted;
 * the invariant of ``cake_causal_conv1d_kcp`` (description) that a fragment
   continuing a document from the previous fragment's tail reproduces the
-  unsplit result.
+  unsplit result;
+* for the speculative state update: decoding a document token by token, or
+  in speculative steps of which only a prefix is kept, gives for every kept
+  token the output of torch conv1d over the whole kept stream.
 
 ``tests/test_oracle_pins.py`` runs them on the oracle, and
 ``tests/test_oracle_mutants.py`` on deliberately broken copies of it, to show
@@ -22,6 +26,7 @@ caught.
 """
 from __future__ import annotations
 
+import dataclasses
 import math
 
 import numpy as np
@@ -37,36 +42,43 @@ def _bf16(values) -> torch.Tensor:
     return torch.as_tensor(np.asarray(values, dtype=np.float32)).to(torch.bfloat16)
 
 
+def _u16(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
 def small_case(seed=1, C=8, lengths=(5, 0, 7, 2, 1, 9), rows=None, n_minus_one=1,
-               has_init_p=0.5, slots=None, b_dtype=torch.float32):
+               has_init_p=0.5, slots=None, b_dtype=torch.float32, width=4, activation="silu"):
     """A tiny packed batch with a pool, a -1 request, an empty sequence,
-    short (<3) sequences and padding rows."""
+    short (< W-1) sequences and padding rows."""
     lengths = np.asarray(lengths)
     rows = int(lengths.sum()) + 3 if rows is None else rows
     return workloads.make_custom(lengths, C, rows=rows, seed=seed, slots=slots,
                                  n_minus_one=n_minus_one, has_init_p=has_init_p,
-                                 b_dtype=b_dtype)
+                                 b_dtype=b_dtype, width=width, activation=activation)
 
 
 def _history(wl, n):
-    """(init [3, C] float64, x_seq [len, C] float64, read_state) for sequence n."""
+    """(init [H, C] float64, x_seq [len, C] float64, read_state) for sequence n."""
+    H = wl.width - 1
     cu = wl.cu_seqlens.tolist()
     s, e = cu[n], cu[n + 1]
     x_seq = wl.x[s:e].to(F64)
     read = bool(wl.has_initial_state[n]) if wl.has_initial_state is not None else False
     if wl.conv_state is not None and read:
         q = int(wl.cache_indices[n])
-        init = wl.conv_state[q, :, 0:3].to(F64).t().contiguous()   # [3, C], pos 0 oldest
+        init = wl.conv_state[q, :, 0:H].to(F64).t().contiguous()   # [H, C], pos 0 oldest
     else:
-        init = torch.zeros(3, wl.C, dtype=F64)
+        init = torch.zeros(H, wl.C, dtype=F64)
     return init, x_seq, read
 
 
-def _torch_forward(init, x_seq, w, b):
-    """Library composition: depthwise conv1d over [init; x] then SiLU."""
-    h = torch.cat([init, x_seq], 0).t().unsqueeze(0)            # [1, C, len+3]
+def _torch_forward(init, x_seq, w, b, activation="silu"):
+    """Library composition: depthwise conv1d over [init; x] then SiLU (or
+    nothing)."""
+    h = torch.cat([init, x_seq], 0).t().unsqueeze(0)            # [1, C, len+H]
     z = F.conv1d(h, w.unsqueeze(1), b, groups=w.shape[0])        # [1, C, len]
-    return F.silu(z)[0].t()                                      # [len, C]
+    y = F.silu(z) if activation else z
+    return y[0].t()                                              # [len, C]
 
 
 def _live(wl, n):
@@ -76,7 +88,7 @@ def _live(wl, n):
 def check_forward_matches_conv1d(orc, wl=None):
     wl = wl or small_case()
     out, _, _ = orc.fwd(wl.x, wl.weight, wl.bias, wl.cu_seqlens, wl.conv_state,
-                        wl.cache_indices, wl.has_initial_state)
+                        wl.cache_indices, wl.has_initial_state, activation=wl.activation)
     w = wl.weight.to(F64)
     b = None if wl.bias is None else wl.bias.to(F64)
     cu = wl.cu_seqlens.tolist()
@@ -89,20 +101,21 @@ def check_forward_matches_conv1d(orc, wl=None):
             assert np.all(got == 0.0) and not np.any(np.signbit(got)), "-1 output must be +0"
             continue
         init, x_seq, _ = _history(wl, n)
-        ref = _torch_forward(init, x_seq, w, b).numpy()
+        ref = _torch_forward(init, x_seq, w, b, wl.activation).numpy()
         np.testing.assert_allclose(out[s:e], ref, rtol=1e-12, atol=1e-14)
     assert np.all(np.isnan(out[cu[-1]:])), "padding rows must not be written"
 
 
 def check_backward_matches_autograd(orc, wl=None, with_d_final=True):
     wl = wl or small_case()
+    H = wl.width - 1
     out, _, hist = orc.fwd(wl.x, wl.weight, wl.bias, wl.cu_seqlens, wl.conv_state,
-                           wl.cache_indices, wl.has_initial_state)
+                           wl.cache_indices, wl.has_initial_state, activation=wl.activation)
     gen = torch.Generator().manual_seed(7)
-    d_final = torch.randn(wl.n_seqs, 3, wl.C, generator=gen, dtype=F64) if with_d_final else None
+    d_final = torch.randn(wl.n_seqs, H, wl.C, generator=gen, dtype=F64) if with_d_final else None
     hist_arg = hist if wl.conv_state is not None else None
     got = orc.bwd(wl.x, wl.weight, wl.bias, wl.cu_seqlens, wl.dy, hist_arg,
-                  wl.cache_indices, wl.has_initial_state, d_final)
+                  wl.cache_indices, wl.has_initial_state, d_final, activation=wl.activation)
     w = wl.weight.to(F64).clone().requires_grad_(True)
     b = None if wl.bias is None else wl.bias.to(F64).clone().requires_grad_(True)
     cu = wl.cu_seqlens.tolist()
@@ -115,10 +128,10 @@ def check_backward_matches_autograd(orc, wl=None, with_d_final=True):
         init, x_seq, read = _history(wl, n)
         x_seq = x_seq.clone().requires_grad_(True)
         init = init.clone().requires_grad_(read)
-        y = _torch_forward(init, x_seq, w, b)
+        y = _torch_forward(init, x_seq, w, b, wl.activation)
         loss = loss + (y * wl.dy[s:e].to(F64)).sum()
         if d_final is not None:
-            final = torch.cat([init, x_seq], 0)[e - s:e - s + 3]     # [3, C]
+            final = torch.cat([init, x_seq], 0)[e - s:e - s + H]     # [H, C]
             loss = loss + (final * d_final[n]).sum()
         grads_x[n] = x_seq
         grads_init[n] = (init, read)
@@ -131,7 +144,7 @@ def check_backward_matches_autograd(orc, wl=None, with_d_final=True):
             continue
         np.testing.assert_allclose(got["dx"][s:e], grads_x[n].grad.numpy(), rtol=1e-11, atol=1e-13)
         init, read = grads_init[n]
-        ref_di = init.grad.numpy() if read else np.zeros((3, wl.C))
+        ref_di = init.grad.numpy() if read else np.zeros((H, wl.C))
         np.testing.assert_allclose(got["d_init"][n], ref_di, rtol=1e-11, atol=1e-13)
     np.testing.assert_allclose(got["dweight"], w.grad.numpy(), rtol=1e-11, atol=1e-12)
     if b is not None:
@@ -173,20 +186,23 @@ def check_weight_grad_finite_difference(orc):
 
 def check_impulse_response(orc):
     """x = unit impulse at row t0 of channel 3, w = e_k, no bias, no state:
-    the only nonzero output is SiLU(1) at row t0 + 3 - k (tap 3 = current
-    token, FlashInfer causal_conv1d_fn, weight)."""
+    the only nonzero output is SiLU(1) (or 1 without activation) at row
+    t0 + W-1 - k (tap W-1 = current token, FlashInfer causal_conv1d_fn,
+    weight), for every width W = 2, 3, 4."""
     C, L, t0 = 8, 12, 4
     silu1 = 1.0 / (1.0 + math.exp(-1.0))
-    for k in range(4):
-        x = np.zeros((L, C), dtype=np.float32)
-        x[t0, 3] = 1.0
-        w = np.zeros((C, 4))
-        w[:, k] = 1.0
-        cu = torch.tensor([0, L], dtype=torch.int32)
-        out, _, _ = orc.fwd(_bf16(x), w, None, cu)
-        expect = np.zeros((L, C))
-        expect[t0 + 3 - k, 3] = silu1
-        np.testing.assert_allclose(out, expect, rtol=1e-15, atol=0.0)
+    for W in (2, 3, 4):
+        for act, peak in (("silu", silu1), (None, 1.0)):
+            for k in range(W):
+                x = np.zeros((L, C), dtype=np.float32)
+                x[t0, 3] = 1.0
+                w = np.zeros((C, W))
+                w[:, k] = 1.0
+                cu = torch.tensor([0, L], dtype=torch.int32)
+                out, _, _ = orc.fwd(_bf16(x), w, None, cu, activation=act)
+                expect = np.zeros((L, C))
+                expect[t0 + W - 1 - k, 3] = peak
+                np.testing.assert_allclose(out, expect, rtol=1e-15, atol=0.0, err_msg=f"W={W} k={k} {act}")
 
 
 def check_zero_weight(orc):
@@ -206,14 +222,15 @@ def check_zero_weight(orc):
     assert np.all(out0[: cu[-1]] == 0.0)
 
 
-def check_state_rules(orc):
+def check_state_rules(orc, width=4):
     """Bit-exact state contract of causal_conv1d_fn (conv_state, cu_seqlens,
-    cache_indices, has_initial_state)."""
-    wl = small_case(seed=11, lengths=(7, 0, 2, 1, 5, 3), n_minus_one=1, slots=10)
-    before = wl.conv_state.view(torch.int16).numpy().view(np.uint16).copy()
+    cache_indices, has_initial_state), with W-1 carried values."""
+    H = width - 1
+    wl = small_case(seed=11, lengths=(7, 0, 2, 1, 5, 3), n_minus_one=1, slots=10, width=width)
+    before = _u16(wl.conv_state).copy()
     _, st, hist = orc.fwd(wl.x, wl.weight, wl.bias, wl.cu_seqlens, wl.conv_state,
                           wl.cache_indices, wl.has_initial_state)
-    xb = wl.x.view(torch.int16).numpy().view(np.uint16)
+    xb = _u16(wl.x)
     cu = wl.cu_seqlens.tolist()
     cache = wl.cache_indices.tolist()
     hi = wl.has_initial_state.tolist()
@@ -225,13 +242,13 @@ def check_state_rules(orc):
         if q == -1 or L == 0:
             continue
         touched.add(q)
-        init = before[q, :, 0:3].T if hi[n] else np.zeros((3, wl.C), np.uint16)   # [3, C]
+        init = before[q, :, 0:H].T if hi[n] else np.zeros((H, wl.C), np.uint16)   # [H, C]
         np.testing.assert_array_equal(hist[n], init)
-        full = np.concatenate([init, xb[s:e]], 0)                 # [L+3, C]
-        np.testing.assert_array_equal(st[q, :, 0:3].T, full[L:L + 3])
-        if L >= 3:
-            np.testing.assert_array_equal(st[q, :, 0:3].T, xb[e - 3:e])
-        np.testing.assert_array_equal(st[q, :, 3:], before[q, :, 3:])
+        full = np.concatenate([init, xb[s:e]], 0)                 # [L+H, C]
+        np.testing.assert_array_equal(st[q, :, 0:H].T, full[L:L + H])
+        if L >= H:
+            np.testing.assert_array_equal(st[q, :, 0:H].T, xb[e - H:e])
+        np.testing.assert_array_equal(st[q, :, H:], before[q, :, H:])
     for q in range(before.shape[0]):
         if q not in touched:
             np.testing.assert_array_equal(st[q], before[q])
@@ -243,35 +260,204 @@ def check_state_rules(orc):
     np.testing.assert_array_equal(o1, o2)
 
 
-def check_split_invariance(orc, cuts=(1, 2, 3, 5, 12), L=23, C=8):
+def check_split_invariance(orc, cuts=(1, 2, 3, 5, 12), L=23, C=8, width=4, activation="silu"):
     """A document processed as two fragments, the second starting from the
     first's written state (and the first's backward seeded with the second's
     d_init), reproduces the unsplit result (cake_causal_conv1d_kcp)."""
-    wl = workloads.make_custom([L], C, seed=13, slots=1, has_init_p=1.0)
+    H = width - 1
+    wl = workloads.make_custom([L], C, seed=13, slots=1, has_init_p=1.0, width=width)
     cache = torch.tensor([0], dtype=torch.int32)
     yes = torch.tensor([True])
     gen = torch.Generator().manual_seed(2)
-    d_last = torch.randn(1, 3, C, generator=gen, dtype=F64)
+    d_last = torch.randn(1, H, C, generator=gen, dtype=F64)
+    act = dict(activation=activation)
     out_u, st_u, hist_u = orc.fwd(wl.x, wl.weight, wl.bias, wl.cu_seqlens, wl.conv_state,
-                                  cache, yes)
-    g_u = orc.bwd(wl.x, wl.weight, wl.bias, wl.cu_seqlens, wl.dy, hist_u, cache, yes, d_last)
+                                  cache, yes, **act)
+    g_u = orc.bwd(wl.x, wl.weight, wl.bias, wl.cu_seqlens, wl.dy, hist_u, cache, yes, d_last, **act)
     for r in cuts:
         xa, xb = wl.x[:r], wl.x[r:]
         cua = torch.tensor([0, r], dtype=torch.int32)
         cub = torch.tensor([0, L - r], dtype=torch.int32)
-        out_a, st_a, hist_a = orc.fwd(xa, wl.weight, wl.bias, cua, wl.conv_state, cache, yes)
+        out_a, st_a, hist_a = orc.fwd(xa, wl.weight, wl.bias, cua, wl.conv_state, cache, yes, **act)
         out_b, st_b, hist_b = orc.fwd(xb, wl.weight, wl.bias, cub,
                                       torch.from_numpy(st_a.view(np.int16)).view(torch.bfloat16),
-                                      cache, yes)
+                                      cache, yes, **act)
         np.testing.assert_array_equal(np.concatenate([out_a, out_b]), out_u)
         np.testing.assert_array_equal(st_b, st_u)
-        g_b = orc.bwd(xb, wl.weight, wl.bias, cub, wl.dy[r:], hist_b, cache, yes, d_last)
+        g_b = orc.bwd(xb, wl.weight, wl.bias, cub, wl.dy[r:], hist_b, cache, yes, d_last, **act)
         g_a = orc.bwd(xa, wl.weight, wl.bias, cua, wl.dy[:r], hist_a, cache, yes,
-                      g_b["d_init"])
+                      g_b["d_init"], **act)
         np.testing.assert_array_equal(np.concatenate([g_a["dx"], g_b["dx"]]), g_u["dx"])
         np.testing.assert_array_equal(g_a["d_init"], g_u["d_init"])
         np.testing.assert_allclose(g_a["dweight"] + g_b["dweight"], g_u["dweight"], rtol=1e-12, atol=1e-14)
         np.testing.assert_allclose(g_a["dbias"] + g_b["dbias"], g_u["dbias"], rtol=1e-12, atol=1e-14)
+
+
+def check_variants_match_torch(orc):
+    """Widths 2 and 3 and the no-activation variant (Megatron-Core
+    causal_conv1d_cp: weight [D, W], activation optional) against torch
+    conv1d / autograd, and their state and split rules."""
+    for W in (2, 3, 4):
+        for act in ("silu", None):
+            if W == 4 and act == "silu":
+                continue  # the main pins
+            wl = small_case(seed=30 + W, lengths=(5, 0, 7, 1, 2, 9), width=W, activation=act)
+            check_forward_matches_conv1d(orc, wl)
+            check_backward_matches_autograd(orc, wl)
+        check_state_rules(orc, width=W)
+        check_split_invariance(orc, cuts=(1, 2, 7), L=17, width=W, activation=None if W == 3 else "silu")
+
+
+# ----------------------------------------------------- speculative update --
+
+def _stream_case(seed, C, n_live, T, width, slots, L):
+    """True token streams [n_live][T, C] (BF16 values), the taps, a bias, an
+    initial pool and distinct slots."""
+    rng = np.random.default_rng(seed)
+    g = torch.Generator().manual_seed(seed)
+    streams = [_bf16(rng.standard_normal((T, C))) for _ in range(n_live)]
+    w = (torch.rand((C, width), generator=g, dtype=F64) - 0.5)
+    b = torch.randn(C, generator=g, dtype=F64) * 0.1
+    pool = _bf16(rng.standard_normal((slots, C, L)))
+    slot_ids = rng.permutation(slots)[:n_live + 1].astype(np.int32)
+    return rng, streams, w, b, pool, slot_ids
+
+
+def _pack(chunks, C):
+    lengths = [c.shape[0] for c in chunks]
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32)
+    x = torch.cat(chunks, 0) if sum(lengths) else torch.zeros((0, C), dtype=torch.bfloat16)
+    return x, cu
+
+
+def check_update_decode_chain(orc, width=4, activation="silu"):
+    """Prefill a prefix of each stream, then decode the rest one token per
+    step with accepted count 1 (causal_conv1d_fn, Notes): every output equals
+    torch conv1d over the whole stream from the initial state, and the state
+    ends as the last W-1 tokens."""
+    H = width - 1
+    C, T, L = 8, 12, H + 2
+    rng, streams, w, b, pool, slot_ids = _stream_case(41, C, 3, T, width, 6, L)
+    prefix = [4, 1, 0]
+    cache = torch.tensor(slot_ids[:3])
+    init = [pool[q, :, 0:H].to(F64).t() for q in slot_ids[:3]]
+    refs = [_torch_forward(init[i], streams[i].to(F64), w, b, activation).numpy() for i in range(3)]
+    before = _u16(pool).copy()
+    x, cu = _pack([streams[i][:prefix[i]] for i in range(3)], C)
+    out, st, _ = orc.fwd(x, w, b, cu, pool, cache, torch.tensor([True] * 3), activation=activation)
+    for i in range(3):
+        np.testing.assert_allclose(out[int(cu[i]):int(cu[i + 1])], refs[i][:prefix[i]], rtol=1e-12, atol=1e-14)
+    state = torch.from_numpy(st.view(np.int16)).view(torch.bfloat16)
+    for t in range(T):
+        chunks = [streams[i][t:t + 1] if t >= prefix[i] else streams[i][:0] for i in range(3)]
+        x, cu = _pack(chunks, C)
+        out, st = orc.update(x, w, b, cu, state, cache, None, activation=activation)
+        for i in range(3):
+            if t >= prefix[i]:
+                np.testing.assert_allclose(out[int(cu[i])], refs[i][t], rtol=1e-12, atol=1e-14,
+                                           err_msg=f"stream {i} token {t}")
+        state = torch.from_numpy(st.view(np.int16)).view(torch.bfloat16)
+    final = _u16(state)
+    for i, q in enumerate(slot_ids[:3]):
+        np.testing.assert_array_equal(final[q, :, 0:H].T, _u16(streams[i])[T - H:T])
+    for q in range(pool.shape[0]):
+        if q not in slot_ids[:3]:
+            np.testing.assert_array_equal(final[q], before[q])
+
+
+def check_update_speculative_chain(orc, width=4, activation="silu"):
+    """Speculative steps: each live sequence feeds k drafts whose first m are
+    the stream's next tokens and the rest junk; the next step brings accepted
+    count m.  Every kept output equals torch conv1d over the kept stream;
+    a -1 request writes zeros and leaves its slot alone; a step with no token
+    leaves the slot alone (and the accepted count stands); positions at and
+    past k + W-2 are never written."""
+    H = width - 1
+    C, T, kmax = 8, 48, 5
+    L = kmax + H + 1
+    rng, streams, w, b, pool, slot_ids = _stream_case(43, C, 3, T, width, 8, L)
+    cache = torch.tensor(slot_ids)          # 3 live slots, then a -1 request
+    cache[3] = -1
+    init = [pool[q, :, 0:H].to(F64).t() for q in slot_ids[:3]]
+    refs = [_torch_forward(init[i], streams[i].to(F64), w, b, activation).numpy() for i in range(3)]
+    state = pool.clone()
+    pos = [0, 0, 0]
+    acc = [1, 1, 1, 1]
+    saw_full = saw_partial = saw_empty = False
+    for step in range(14):
+        chunks, keep = [], []
+        for i in range(3):
+            k = int(rng.integers(0 if i == 2 else 1, kmax + 1))
+            k = min(k, T - pos[i])
+            m = int(rng.integers(1, k + 1)) if k > 0 else 0
+            junk = _bf16(rng.standard_normal((k - m, C)) * 3.0)
+            chunks.append(torch.cat([streams[i][pos[i]:pos[i] + m], junk], 0))
+            keep.append((k, m))
+            saw_full |= k > 0 and m == k
+            saw_partial |= 0 < m < k
+            saw_empty |= k == 0
+        chunks.append(_bf16(rng.standard_normal((int(rng.integers(0, 3)), C))))
+        x, cu = _pack(chunks, C)
+        before = _u16(state).copy()
+        out, st = orc.update(x, w, b, cu, state, cache, torch.tensor(acc, dtype=torch.int32),
+                             activation=activation)
+        for i in range(3):
+            k, m = keep[i]
+            s = int(cu[i])
+            q = slot_ids[i]
+            if k == 0:
+                np.testing.assert_array_equal(st[q], before[q])
+                continue
+            np.testing.assert_allclose(out[s:s + m], refs[i][pos[i]:pos[i] + m], rtol=1e-12, atol=1e-14,
+                                       err_msg=f"step {step} stream {i}")
+            np.testing.assert_array_equal(st[q, :, k + H - 1:], before[q, :, k + H - 1:])
+            pos[i] += m
+            acc[i] = m
+        s3, e3 = int(cu[3]), int(cu[4])
+        assert np.all(out[s3:e3] == 0.0) and not np.any(np.signbit(out[s3:e3]))
+        untouched = [q for q in range(pool.shape[0]) if q not in slot_ids[:3]]
+        np.testing.assert_array_equal(st[untouched], before[untouched])
+        state = torch.from_numpy(st.view(np.int16)).view(torch.bfloat16)
+    assert saw_full and saw_partial and saw_empty
+
+
+def check_update_special_cases(orc):
+    """One token with accepted count 1 is a one-token prefill from the state
+    (same output, same positions 0:W-1); more tokens leave h[p+1] at position
+    p for p < len + W-2."""
+    for W in (2, 3, 4):
+        H = W - 1
+        wl = small_case(seed=50 + W, lengths=(1, 1, 4, 2), n_minus_one=0, slots=6, has_init_p=1.0,
+                        width=W)
+        wl = dataclasses.replace(wl, conv_state=_bf16(np.random.default_rng(W).standard_normal((6, wl.C, 8))))
+        cu = wl.cu_seqlens
+        one = torch.tensor([0, 1, 2], dtype=torch.int32)
+        out_p, st_p, _ = orc.fwd(wl.x[:2], wl.weight, wl.bias, one, wl.conv_state, wl.cache_indices[:2],
+                                 torch.tensor([True, True]))
+        out_u, st_u = orc.update(wl.x[:2], wl.weight, wl.bias, one, wl.conv_state, wl.cache_indices[:2])
+        np.testing.assert_array_equal(out_u, out_p)
+        for q in wl.cache_indices[:2].tolist():
+            np.testing.assert_array_equal(st_u[q, :, 0:H], st_p[q, :, 0:H])
+        # the write rule on longer steps, with accepted counts > 1
+        before = _u16(wl.conv_state)
+        accepted = torch.tensor([1, 2, 3, 2], dtype=torch.int32)
+        _, st = orc.update(wl.x, wl.weight, wl.bias, cu, wl.conv_state, wl.cache_indices, accepted)
+        xb = _u16(wl.x)
+        for n, q in enumerate(wl.cache_indices.tolist()):
+            s, e = int(cu[n]), int(cu[n + 1])
+            a = int(accepted[n])
+            h = np.concatenate([before[q, :, a - 1:a - 1 + H].T, xb[s:e]], 0)     # [H+len, C]
+            n_w = (e - s) + H - 1
+            np.testing.assert_array_equal(st[q, :, :n_w].T, h[1:1 + n_w])
+            np.testing.assert_array_equal(st[q, :, n_w:], before[q, :, n_w:])
+
+
+def check_update_variants(orc):
+    """The decode and speculative chains at widths 2 and 3 and without
+    activation."""
+    for W, act in ((2, "silu"), (3, None), (4, None)):
+        check_update_decode_chain(orc, width=W, activation=act)
+        check_update_speculative_chain(orc, width=W, activation=act)
 
 
 ALL_CHECKS = [
@@ -282,4 +468,9 @@ ALL_CHECKS = [
     check_zero_weight,
     check_state_rules,
     check_split_invariance,
+    check_variants_match_torch,
+    check_update_decode_chain,
+    check_update_speculative_chain,
+    check_update_special_cases,
+    check_update_variants,
 ]
