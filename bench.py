@@ -403,6 +403,121 @@ def run_ours(args, ws, rank, local):
         dist.destroy_process_group()
 
 
+UPDATE_METRIC = "decode-step tokens/s and effective HBM GB/s of ccc_update (serving pool, C=8192)"
+
+
+def update_algorithmic_bytes(wl):
+    """Bytes a decode step must move: x read and out written for the new
+    tokens of live requests (-1 requests write zeros only), W-1 state values
+    read and min(len + W-2, L) written per live channel, weights and bias.
+    Also returns the state bytes a dense history-contiguous pool moves at
+    sector granularity (each live slot's [C, L] block read and written)."""
+    C, W = wl.C, wl.width
+    H = W - 1
+    L = wl.conv_state.shape[2]
+    lens = wl.lengths
+    live = wl.cache_indices.cpu().numpy() != -1
+    ne = lens > 0
+    n_w = np.minimum(lens + H - 1, L)
+    b = int((lens[live] * 4).sum()) * C + int((lens[~live] * 2).sum()) * C
+    b += int((live & ne).sum()) * C * 2 * H + int((n_w[live & ne] * 2).sum()) * C
+    b += C * W * wl.weight.element_size() + (0 if wl.bias is None else C * wl.bias.element_size())
+    block = int((lens[live] * 4).sum()) * C + int((lens[~live] * 2).sum()) * C + int((live & ne).sum()) * C * 4 * L
+    return b, block
+
+
+def run_update(args, ws, rank, local):
+    """Decode-step timing of ccc_update: K steps, each after an L2 flush (the
+    whole step's working set fits in L2), timed alone with CUDA events."""
+    import ssm_depthwise_causal_gb300 as ccc
+    from ssm_depthwise_causal_gb300 import workloads
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = init_dist(ws, "nccl")
+    ccc._lib.lib()
+    wl = workloads.WORKLOADS[args.workload](device=dev)
+    if wl.num_accepted is None:
+        raise SystemExit("--op update needs a decode workload (decode, spec_decode)")
+    T, C, N = wl.valid_tokens, wl.C, wl.n_seqs
+    pool = wl.conv_state
+    out = torch.empty_like(wl.x)
+    acc = wl.num_accepted if wl.lengths.max() > 1 else None
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def call(x, s):
+        ccc.ccc_update(x, wl.weight, wl.bias, pool, wl.cu_seqlens, wl.cache_indices, acc, out, stream=s)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.zero_()
+            call(wl.x, stream)
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    clocks = ClockSampler(local)
+    if dist:
+        dist.barrier()
+    clocks.start()
+    time.sleep(0.3)
+    launches = 0
+    with torch.cuda.stream(stream):
+        for k in range(K):
+            flush.zero_()
+            ev[k][0].record(stream)
+            call(wl.x, stream)
+            launches += ccc.last_launch_count()
+            ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = job_max(statistics.mean(a.elapsed_time(b) for a, b in ev), dist, dev)
+    value = job_throughput(ws, T, ms)
+    alg, block = update_algorithmic_bytes(wl)
+    peak, peak_kind = measured_peak()
+    gbs = alg / (ms / 1e3) / 1e9
+
+    # end to end: the new tokens from pinned host memory, outputs back
+    hx = torch.empty(wl.x.shape, dtype=wl.x.dtype, pin_memory=True)
+    hx.copy_(wl.x)
+    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    xin = torch.empty_like(wl.x)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(K):
+            xin.copy_(hx, non_blocking=True)
+            call(xin, stream)
+            hout.copy_(out, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = job_max(e0.elapsed_time(e1) / K, dist, dev)
+    if rank == 0:
+        line = {
+            "metric": UPDATE_METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "storage_dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "n_seqs": N, "tokens": T, "C": C,
+                       "pool": list(pool.shape), "l2": "flushed before every timed step (working set < L2)",
+                       "parallelism": f"replicas x{ws}"},
+            "effective_gbs": gbs,
+            "roofline": {"kernel": "update_kernel (one launch per step)", "bound": "hbm", "achieved": gbs,
+                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": gbs / peak,
+                         "traffic": None, "algorithmic_bytes_per_launch": alg,
+                         "state_block_bytes_per_launch": block},
+            "e2e": {"value": job_throughput(ws, T, e2e_ms), "unit": UNIT,
+                    "h2d_bytes_per_step": hx.numel() * 2, "d2h_bytes_per_step": hout.numel() * 2,
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": launches,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
 def run_profile(args, local):
     """W warm-up steps then one step of the same calls, nothing else: the
     command the ncu captures run."""
@@ -413,6 +528,13 @@ def run_profile(args, local):
     wl = workloads.WORKLOADS[args.workload](device=dev)
     T, C, N, rows = wl.valid_tokens, wl.C, wl.n_seqs, wl.rows
     out = torch.empty_like(wl.x)
+    if wl.num_accepted is not None:  # a decode step: ccc_update only
+        acc = wl.num_accepted if wl.lengths.max() > 1 else None
+        for _ in range(args.warmup + 1):
+            ccc.ccc_update(wl.x, wl.weight, wl.bias, wl.conv_state, wl.cu_seqlens, wl.cache_indices, acc, out)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_case": wl.name, "valid_tokens": T}), flush=True)
+        return
     hist = torch.empty((N, 3, C), dtype=torch.bfloat16, device=dev)
     ws_f = torch.empty(max(1, ccc.ccc_workspace_size(rows, N, C, False)), dtype=torch.uint8, device=dev)
     state = None if wl.conv_state is None else wl.conv_state.clone()
@@ -442,12 +564,20 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", action="store_true",
                     help="run warm-up + one step of --workload only (for ncu captures)")
-    ap.add_argument("--workload", default="packed", choices=["tiny", "dense", "packed", "packed_small", "serving", "long"])
+    ap.add_argument("--workload", default="packed",
+                    choices=["tiny", "dense", "packed", "packed_small", "serving", "long", "decode", "spec_decode"])
+    ap.add_argument("--op", default="fwdbwd", choices=["fwdbwd", "update"],
+                    help="fwdbwd: the packed training step (the headline); update: one decode step "
+                         "(ccc_update) of --workload decode / spec_decode")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     ws, rank, local = dist_env()
     if args.profile:
         run_profile(args, local)
+    elif args.op == "update":
+        if args.workload not in ("decode", "spec_decode"):
+            args.workload = "decode"
+        run_update(args, ws, rank, local)
     elif args.impl == "reference":
         run_reference(args, ws, rank)
     else:

@@ -1,7 +1,9 @@
 /*
  * ccc.h -- C ABI of the GB300 (sm_103a) packed, width-4, depthwise causal
- * Conv1d + SiLU ("ccc"): forward with in-place conv_state pool update, and
- * the fused backward with a deterministic FP32 weight/bias gradient.
+ * Conv1d + SiLU ("ccc"): forward with in-place conv_state pool update, the
+ * fused backward with a deterministic FP32 weight/bias gradient, and the
+ * speculative / single-token decode update of the pool.  Widths 2 and 3 and
+ * the no-activation variant are served by the same entry points.
  *
  * The operation (FlashInfer "flashinfer.mamba.causal_conv1d_fn", Parameters
  * and Notes): sequence n owns the packed rows [cu_seqlens[n], cu_seqlens[n+1])
@@ -64,10 +66,14 @@ extern "C" {
 
 typedef enum { CCC_F32 = 0, CCC_BF16 = 1, CCC_NONE = -1 } ccc_dtype;
 
+/* Activation after the convolution (Megatron-Core "core.ssm.causal_conv1d",
+ * causal_conv1d_cp: optional activation passed to causal_conv1d_fn). */
+typedef enum { CCC_ACT_NONE = 0, CCC_ACT_SILU = 1 } ccc_activation;
+
 typedef enum {
     CCC_OK = 0,
     CCC_ERR_NULL = -1,      /* a required pointer is NULL */
-    CCC_ERR_SHAPE = -2,     /* a size or stride is invalid (C % 8, state_len < 3, ...) */
+    CCC_ERR_SHAPE = -2,     /* a size or stride is invalid (C % 8, state_len < W-1, width, activation, ...) */
     CCC_ERR_DTYPE = -3,     /* unknown dtype code, or a dtype code without its buffer */
     CCC_ERR_ALIGN = -4,     /* x/out/dy/dx/saved_hist not 16-byte aligned, or misaligned element pointers */
     CCC_ERR_WORKSPACE = -5, /* workspace NULL or smaller than ccc_workspace_size() */
@@ -96,13 +102,18 @@ size_t ccc_workspace_size(int64_t rows, int32_t n_seqs, int32_t channels, int32_
  *               aligned; x_row_stride >= C, a multiple of 8.  Rows after
  *               cu_seqlens[N] may be padding.
  *  rows, C      C > 0 and a multiple of 8 (cake_causal_conv1d_kcp, x_local).
- *  weight       [dev] [C][4] contiguous, w_dtype CCC_F32 or CCC_BF16.
+ *  weight       [dev] [C][width] contiguous, w_dtype CCC_F32 or CCC_BF16.
+ *  width        taps W: 4 (causal_conv1d_fn), or 2 or 3 (causal_conv1d_cp,
+ *               weight [D, W]).  Everything written "3" below is W - 1: the
+ *               history rows, the state positions read and written, the rows
+ *               of saved_hist / d_final_state / d_init_state.
  *  bias         [dev] [C] with b_dtype CCC_F32/CCC_BF16, or NULL with
  *               b_dtype CCC_NONE.
+ *  activation   CCC_ACT_SILU (causal_conv1d_fn) or CCC_ACT_NONE (out = z).
  *  conv_state   [dev] BF16 pool, in place, or NULL (zero history, no
  *               write-back).  Element (slot, c, l) is at
  *               st_slot*slot + st_c*c + st_l*l; st_c == 1 or st_l == 1; slots
- *               must not overlap; state_len >= 3; n_slots >= 1.
+ *               must not overlap; state_len >= W - 1; n_slots >= 1.
  *  cu_seqlens   [dev] int32 [N+1]: 0, nondecreasing, cu_seqlens[N] <= rows.
  *  cache_indices[dev] int32 [N] slot per sequence, -1 = zero output and no
  *               state access.  Required with a pool; optional without (then
@@ -118,7 +129,8 @@ size_t ccc_workspace_size(int64_t rows, int32_t n_seqs, int32_t channels, int32_
  *               aligned (NULL allowed when that size is 0).
  */
 int ccc_fwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
-            const void *weight, int32_t w_dtype, const void *bias, int32_t b_dtype,
+            const void *weight, int32_t w_dtype, int32_t width,
+            const void *bias, int32_t b_dtype, int32_t activation,
             void *conv_state, int32_t n_slots, int32_t state_len,
             int64_t st_slot, int64_t st_c, int64_t st_l,
             const int32_t *cu_seqlens, int32_t N,
@@ -132,8 +144,9 @@ int ccc_fwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
  * dweight; core.ssm.causal_conv1d, _exchange_initial_states: the state
  * gradient is what a preceding fragment receives).
  *
- *  x, rows, C, x_row_stride, weight, w_dtype, bias, b_dtype: as in ccc_fwd
- *               (the same values the forward saw).
+ *  x, rows, C, x_row_stride, weight, w_dtype, width, bias, b_dtype,
+ *               activation: as in ccc_fwd (the same values the forward saw).
+ *               Without activation dz = dy.
  *  saved_hist   [dev] BF16 [N][3][C] from ccc_fwd, or NULL (zero history).
  *  cu_seqlens, N, cache_indices (NULL = all live), has_initial_state (NULL =
  *               all false): as in ccc_fwd.
@@ -144,7 +157,7 @@ int ccc_fwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
  *               d_init_state of the fragment that continued this one.
  *  dx           [dev] BF16 [rows][dx_row_stride]; rows after cu_seqlens[N] are
  *               not written; zero for -1 requests.
- *  dweight      [dev] FP32 [C][4], overwritten (not accumulated).
+ *  dweight      [dev] FP32 [C][width], overwritten (not accumulated).
  *  dbias        [dev] FP32 [C] or NULL, overwritten.
  *  d_init_state [dev] FP32 [N][3][C] or NULL: gradient of the initial history
  *               for sequences that read their state (has_initial_state true,
@@ -154,7 +167,8 @@ int ccc_fwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
  * Every buffer written must not overlap any other operand.
  */
 int ccc_bwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
-            const void *weight, int32_t w_dtype, const void *bias, int32_t b_dtype,
+            const void *weight, int32_t w_dtype, int32_t width,
+            const void *bias, int32_t b_dtype, int32_t activation,
             const void *saved_hist,
             const int32_t *cu_seqlens, int32_t N,
             const int32_t *cache_indices, const uint8_t *has_initial_state,
@@ -187,7 +201,8 @@ int ccc_bwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
 #define CCC_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 
 int ccc_bwd_noalloc(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
-                    const void *weight, int32_t w_dtype, const void *bias, int32_t b_dtype,
+                    const void *weight, int32_t w_dtype, int32_t width,
+                    const void *bias, int32_t b_dtype, int32_t activation,
                     const void *saved_hist,
                     const int32_t *cu_seqlens, int32_t N,
                     const int32_t *cache_indices, const uint8_t *has_initial_state,
@@ -197,11 +212,54 @@ int ccc_bwd_noalloc(const void *x, int64_t rows, int32_t C, int64_t x_row_stride
                     float *dweight, float *dbias, float *d_init_state,
                     void *cuda_stream);
 
+/*
+ * Speculative / single-token decode step (causal_conv1d_fn, Notes: "after
+ * prefill, the first speculative update uses accepted count 1"; the pages
+ * define nothing more, so the rule below is this library's reading of it).
+ *
+ * Sequence n feeds len = cu_seqlens[n+1] - cu_seqlens[n] new tokens (1 for a
+ * plain decode step, the draft tokens for a speculative one).  With
+ * a = num_accepted[n] (1 when num_accepted is NULL) -- how many tokens of the
+ * slot's previous step were kept -- the W-1 history values before the first
+ * new token are conv_state positions a-1 .. a+W-3 of slot cache_indices[n];
+ * each token's output is computed exactly as in ccc_fwd; then the step writes
+ * history value h[p+1] to position p for p < min(len + W - 2, state_len)
+ * (h = the W-1 values read, then the len new tokens), so the next step,
+ * keeping a' of these tokens, reads positions a'-1 .. a'+W-3.  A prefill
+ * (ccc_fwd) leaves exactly the state this rule expects for a = 1, and one
+ * token with a = 1 is the ordinary shift-by-one decode update.  A -1 slot
+ * gives zero output and no state access; an empty sequence leaves its slot
+ * alone.  No workspace, one kernel launch.
+ *
+ *  x, rows, C, x_row_stride, weight, w_dtype, width, bias, b_dtype,
+ *               activation, out, out_row_stride: as in ccc_fwd.
+ *  conv_state   [dev] BF16 pool, required, same layout rules as ccc_fwd;
+ *               state_len >= W - 1, and >= len + W - 2 for every position a
+ *               later step may read to have been written.  A dense
+ *               [slots][C][state_len] pool with state_len <= 8, or a
+ *               channel-contiguous one, is moved in 16-byte vectors.
+ *  cache_indices[dev] int32 [N], required; live slots unique, in
+ *               [0, n_slots).
+ *  num_accepted [dev] int32 [N] or NULL; values outside [1, state_len - W
+ *               + 2] are clamped into it (caller-owned constraint).
+ * Meant for short per-sequence lengths (one warp walks each sequence's
+ * tokens); long prompts belong to ccc_fwd.
+ */
+int ccc_update(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
+               const void *weight, int32_t w_dtype, int32_t width,
+               const void *bias, int32_t b_dtype, int32_t activation,
+               void *conv_state, int32_t n_slots, int32_t state_len,
+               int64_t st_slot, int64_t st_c, int64_t st_l,
+               const int32_t *cu_seqlens, int32_t N,
+               const int32_t *cache_indices, const int32_t *num_accepted,
+               void *out, int64_t out_row_stride, void *cuda_stream);
+
 /* Name of a ccc_status value ("CCC_OK", ...); "unknown" otherwise. */
 const char *ccc_status_string(int status);
 
-/* Number of kernel launches the last successful ccc_fwd / ccc_bwd on this
- * host thread enqueued (for launch accounting; memsets not included). */
+/* Number of kernel launches the last successful ccc_fwd / ccc_bwd /
+ * ccc_update on this host thread enqueued (for launch accounting; memsets
+ * not included). */
 int ccc_last_launch_count(void);
 
 #ifdef __cplusplus

@@ -14,8 +14,8 @@ _PATH = os.path.join(_PKG, "libccc.so")
 _lock = threading.Lock()
 _handle = None
 
-EXPORTS = ("ccc_workspace_size", "ccc_fwd", "ccc_bwd", "ccc_bwd_noalloc", "ccc_status_string",
-           "ccc_last_launch_count")
+EXPORTS = ("ccc_workspace_size", "ccc_fwd", "ccc_bwd", "ccc_bwd_noalloc", "ccc_update",
+           "ccc_status_string", "ccc_last_launch_count")
 
 # Size of the fixed scratch array behind ccc_bwd_noalloc (CCC_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -39,15 +39,18 @@ def lib() -> ctypes.CDLL:
             P, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
             h.ccc_workspace_size.argtypes = [i64, i32, i32, i32]
             h.ccc_workspace_size.restype = sz
-            h.ccc_fwd.argtypes = [P, i64, i32, i64, P, i32, P, i32, P, i32, i32, i64, i64, i64,
+            h.ccc_fwd.argtypes = [P, i64, i32, i64, P, i32, i32, P, i32, i32, P, i32, i32, i64, i64, i64,
                                   P, i32, P, P, P, i64, P, P, sz, P]
             h.ccc_fwd.restype = ctypes.c_int
-            h.ccc_bwd.argtypes = [P, i64, i32, i64, P, i32, P, i32, P, P, i32, P, P, P, i64, P,
+            h.ccc_bwd.argtypes = [P, i64, i32, i64, P, i32, i32, P, i32, i32, P, P, i32, P, P, P, i64, P,
                                   P, i64, P, P, P, P, sz, P]
             h.ccc_bwd.restype = ctypes.c_int
-            h.ccc_bwd_noalloc.argtypes = [P, i64, i32, i64, P, i32, P, i32, P, P, i32, P, P, P, i64, P,
-                                          P, i64, P, P, P, P]
+            h.ccc_bwd_noalloc.argtypes = [P, i64, i32, i64, P, i32, i32, P, i32, i32, P, P, i32, P, P, P,
+                                          i64, P, P, i64, P, P, P, P]
             h.ccc_bwd_noalloc.restype = ctypes.c_int
+            h.ccc_update.argtypes = [P, i64, i32, i64, P, i32, i32, P, i32, i32, P, i32, i32, i64, i64, i64,
+                                     P, i32, P, P, P, i64, P]
+            h.ccc_update.restype = ctypes.c_int
             h.ccc_status_string.argtypes = [ctypes.c_int]
             h.ccc_status_string.restype = ctypes.c_char_p
             h.ccc_last_launch_count.argtypes = []

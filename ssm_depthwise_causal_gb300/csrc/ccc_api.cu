@@ -56,6 +56,10 @@ size_t map_bytes(int64_t rows, int N, int B) {
 
 int dtype_size(int code) { return code == CCC_F32 ? 4 : (code == CCC_BF16 ? 2 : 0); }
 
+bool width_ok(int width) { return width >= 2 && width <= 4; }
+
+bool activation_ok(int act) { return act == CCC_ACT_NONE || act == CCC_ACT_SILU; }
+
 // Pool layout check: strides non-negative, channel or history axis
 // contiguous, and distinct (slot, c, l) never share an element (sorted-stride
 // criterion: each stride exceeds the span of the smaller dimensions).
@@ -105,7 +109,9 @@ size_t ccc_workspace_size(int64_t rows, int32_t n_seqs, int32_t channels, int32_
     if (rows == 0 || n_seqs == 0) return 0;
     if (!for_bwd) return map_bytes(rows, n_seqs, ccc::kFwdChunk);
     const size_t mb = map_bytes(rows, n_seqs, ccc::kBwdChunk);
-    const int R = ccc::bwd_runs(rows, n_seqs, channels);
+    // Enough partial rows for whichever backward kernel the width picks.
+    int R = ccc::bwd_runs(rows, n_seqs, channels, false);
+    if (ccc::kBwdTma) R = std::max(R, ccc::bwd_runs(rows, n_seqs, channels, true));
     return mb + round_up(static_cast<size_t>(R) * 5 * channels * sizeof(float), kAlignWs);
 }
 
@@ -126,7 +132,8 @@ const char *ccc_status_string(int status) {
 int ccc_last_launch_count(void) { return g_last_launches; }
 
 int ccc_fwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
-            const void *weight, int32_t w_dtype, const void *bias, int32_t b_dtype,
+            const void *weight, int32_t w_dtype, int32_t width,
+            const void *bias, int32_t b_dtype, int32_t activation,
             void *conv_state, int32_t n_slots, int32_t state_len,
             int64_t st_slot, int64_t st_c, int64_t st_l,
             const int32_t *cu_seqlens, int32_t N,
@@ -141,8 +148,10 @@ int ccc_fwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
     if (x_row_stride > INT32_MAX || out_row_stride > INT32_MAX) return CCC_ERR_SHAPE;
     if (w_dtype != CCC_F32 && w_dtype != CCC_BF16) return CCC_ERR_DTYPE;
     if (bias ? (b_dtype != CCC_F32 && b_dtype != CCC_BF16) : (b_dtype != CCC_NONE)) return CCC_ERR_DTYPE;
+    if (!width_ok(width) || !activation_ok(activation)) return CCC_ERR_SHAPE;
+    const int H = width - 1;
     if (conv_state) {
-        if (state_len < 3 || n_slots < 1) return CCC_ERR_SHAPE;
+        if (state_len < H || n_slots < 1) return CCC_ERR_SHAPE;
         if (!state_layout_ok(n_slots, C, state_len, st_slot, st_c, st_l)) return CCC_ERR_SHAPE;
     }
     // ---- pointers
@@ -159,7 +168,7 @@ int ccc_fwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
     // ---- aliasing: every written buffer against every other operand
     const Span s_x = span(x, mat_bytes(rows, x_row_stride, C));
     const Span s_out = span(out, mat_bytes(rows, out_row_stride, C));
-    const Span s_w = span(weight, static_cast<size_t>(C) * 4 * dtype_size(w_dtype));
+    const Span s_w = span(weight, static_cast<size_t>(C) * width * dtype_size(w_dtype));
     const Span s_b = span(bias, bias ? static_cast<size_t>(C) * dtype_size(b_dtype) : 0);
     Span s_st;
     if (conv_state) {
@@ -169,7 +178,7 @@ int ccc_fwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
     const Span s_cu = span(cu_seqlens, static_cast<size_t>(N + 1) * 4);
     const Span s_ci = span(cache_indices, static_cast<size_t>(N) * 4);
     const Span s_hi = span(has_initial_state, static_cast<size_t>(N));
-    const Span s_h = span(saved_hist, static_cast<size_t>(N) * 3 * C * 2);
+    const Span s_h = span(saved_hist, static_cast<size_t>(N) * H * C * 2);
     const Span s_ws = span(workspace, ws_need);
     const Span *all[] = {&s_x, &s_out, &s_w, &s_b, &s_st, &s_cu, &s_ci, &s_hi, &s_h, &s_ws};
     const Span *written[] = {&s_out, &s_st, &s_h, &s_ws};
@@ -190,6 +199,8 @@ int ccc_fwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
     a.w_bf16 = w_dtype == CCC_BF16;
     a.b = bias;
     a.b_kind = bias ? (b_dtype == CCC_F32 ? 1 : 2) : 0;
+    a.width = width;
+    a.act = activation;
     a.state = static_cast<uint16_t *>(conv_state);
     a.n_slots = n_slots;
     a.st_slot = st_slot;
@@ -225,7 +236,8 @@ int ccc_fwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
 }
 
 int ccc_bwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
-            const void *weight, int32_t w_dtype, const void *bias, int32_t b_dtype,
+            const void *weight, int32_t w_dtype, int32_t width,
+            const void *bias, int32_t b_dtype, int32_t activation,
             const void *saved_hist,
             const int32_t *cu_seqlens, int32_t N,
             const int32_t *cache_indices, const uint8_t *has_initial_state,
@@ -242,6 +254,8 @@ int ccc_bwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
     if (x_row_stride > INT32_MAX || dy_row_stride > INT32_MAX || dx_row_stride > INT32_MAX) return CCC_ERR_SHAPE;
     if (w_dtype != CCC_F32 && w_dtype != CCC_BF16) return CCC_ERR_DTYPE;
     if (bias ? (b_dtype != CCC_F32 && b_dtype != CCC_BF16) : (b_dtype != CCC_NONE)) return CCC_ERR_DTYPE;
+    if (!width_ok(width) || !activation_ok(activation)) return CCC_ERR_SHAPE;
+    const int H = width - 1;
     if (!x || !weight || !cu_seqlens || !dy || !dx || !dweight) return CCC_ERR_NULL;
     if (!aligned(x, 16) || !aligned(dy, 16) || !aligned(dx, 16) || (saved_hist && !aligned(saved_hist, 16)) ||
         (d_final_state && !aligned(d_final_state, 16)) || (d_init_state && !aligned(d_init_state, 16)))
@@ -257,16 +271,16 @@ int ccc_bwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
     const Span s_x = span(x, mat_bytes(rows, x_row_stride, C));
     const Span s_dy = span(dy, mat_bytes(rows, dy_row_stride, C));
     const Span s_dx = span(dx, mat_bytes(rows, dx_row_stride, C));
-    const Span s_w = span(weight, static_cast<size_t>(C) * 4 * dtype_size(w_dtype));
+    const Span s_w = span(weight, static_cast<size_t>(C) * width * dtype_size(w_dtype));
     const Span s_b = span(bias, bias ? static_cast<size_t>(C) * dtype_size(b_dtype) : 0);
-    const Span s_h = span(saved_hist, static_cast<size_t>(N) * 3 * C * 2);
+    const Span s_h = span(saved_hist, static_cast<size_t>(N) * H * C * 2);
     const Span s_cu = span(cu_seqlens, static_cast<size_t>(N + 1) * 4);
     const Span s_ci = span(cache_indices, static_cast<size_t>(N) * 4);
     const Span s_hi = span(has_initial_state, static_cast<size_t>(N));
-    const Span s_df = span(d_final_state, static_cast<size_t>(N) * 3 * C * 4);
-    const Span s_dw = span(dweight, static_cast<size_t>(C) * 4 * 4);
+    const Span s_df = span(d_final_state, static_cast<size_t>(N) * H * C * 4);
+    const Span s_dw = span(dweight, static_cast<size_t>(C) * width * 4);
     const Span s_db = span(dbias, static_cast<size_t>(C) * 4);
-    const Span s_di = span(d_init_state, static_cast<size_t>(N) * 3 * C * 4);
+    const Span s_di = span(d_init_state, static_cast<size_t>(N) * H * C * 4);
     const Span s_ws = span(workspace, ws_need);
     const Span *all[] = {&s_x, &s_dy, &s_dx, &s_w, &s_b, &s_h, &s_cu, &s_ci, &s_hi, &s_df, &s_dw, &s_db, &s_di, &s_ws};
     const Span *written[] = {&s_dx, &s_dw, &s_db, &s_di, &s_ws};
@@ -277,7 +291,7 @@ int ccc_bwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
     g_last_launches = 0;
     cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
     if (rows == 0 || N == 0) {  // no token: the gradients are zero
-        if (cudaMemsetAsync(dweight, 0, static_cast<size_t>(C) * 4 * sizeof(float), st) != cudaSuccess)
+        if (cudaMemsetAsync(dweight, 0, static_cast<size_t>(C) * width * sizeof(float), st) != cudaSuccess)
             return CCC_ERR_CUDA;
         if (dbias && cudaMemsetAsync(dbias, 0, static_cast<size_t>(C) * sizeof(float), st) != cudaSuccess)
             return CCC_ERR_CUDA;
@@ -293,6 +307,8 @@ int ccc_bwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
     a.w_bf16 = w_dtype == CCC_BF16;
     a.b = bias;
     a.b_kind = bias ? (b_dtype == CCC_F32 ? 1 : 2) : 0;
+    a.width = width;
+    a.act = activation;
     a.hist = static_cast<const uint16_t *>(saved_hist);
     a.cu = cu_seqlens;
     a.N = N;
@@ -319,14 +335,85 @@ int ccc_bwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
         a.map = map;
         pdl = true;
     }
-    a.slabs = ccc::bwd_columns(C);
-    a.runs = ccc::bwd_runs(rows, N, C);
-    if ((ccc::kBwdTma ? ccc::launch_bwd_tma(a, pdl, st) : ccc::launch_bwd(a, pdl, st)) != cudaSuccess)
-        return CCC_ERR_CUDA;
+    const bool tma = ccc::bwd_uses_tma(width, activation);
+    a.slabs = ccc::bwd_columns(C, tma);
+    a.runs = ccc::bwd_runs(rows, N, C, tma);
+    if ((tma ? ccc::launch_bwd_tma(a, pdl, st) : ccc::launch_bwd(a, pdl, st)) != cudaSuccess) return CCC_ERR_CUDA;
     ++launches;
-    if (ccc::launch_reduce(a.part, a.runs, C, dweight, dbias, true, st) != cudaSuccess) return CCC_ERR_CUDA;
+    if (ccc::launch_reduce(a.part, a.runs, C, width, dweight, dbias, true, st) != cudaSuccess) return CCC_ERR_CUDA;
     ++launches;
     g_last_launches = launches;
+    return CCC_OK;
+}
+
+int ccc_update(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
+               const void *weight, int32_t w_dtype, int32_t width,
+               const void *bias, int32_t b_dtype, int32_t activation,
+               void *conv_state, int32_t n_slots, int32_t state_len,
+               int64_t st_slot, int64_t st_c, int64_t st_l,
+               const int32_t *cu_seqlens, int32_t N,
+               const int32_t *cache_indices, const int32_t *num_accepted,
+               void *out, int64_t out_row_stride, void *cuda_stream) {
+    if (rows < 0 || N < 0 || C <= 0 || C % 8 != 0) return CCC_ERR_SHAPE;
+    if (rows > INT32_MAX) return CCC_ERR_SHAPE;
+    if (x_row_stride < C || out_row_stride < C || x_row_stride % 8 || out_row_stride % 8) return CCC_ERR_SHAPE;
+    if (x_row_stride > INT32_MAX || out_row_stride > INT32_MAX) return CCC_ERR_SHAPE;
+    if (w_dtype != CCC_F32 && w_dtype != CCC_BF16) return CCC_ERR_DTYPE;
+    if (bias ? (b_dtype != CCC_F32 && b_dtype != CCC_BF16) : (b_dtype != CCC_NONE)) return CCC_ERR_DTYPE;
+    if (!width_ok(width) || !activation_ok(activation)) return CCC_ERR_SHAPE;
+    if (!x || !weight || !cu_seqlens || !out || !conv_state || !cache_indices) return CCC_ERR_NULL;
+    if (state_len < width - 1 || n_slots < 1) return CCC_ERR_SHAPE;
+    if (!state_layout_ok(n_slots, C, state_len, st_slot, st_c, st_l)) return CCC_ERR_SHAPE;
+    if (!aligned(x, 16) || !aligned(out, 16) || !aligned(conv_state, 2) || !aligned(cu_seqlens, 4) ||
+        !aligned(cache_indices, 4) || (num_accepted && !aligned(num_accepted, 4)))
+        return CCC_ERR_ALIGN;
+    if (!aligned(weight, dtype_size(w_dtype)) || (bias && !aligned(bias, dtype_size(b_dtype)))) return CCC_ERR_ALIGN;
+    const Span s_x = span(x, mat_bytes(rows, x_row_stride, C));
+    const Span s_out = span(out, mat_bytes(rows, out_row_stride, C));
+    const Span s_w = span(weight, static_cast<size_t>(C) * width * dtype_size(w_dtype));
+    const Span s_b = span(bias, bias ? static_cast<size_t>(C) * dtype_size(b_dtype) : 0);
+    const int64_t last = (n_slots - 1) * st_slot + (C - 1) * st_c + (state_len - 1) * st_l;
+    const Span s_st = span(conv_state, static_cast<size_t>(last + 1) * 2);
+    const Span s_cu = span(cu_seqlens, static_cast<size_t>(N + 1) * 4);
+    const Span s_ci = span(cache_indices, static_cast<size_t>(N) * 4);
+    const Span s_na = span(num_accepted, static_cast<size_t>(N) * 4);
+    const Span *all[] = {&s_x, &s_out, &s_w, &s_b, &s_st, &s_cu, &s_ci, &s_na};
+    const Span *written[] = {&s_out, &s_st};
+    for (const Span *wsp : written)
+        for (const Span *o : all)
+            if (o != wsp && overlap(*wsp, *o)) return CCC_ERR_ALIAS;
+
+    g_last_launches = 0;
+    if (rows == 0 || N == 0) return CCC_OK;
+    ccc::UpdArgs a = {};
+    a.x = static_cast<const uint16_t *>(x);
+    a.rows = rows;
+    a.C = C;
+    a.xs = static_cast<int>(x_row_stride);
+    a.w = weight;
+    a.w_bf16 = w_dtype == CCC_BF16;
+    a.b = bias;
+    a.b_kind = bias ? (b_dtype == CCC_F32 ? 1 : 2) : 0;
+    a.width = width;
+    a.act = activation;
+    a.state = static_cast<uint16_t *>(conv_state);
+    a.n_slots = n_slots;
+    a.L = state_len;
+    a.st_slot = st_slot;
+    a.st_c = st_c;
+    a.st_l = st_l;
+    a.state_vec = st_c == 1 && st_slot % 8 == 0 && st_l % 8 == 0 && aligned(conv_state, 16);
+    a.state_stage = !a.state_vec && st_l == 1 && st_c == state_len && st_slot % 8 == 0 &&
+                    state_len <= ccc::update_stage_max_len() && aligned(conv_state, 16);
+    a.cu = cu_seqlens;
+    a.N = N;
+    a.cache = cache_indices;
+    a.accepted = num_accepted;
+    a.out = static_cast<uint16_t *>(out);
+    a.os = static_cast<int>(out_row_stride);
+    a.slabs = ccc::update_slabs(C);
+    if (ccc::launch_update(a, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return CCC_ERR_CUDA;
+    g_last_launches = 1;
     return CCC_OK;
 }
 

@@ -30,6 +30,11 @@
 // 3 rows before it, and only where it stops before the sequence end does it
 // read 3 rows past it (both from L2: the neighbouring warp's run).
 //
+// Widths and activation.  The kernel is a template over the width W (2..4:
+// W-1 history rows, W-1 initial-state gradients, W taps; Megatron-Core
+// causal_conv1d_cp, weight [D, W]) and the activation (SiLU, or none: then
+// dz = dy); W = 4 with SiLU is the contract above, and "3" reads W-1.
+//
 // Determinism.  The number of runs per slab R is fixed by (rows, N, C) only;
 // the warp with task (slab, run r) walks items [r*total/R, (r+1)*total/R) in
 // order and writes partial[r][k][c] for its channels, so every partial sum
@@ -42,13 +47,48 @@ namespace ccc {
 
 namespace {
 
+// One step of the walk for one channel pair: dz of the current row, the
+// dH accumulation (carry first, then tap k on dz_{i-k}: dz, dwin[0] =
+// dz_{i-1}, ...), all with the forward's operand order.
+template <int W, bool ACT, int NV>
+__device__ __forceinline__ float2 bwd_dz(const float2 (&wt)[W][NV], float2 b, const float2 (&hw)[W - 1][NV],
+                                         float2 hc, float2 gy, int v) {
+    if constexpr (ACT) {
+        return activate2_grad<true>(conv_pre<W, NV>(wt, b, hw, hc, v), gy);
+    } else {
+        return gy;
+    }
+}
+
+template <int W, int NV>
+__device__ __forceinline__ float2 bwd_dh(const float2 (&wt)[W][NV], float2 carry, float2 dz,
+                                         const float2 (&dwin)[W - 1][NV], int v) {
+    float2 c = __ffma2_rn(wt[0][v], dz, carry);
+#pragma unroll
+    for (int k = 1; k < W; ++k) c = __ffma2_rn(wt[k][v], dwin[k - 1][v], c);
+    return c;
+}
+
+// Move both windows one row on: dwin[0] = dz_i, hw[H-1] = h of row i.
+template <int W, int NV>
+__device__ __forceinline__ void bwd_shift(float2 (&hw)[W - 1][NV], float2 (&dwin)[W - 1][NV], float2 hc, float2 dz,
+                                          int v) {
+#pragma unroll
+    for (int k = W - 2; k > 0; --k) dwin[k][v] = dwin[k - 1][v];
+    dwin[0][v] = dz;
+#pragma unroll
+    for (int k = 0; k + 1 < W - 1; ++k) hw[k][v] = hw[k + 1][v];
+    hw[W - 2][v] = hc;
+}
+
 // P = 0: each lane loads its U rows of x and dy straight into registers.
 // P > 0: each lane streams the rows of its walk through a P-stage ring of
 // U-row batches in shared memory (cp.async), keeping up to P-1 batches in
 // flight ahead of the math.
-template <int VEC, int U, int P>
+template <int VEC, int U, int P, int W, bool ACT>
 __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const BwdArgs a) {
     constexpr int NV = VEC / 2;
+    constexpr int H = W - 1;                            // history rows
     constexpr int VB = VEC * 2;                         // bytes per lane per row
     constexpr int RING_WARP = P * U * 2 * 32 * VB;      // ring bytes per warp
     static_assert(P == 0 || kBwdChunk % U == 0, "items must be whole batches");
@@ -62,12 +102,16 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
     const bool full = (slab + 1) * 32 * VEC <= a.C;  // warp-uniform: all lanes have channels
     const int c0 = act ? cv * VEC : 0;
 
-    float2 w0[NV], w1[NV], w2[NV], w3[NV], bb[NV];
-    load_taps<NV>(a.w, a.w_bf16, a.b, a.b_kind, c0, act, w0, w1, w2, w3, bb);
+    float2 wt[W][NV], bb[NV];
+    load_taps_w<NV, W>(a.w, a.w_bf16, a.b, a.b_kind, c0, act, wt, bb);
 
-    float2 g0[NV], g1[NV], g2[NV], g3[NV], gb[NV];  // sum dz*h[j+k], sum dz
+    float2 g[W][NV], gb[NV];  // sum dz*h[j+k], sum dz
 #pragma unroll
-    for (int v = 0; v < NV; ++v) g0[v] = g1[v] = g2[v] = g3[v] = gb[v] = f2_zero();
+    for (int v = 0; v < NV; ++v) {
+#pragma unroll
+        for (int k = 0; k < W; ++k) g[k][v] = f2_zero();
+        gb[v] = f2_zero();
+    }
 
     grid_dependency_wait();  // the chunk map, when one was built
 
@@ -89,8 +133,9 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
     }
 
     // Sliding windows, carried from one item to the next when the next item
-    // continues the same sequence: history rows h[i..i+2] and dz_{i-1..i-3}.
-    float2 h0[NV], h1[NV], h2[NV], d1[NV], d2[NV], d3[NV];
+    // continues the same sequence: history rows h[i..i+H-1] and
+    // dz_{i-1..i-H}.
+    float2 hw[H][NV], dwin[H][NV];
     Item cur = {};
     bool live = true, read_state = false;
 
@@ -139,7 +184,7 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
         const bool next_cont = it + 1 < hi && t.r0 + t.nr < t.e;
         const int nr = t.nr;
         const int o0 = t.r0 - t.s, L = t.e - t.s;
-        float *dinit = a.d_init ? a.d_init + static_cast<int64_t>(t.n) * 3 * a.C + c0 : nullptr;
+        float *dinit = a.d_init ? a.d_init + static_cast<int64_t>(t.n) * H * a.C + c0 : nullptr;
 
         if (!live || L == 0) {  // zero gradient, no contribution
             if (act) {
@@ -147,7 +192,7 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
                 for (int r = 0; r < nr; ++r) st_stream<NV>(a.dx + static_cast<int64_t>(t.r0 + r) * a.dxs + c0, z);
                 if (o0 == 0 && dinit)
 #pragma unroll
-                    for (int p = 0; p < 3; ++p)
+                    for (int p = 0; p < H; ++p)
 #pragma unroll
                         for (int v = 0; v < NV; ++v)
                             reinterpret_cast<float2 *>(dinit + p * a.C)[v] = f2_zero();
@@ -158,48 +203,49 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
         if constexpr (P > 0) {
             if (!cont) {
                 // A new walk: the rows it will load are [t.r0, p_end) -- to the
-                // end of the sequence, or for the run's last sequence to 3 rows
+                // end of the sequence, or for the run's last sequence to H rows
                 // past the run (within the sequence).
                 cp_async_wait(0);
                 p_row = t.r0;
-                p_end = t.n == last_n ? min(last_end + 3, t.e) : t.e;
+                p_end = t.n == last_n ? min(last_end + H, t.e) : t.e;
                 issued = consumed = 0;
                 while (issued < P - 1 && p_row < p_end) issue();
             }
         }
         if (!cont) {
-            // History rows o0-3 .. o0-1 (the initial history for a first item).
-            Raw<NV> hr[3];
+            // History rows o0-H .. o0-1 (the initial history for a first item).
+            Raw<NV> hr[H];
 #pragma unroll
-            for (int p = 0; p < 3; ++p) hr[p] = raw_zero<NV>();
+            for (int p = 0; p < H; ++p) hr[p] = raw_zero<NV>();
             if (act) {
                 if (o0 > 0) {
 #pragma unroll
-                    for (int p = 0; p < 3; ++p) hr[p] = ld_ro<NV>(a.x + static_cast<int64_t>(t.r0 - 3 + p) * a.xs + c0);
+                    for (int p = 0; p < H; ++p) hr[p] = ld_ro<NV>(a.x + static_cast<int64_t>(t.r0 - H + p) * a.xs + c0);
                 } else if (a.hist) {
 #pragma unroll
-                    for (int p = 0; p < 3; ++p)
-                        hr[p] = ld_ro<NV>(a.hist + (static_cast<int64_t>(t.n) * 3 + p) * a.C + c0);
+                    for (int p = 0; p < H; ++p)
+                        hr[p] = ld_ro<NV>(a.hist + (static_cast<int64_t>(t.n) * H + p) * a.C + c0);
                 }
             }
-            unpack<NV>(hr[0], h0);
-            unpack<NV>(hr[1], h1);
-            unpack<NV>(hr[2], h2);
 #pragma unroll
-            for (int v = 0; v < NV; ++v) d1[v] = d2[v] = d3[v] = f2_zero();
+            for (int p = 0; p < H; ++p) unpack<NV>(hr[p], hw[p]);
+#pragma unroll
+            for (int p = 0; p < H; ++p)
+#pragma unroll
+                for (int v = 0; v < NV; ++v) dwin[p][v] = f2_zero();
         }
 
         // i = o0 + k.  Rows k < nr are this item's; when the next item does
-        // not continue the walk, 3 more steps finish dx of the last 3 rows
+        // not continue the walk, H more steps finish dx of the last H rows
         // (loading x / dy past the item while still inside the sequence).
-        const int iters = nr + (next_cont ? 0 : 3);
+        const int iters = nr + (next_cont ? 0 : H);
         const int nload = L - o0 < iters ? L - o0 : iters;  // steps with i < L
         for (int base = 0; base < iters; base += U) {
             // Steady state: every step of the batch loads a row, is one of
-            // this item's tokens and emits dx of the row 3 back (no carry:
+            // this item's tokens and emits dx of the row H back (no carry:
             // all i < L).  Such batches run guard-free; the first batch of a
             // walk and the tail take the general path.
-            const bool fast = full && (cont || base >= 3) && base + U <= nload && base + U <= nr;
+            const bool fast = full && (cont || base >= H) && base + U <= nload && base + U <= nr;
             Raw<NV> xr[U], gr[U];
             if constexpr (P == 0) {
                 if (fast) {  // all lanes, all rows: unconditional loads, stepping row pointers
@@ -248,32 +294,23 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
             }
 
             if (fast) {
-                uint16_t *dxp = a.dx + static_cast<int64_t>(t.r0 + base - 3) * a.dxs + c0;
+                uint16_t *dxp = a.dx + static_cast<int64_t>(t.r0 + base - H) * a.dxs + c0;
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    float2 hc[NV], gy[NV], dz[NV];
+                    float2 hc[NV], gy[NV];
                     unpack<NV>(xr[u], hc);
                     unpack<NV>(gr[u], gy);
                     Raw<NV> o;
 #pragma unroll
                     for (int v = 0; v < NV; ++v) {
-                        dz[v] = silu_grad(bb[v], w0[v], w1[v], w2[v], w3[v], h0[v], h1[v], h2[v], hc[v], gy[v]);
-                        g0[v] = __ffma2_rn(dz[v], h0[v], g0[v]);
-                        g1[v] = __ffma2_rn(dz[v], h1[v], g1[v]);
-                        g2[v] = __ffma2_rn(dz[v], h2[v], g2[v]);
-                        g3[v] = __ffma2_rn(dz[v], hc[v], g3[v]);
-                        gb[v] = __fadd2_rn(gb[v], dz[v]);
-                        float2 c = __ffma2_rn(w0[v], dz[v], f2_zero());  // no carry (same op as the general path)
-                        c = __ffma2_rn(w1[v], d1[v], c);
-                        c = __ffma2_rn(w2[v], d2[v], c);
-                        c = __ffma2_rn(w3[v], d3[v], c);
-                        o.u[v] = f2_to_bf2(c);
-                        d3[v] = d2[v];
-                        d2[v] = d1[v];
-                        d1[v] = dz[v];
-                        h0[v] = h1[v];
-                        h1[v] = h2[v];
-                        h2[v] = hc[v];
+                        const float2 dz = bwd_dz<W, ACT, NV>(wt, bb[v], hw, hc[v], gy[v], v);
+#pragma unroll
+                        for (int k = 0; k < H; ++k) g[k][v] = __ffma2_rn(dz, hw[k][v], g[k][v]);
+                        g[H][v] = __ffma2_rn(dz, hc[v], g[H][v]);
+                        gb[v] = __fadd2_rn(gb[v], dz);
+                        // no carry (same op as the general path)
+                        o.u[v] = f2_to_bf2(bwd_dh<W, NV>(wt, f2_zero(), dz, dwin, v));
+                        bwd_shift<W, NV>(hw, dwin, hc[v], dz, v);
                     }
                     st_stream<NV>(dxp, o);
                     dxp += a.dxs;
@@ -292,8 +329,7 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
                     float2 gy[NV];
                     unpack<NV>(gr[u], gy);
 #pragma unroll
-                    for (int v = 0; v < NV; ++v)
-                        dz[v] = silu_grad(bb[v], w0[v], w1[v], w2[v], w3[v], h0[v], h1[v], h2[v], hc[v], gy[v]);
+                    for (int v = 0; v < NV; ++v) dz[v] = bwd_dz<W, ACT, NV>(wt, bb[v], hw, hc[v], gy[v], v);
                 } else {
 #pragma unroll
                     for (int v = 0; v < NV; ++v) dz[v] = f2_zero();
@@ -301,40 +337,33 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
                 if (k < nr) {  // this item's own token: weight / bias partials
 #pragma unroll
                     for (int v = 0; v < NV; ++v) {
-                        g0[v] = __ffma2_rn(dz[v], h0[v], g0[v]);
-                        g1[v] = __ffma2_rn(dz[v], h1[v], g1[v]);
-                        g2[v] = __ffma2_rn(dz[v], h2[v], g2[v]);
-                        g3[v] = __ffma2_rn(dz[v], hc[v], g3[v]);
+#pragma unroll
+                        for (int j = 0; j < H; ++j) g[j][v] = __ffma2_rn(dz[v], hw[j][v], g[j][v]);
+                        g[H][v] = __ffma2_rn(dz[v], hc[v], g[H][v]);
                         gb[v] = __fadd2_rn(gb[v], dz[v]);
                     }
                 }
-                // dH[i] is complete now.  i < 3: an initial-history gradient.
-                // Otherwise it is dx of row i-3, ours unless this is the first
+                // dH[i] is complete now.  i < H: an initial-history gradient.
+                // Otherwise it is dx of row i-H, ours unless this is the first
                 // step of a walk that starts inside a sequence (then the
                 // previous item's owner finished that row).
-                const bool emit_init = i < 3 && dinit != nullptr;
-                const bool emit_dx = i >= 3 && (cont || k >= 3);
+                const bool emit_init = i < H && dinit != nullptr;
+                const bool emit_dx = i >= H && (cont || k >= H);
                 if (emit_dx || emit_init) {
                     const bool carry = i >= L && a.d_final != nullptr;
                     const float2 *cp = carry ? reinterpret_cast<const float2 *>(
-                                                   a.d_final + (static_cast<int64_t>(t.n) * 3 + (i - L)) * a.C + c0)
+                                                   a.d_final + (static_cast<int64_t>(t.n) * H + (i - L)) * a.C + c0)
                                              : nullptr;
                     float2 acc[NV];
 #pragma unroll
-                    for (int v = 0; v < NV; ++v) {
-                        float2 c = (carry && act) ? __ldg(cp + v) : f2_zero();
-                        c = __ffma2_rn(w0[v], dz[v], c);
-                        c = __ffma2_rn(w1[v], d1[v], c);
-                        c = __ffma2_rn(w2[v], d2[v], c);
-                        c = __ffma2_rn(w3[v], d3[v], c);
-                        acc[v] = c;
-                    }
+                    for (int v = 0; v < NV; ++v)
+                        acc[v] = bwd_dh<W, NV>(wt, (carry && act) ? __ldg(cp + v) : f2_zero(), dz[v], dwin, v);
                     if (act) {
                         if (emit_dx) {
                             Raw<NV> o;
 #pragma unroll
                             for (int v = 0; v < NV; ++v) o.u[v] = f2_to_bf2(acc[v]);
-                            st_stream<NV>(a.dx + static_cast<int64_t>(t.s + i - 3) * a.dxs + c0, o);
+                            st_stream<NV>(a.dx + static_cast<int64_t>(t.s + i - H) * a.dxs + c0, o);
                         } else {
                             float2 *dp = reinterpret_cast<float2 *>(dinit + static_cast<int64_t>(i) * a.C);
 #pragma unroll
@@ -343,14 +372,7 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
                     }
                 }
 #pragma unroll
-                for (int v = 0; v < NV; ++v) {
-                    d3[v] = d2[v];
-                    d2[v] = d1[v];
-                    d1[v] = dz[v];
-                    h0[v] = h1[v];
-                    h1[v] = h2[v];
-                    h2[v] = hc[v];
-                }
+                for (int v = 0; v < NV; ++v) bwd_shift<W, NV>(hw, dwin, hc[v], dz[v], v);
             }
         }
     }
@@ -358,44 +380,66 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
     // Let the reduce kernel get scheduled while this warp stores its sums.
     grid_dependents_launch();
 
-    // partial[run][k][c0 .. c0+VEC) for k = 0..3 (taps) and 4 (bias).
+    // partial[run][k][c0 .. c0+VEC) for k = 0..W-1 (taps) and 4 (bias).
     if (act) {
         float *pp = a.part + static_cast<int64_t>(run) * 5 * a.C + c0;
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
-            reinterpret_cast<float2 *>(pp + 0 * a.C)[v] = g0[v];
-            reinterpret_cast<float2 *>(pp + 1 * a.C)[v] = g1[v];
-            reinterpret_cast<float2 *>(pp + 2 * a.C)[v] = g2[v];
-            reinterpret_cast<float2 *>(pp + 3 * a.C)[v] = g3[v];
+#pragma unroll
+            for (int k = 0; k < W; ++k) reinterpret_cast<float2 *>(pp + k * a.C)[v] = g[k][v];
             reinterpret_cast<float2 *>(pp + 4 * a.C)[v] = gb[v];
         }
     }
 }
 
-// dweight[c][k] = sum_{r=0..runs-1} part[r][k][c] (k < 4), dbias[c] likewise
-// with k = 4: one thread per output, fixed order.
+// dweight[c][k] = sum_{r=0..runs-1} part[r][k][c] (k < W), dbias[c] likewise
+// with row 4: one thread per output, fixed order.
 // The partials are written by the backward grid, which may still be running
 // when this grid becomes resident (programmatic dependent launch): they are
 // read with L2-coherent loads, not through the read-only path.
-__global__ void __launch_bounds__(256) reduce_kernel(const float *part, int G, int C, float *dweight,
+__global__ void __launch_bounds__(256) reduce_kernel(const float *part, int G, int C, int W, float *dweight,
                                                      float *dbias) {
     grid_dependency_wait();  // the backward's partials
     const int idx = blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= 5 * C) return;
     const int k = idx / C, c = idx % C;
+    if (k >= W && k < 4) return;  // tap rows a narrower stencil does not have
+    if (k == 4 && !dbias) return;
     const float *p = part + static_cast<int64_t>(k) * C + c;
     float s = __ldcg(p);
     for (int g = 1; g < G; ++g) s += __ldcg(p + static_cast<int64_t>(g) * 5 * C);
     if (k < 4) {
-        dweight[4 * c + k] = s;
-    } else if (dbias) {
+        dweight[W * c + k] = s;
+    } else {
         dbias[c] = s;
+    }
+}
+
+using BwdKernel = void (*)(const BwdArgs);
+
+template <int W, bool ACT>
+constexpr BwdKernel bwd_kernel_of() {
+    return bwd_kernel<kBwdVec, kBwdUnroll, kBwdRing, W, ACT>;
+}
+
+// The instantiation for (width, activation); nullptr for an unsupported pair.
+BwdKernel bwd_kernel_for(int width, int act) {
+    switch (width * 2 + (act ? 1 : 0)) {
+        case 4: return bwd_kernel_of<2, false>();
+        case 5: return bwd_kernel_of<2, true>();
+        case 6: return bwd_kernel_of<3, false>();
+        case 7: return bwd_kernel_of<3, true>();
+        case 8: return bwd_kernel_of<4, false>();
+        case 9: return bwd_kernel_of<4, true>();
+        default: return nullptr;
     }
 }
 
 }  // namespace
 
 cudaError_t launch_bwd(const BwdArgs &a, bool pdl, cudaStream_t st) {
+    const BwdKernel kern = bwd_kernel_for(a.width, a.act);
+    if (!kern) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(static_cast<int64_t>(a.slabs) * a.runs, kWarpsPerCta)));
     cfg.blockDim = dim3(kCtaThreads);
@@ -409,24 +453,25 @@ cudaError_t launch_bwd(const BwdArgs &a, bool pdl, cudaStream_t st) {
     }
     constexpr int P = kBwdRing;
     constexpr size_t ring_bytes = static_cast<size_t>(P) * kBwdUnroll * 2 * 32 * kBwdVec * 2 * kWarpsPerCta;
-    auto kern = bwd_kernel<kBwdVec, kBwdUnroll, P>;
     if (ring_bytes > 48 * 1024) {
-        // Opt in to more than 48 KB of dynamic shared memory, once per device.
-        static bool attr_set[64] = {};
+        // Opt in to more than 48 KB of dynamic shared memory, once per device
+        // and instantiation.
+        static bool attr_set[64][6] = {};
+        const int slot = (a.width - 2) * 2 + (a.act ? 1 : 0);
         int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
-        if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+        if (dev < 0 || dev >= 64 || !attr_set[dev][slot]) {
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ring_bytes));
             if (e != cudaSuccess) return e;
-            if (dev >= 0 && dev < 64) attr_set[dev] = true;
+            if (dev >= 0 && dev < 64) attr_set[dev][slot] = true;
         }
     }
     cfg.dynamicSmemBytes = ring_bytes;
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-cudaError_t launch_reduce(const float *part, int G, int C, float *dweight, float *dbias, bool pdl,
+cudaError_t launch_reduce(const float *part, int G, int C, int width, float *dweight, float *dbias, bool pdl,
                           cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(5 * static_cast<int64_t>(C), 256)));
@@ -439,7 +484,7 @@ cudaError_t launch_reduce(const float *part, int G, int C, float *dweight, float
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, reduce_kernel, part, G, C, dweight, dbias);
+    return cudaLaunchKernelEx(&cfg, reduce_kernel, part, G, C, width, dweight, dbias);
 }
 
 }  // namespace ccc

@@ -302,6 +302,80 @@ __device__ __forceinline__ void load_taps(const void *w, int w_bf16, const void 
     }
 }
 
+// Taps [C][W] (FP32 or BF16) and bias [C] (FP32 / BF16 / none) for a
+// width-W kernel, read once per lane: wt[k][v] holds tap k of channels
+// c0+2v, c0+2v+1 (Megatron-Core "core.ssm.causal_conv1d", causal_conv1d_cp:
+// weight [D, W]).
+template <int NV, int W>
+__device__ __forceinline__ void load_taps_w(const void *w, int w_bf16, const void *b, int b_kind, int c0,
+                                            bool act, float2 (&wt)[W][NV], float2 (&bb)[NV]) {
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        float t[2][W], bv[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int c = c0 + 2 * v + h;
+#pragma unroll
+            for (int k = 0; k < W; ++k) {
+                float val = 0.0f;
+                if (act) {
+                    if (w_bf16) {
+                        val = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(w)[W * c + k]);
+                    } else {
+                        val = __ldg(reinterpret_cast<const float *>(w) + W * c + k);
+                    }
+                }
+                t[h][k] = val;
+            }
+            float bval = 0.0f;
+            if (act && b_kind == 1) bval = __ldg(reinterpret_cast<const float *>(b) + c);
+            if (act && b_kind == 2) bval = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(b)[c]);
+            bv[h] = bval;
+        }
+#pragma unroll
+        for (int k = 0; k < W; ++k) wt[k][v] = make_float2(t[0][k], t[1][k]);
+        bb[v] = make_float2(bv[0], bv[1]);
+    }
+}
+
+// Pre-activation of one channel pair for a width-W stencil: the bias, then
+// tap k on history row k (k < W-1, oldest first), then tap W-1 on the
+// current row -- the FMA order of FlashInfer causal_conv1d_fn (bias added
+// before the FMAs).  hw[k] is history row k of this pair.
+template <int W, int NV>
+__device__ __forceinline__ float2 conv_pre(const float2 (&wt)[W][NV], float2 b, const float2 (&hw)[W - 1][NV],
+                                           float2 hc, int v) {
+    float2 z = b;
+#pragma unroll
+    for (int k = 0; k < W - 1; ++k) z = __ffma2_rn(wt[k][v], hw[k][v], z);
+    return __ffma2_rn(wt[W - 1][v], hc, z);
+}
+
+// Output of the activation: SiLU z * sigmoid(z), or z itself.
+template <bool ACT>
+__device__ __forceinline__ float2 activate2(float2 z) {
+    if constexpr (ACT) {
+        return __fmul2_rn(z, sigmoid2(z));
+    } else {
+        return z;
+    }
+}
+
+// dz = dy * d act / dz: dy * s * (1 + z * (1 - s)) with s = sigmoid(z) for
+// SiLU, dy itself without activation.
+template <bool ACT>
+__device__ __forceinline__ float2 activate2_grad(float2 z, float2 gy) {
+    if constexpr (ACT) {
+        const float2 s = sigmoid2(z);
+        const float2 one = make_float2(1.0f, 1.0f);
+        const float2 oms = __ffma2_rn(s, make_float2(-1.0f, -1.0f), one);  // 1 - s
+        const float2 f = __ffma2_rn(z, oms, one);
+        return __fmul2_rn(gy, __fmul2_rn(s, f));
+    } else {
+        return gy;
+    }
+}
+
 // ---------------------------------------------------------- work items --
 //
 // A work item is (sequence n, first row r0, rows nr <= B) inside one

@@ -1,5 +1,5 @@
-// ccc_fwd.cu -- forward kernel: packed width-4 causal depthwise Conv1d +
-// SiLU with the conv_state gather/scatter fused in.
+// ccc_fwd.cu -- forward kernel: packed causal depthwise Conv1d (+ SiLU)
+// with the conv_state gather/scatter fused in.
 //
 // FlashInfer "flashinfer.mamba.causal_conv1d_fn" (Parameters): for token j of
 // sequence n and channel c, z = bias + w0*h[j] + w1*h[j+1] + w2*h[j+2] +
@@ -7,7 +7,11 @@
 // out = BF16(z * sigmoid(z)); h starts with three state values (slot
 // cache_indices[n], positions 0:3, when has_initial_state[n]) or zeros; a -1
 // slot gives zero output and no state access; each nonempty live sequence
-// leaves its last three raw history values in positions 0:3.
+// leaves its last three raw history values in positions 0:3.  The kernel is
+// a template over the width W (2..4: W-1 history rows and state positions,
+// Megatron-Core "core.ssm.causal_conv1d", causal_conv1d_cp: weight [D, W])
+// and the activation (SiLU or none, the same page's `activation`); W = 4
+// with SiLU is FlashInfer's contract.
 //
 // Mapping.  A warp owns one (work item, 32*VEC-channel slab): up to B rows
 // of one sequence.  Lane l holds channels [c0, c0+VEC) with c0 = (slab*32 +
@@ -34,60 +38,69 @@ namespace ccc {
 
 namespace {
 
-template <int NV>
-__device__ __forceinline__ void gather_state(const FwdArgs &a, int q, int c0, Raw<NV> (&hr)[3]) {
-    const uint16_t *base = a.state + static_cast<int64_t>(q) * a.st_slot;
-    if (a.state_vec) {
+// State positions 0..H-1 of slot q (position 0 = oldest), or the window of
+// positions p0 .. p0+H-1 for the speculative update.
+template <int NV, int H>
+__device__ __forceinline__ void gather_state(const uint16_t *state, int64_t st_slot, int64_t st_c, int64_t st_l,
+                                             bool vec, int q, int p0, int c0, Raw<NV> (&hr)[H]) {
+    const uint16_t *base = state + static_cast<int64_t>(q) * st_slot + static_cast<int64_t>(p0) * st_l;
+    if (vec) {
 #pragma unroll
-        for (int p = 0; p < 3; ++p) hr[p] = ld_rw<NV>(base + p * a.st_l + c0);
+        for (int p = 0; p < H; ++p) hr[p] = ld_rw<NV>(base + p * st_l + c0);
     } else {
 #pragma unroll
-        for (int p = 0; p < 3; ++p) {
+        for (int p = 0; p < H; ++p) {
 #pragma unroll
             for (int v = 0; v < NV; ++v) {
-                const uint32_t lo = base[(c0 + 2 * v) * a.st_c + p * a.st_l];
-                const uint32_t hi = base[(c0 + 2 * v + 1) * a.st_c + p * a.st_l];
+                const uint32_t lo = base[(c0 + 2 * v) * st_c + p * st_l];
+                const uint32_t hi = base[(c0 + 2 * v + 1) * st_c + p * st_l];
                 hr[p].u[v] = lo | (hi << 16);
             }
         }
     }
 }
 
+// One state position p of slot q for this lane's channels.
 template <int NV>
-__device__ __forceinline__ void scatter_state(const FwdArgs &a, int q, int c0, const Raw<NV> (&fin)[3]) {
-    uint16_t *base = a.state + static_cast<int64_t>(q) * a.st_slot;
-    if (a.state_vec) {
-#pragma unroll
-        for (int p = 0; p < 3; ++p) st_plain<NV>(base + p * a.st_l + c0, fin[p]);
+__device__ __forceinline__ void put_state(uint16_t *state, int64_t st_slot, int64_t st_c, int64_t st_l, bool vec,
+                                          int q, int p, int c0, const Raw<NV> &val) {
+    uint16_t *base = state + static_cast<int64_t>(q) * st_slot + static_cast<int64_t>(p) * st_l;
+    if (vec) {
+        st_plain<NV>(base + c0, val);
     } else {
 #pragma unroll
-        for (int p = 0; p < 3; ++p) {
-#pragma unroll
-            for (int v = 0; v < NV; ++v) {
-                base[(c0 + 2 * v) * a.st_c + p * a.st_l] = static_cast<uint16_t>(fin[p].u[v] & 0xffffu);
-                base[(c0 + 2 * v + 1) * a.st_c + p * a.st_l] = static_cast<uint16_t>(fin[p].u[v] >> 16);
-            }
+        for (int v = 0; v < NV; ++v) {
+            base[(c0 + 2 * v) * st_c] = static_cast<uint16_t>(val.u[v] & 0xffffu);
+            base[(c0 + 2 * v + 1) * st_c] = static_cast<uint16_t>(val.u[v] >> 16);
         }
     }
 }
 
-// SiLU(z) for z = b + w0 h0 + w1 h1 + w2 h2 + w3 hc (bias first, then the four
-// FMAs in tap order), on a pair of channels.
-__device__ __forceinline__ float2 silu_pre(float2 b, float2 w0, float2 w1, float2 w2, float2 w3, float2 h0,
-                                           float2 h1, float2 h2, float2 hc) {
-    float2 z = __ffma2_rn(w0, h0, b);
-    z = __ffma2_rn(w1, h1, z);
-    z = __ffma2_rn(w2, h2, z);
-    z = __ffma2_rn(w3, hc, z);
-    return __fmul2_rn(z, sigmoid2(z));
+// One output row: y = act(conv_pre) for the VEC channels of this lane, then
+// the history window moves one row on (hw[0] oldest .. hw[H-1] newest).
+template <int W, bool ACT, int NV>
+__device__ __forceinline__ Raw<NV> fwd_row(const float2 (&wt)[W][NV], const float2 (&bb)[NV],
+                                           float2 (&hw)[W - 1][NV], const Raw<NV> &xr) {
+    float2 hc[NV];
+    unpack<NV>(xr, hc);
+    Raw<NV> y;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        y.u[v] = f2_to_bf2(activate2<ACT>(conv_pre<W, NV>(wt, bb[v], hw, hc[v], v)));
+#pragma unroll
+        for (int k = 0; k + 1 < W - 1; ++k) hw[k][v] = hw[k + 1][v];
+        hw[W - 2][v] = hc[v];
+    }
+    return y;
 }
 
 // P = 0: rows are loaded straight into registers, U per batch.  P > 0: each
 // lane streams its run's rows through a P-stage shared-memory ring
 // (LaneRing, cp.async), so loads run ahead of the math.
-template <int VEC, int U, int P>
+template <int VEC, int U, int P, int W, bool ACT>
 __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const FwdArgs a) {
     constexpr int NV = VEC / 2;
+    constexpr int H = W - 1;  // history rows
     extern __shared__ __align__(16) unsigned char fwd_smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int gw = blockIdx.x * kWarpsPerCta + warp;  // this warp's task
@@ -98,8 +111,8 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
     const bool full = (slab + 1) * 32 * VEC <= a.C;  // warp-uniform: all lanes have channels
     const int c0 = act ? cv * VEC : 0;
 
-    float2 w0[NV], w1[NV], w2[NV], w3[NV], bb[NV];
-    load_taps<NV>(a.w, a.w_bf16, a.b, a.b_kind, c0, act, w0, w1, w2, w3, bb);
+    float2 wt[W][NV], bb[NV];
+    load_taps_w<NV, W>(a.w, a.w_bf16, a.b, a.b_kind, c0, act, wt, bb);
 
     grid_dependency_wait();  // the chunk map, when one was built
 
@@ -110,7 +123,7 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
     const int lo = static_cast<int>(static_cast<int64_t>(run) * dec.total / a.runs);
     const int hi = static_cast<int>(static_cast<int64_t>(run + 1) * dec.total / a.runs);
 
-    float2 h0[NV], h1[NV], h2[NV];  // the three rows before the current one
+    float2 hw[H][NV];  // the H rows before the current one, oldest first
 
     using Ring = LaneRing<NV, U, (P > 0 ? P : 1), 1>;
     Ring ring;
@@ -119,11 +132,11 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
         ring.src[0] = a.x + c0;
         ring.stride[0] = a.xs;
         if (lo < hi) {
-            // The run's rows: from its first item (and the 3 rows before it
+            // The run's rows: from its first item (and the H rows before it
             // when it starts inside a sequence) to the end of its last item.
             const Item f = dec.get(lo, a.map, a.cu, a.rows);
             const Item l = dec.get(hi - 1, a.map, a.cu, a.rows);
-            ring.start(f.r0 > f.s ? f.r0 - 3 : f.r0, l.r0 + l.nr);
+            ring.start(f.r0 > f.s ? f.r0 - H : f.r0, l.r0 + l.nr);
         } else {
             ring.start(0, 0);
         }
@@ -157,8 +170,8 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
                 for (int r = 0; r < nr; ++r) st_stream<NV>(orow + static_cast<int64_t>(r) * a.os, z);
                 if (o0 == 0 && a.hist)
 #pragma unroll
-                    for (int p = 0; p < 3; ++p)
-                        st_plain<NV>(a.hist + (static_cast<int64_t>(t.n) * 3 + p) * a.C + c0, z);
+                    for (int p = 0; p < H; ++p)
+                        st_plain<NV>(a.hist + (static_cast<int64_t>(t.n) * H + p) * a.C + c0, z);
             }
             continue;
         }
@@ -166,28 +179,27 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
         const bool rd = o0 == 0 && pool && has_init_n;
 
         if (!cont) {
-            // The three history rows before r0 (raw BF16 bits): the initial
+            // The H history rows before r0 (raw BF16 bits): the initial
             // state (or zeros) for a sequence's first item, else x rows.
-            Raw<NV> hr[3];
+            Raw<NV> hr[H];
 #pragma unroll
-            for (int p = 0; p < 3; ++p) hr[p] = raw_zero<NV>();
+            for (int p = 0; p < H; ++p) hr[p] = raw_zero<NV>();
             if (o0 == 0) {
-                if (rd && act) gather_state<NV>(a, q, c0, hr);
+                if (rd && act) gather_state<NV, H>(a.state, a.st_slot, a.st_c, a.st_l, a.state_vec, q, 0, c0, hr);
                 if (a.hist && act)
 #pragma unroll
-                    for (int p = 0; p < 3; ++p)
-                        st_plain<NV>(a.hist + (static_cast<int64_t>(t.n) * 3 + p) * a.C + c0, hr[p]);
+                    for (int p = 0; p < H; ++p)
+                        st_plain<NV>(a.hist + (static_cast<int64_t>(t.n) * H + p) * a.C + c0, hr[p]);
             } else if constexpr (P > 0) {
-                ring.top_up(t.r0 - 3, act);
+                ring.top_up(t.r0 - H, act);
 #pragma unroll
-                for (int p = 0; p < 3; ++p) hr[p] = ring.get(t.r0 - 3 + p, 0);
+                for (int p = 0; p < H; ++p) hr[p] = ring.get(t.r0 - H + p, 0);
             } else if (act) {
 #pragma unroll
-                for (int p = 0; p < 3; ++p) hr[p] = ld_ro<NV>(xrow - static_cast<int64_t>(3 - p) * a.xs);
+                for (int p = 0; p < H; ++p) hr[p] = ld_ro<NV>(xrow - static_cast<int64_t>(H - p) * a.xs);
             }
-            unpack<NV>(hr[0], h0);
-            unpack<NV>(hr[1], h1);
-            unpack<NV>(hr[2], h2);
+#pragma unroll
+            for (int p = 0; p < H; ++p) unpack<NV>(hr[p], hw[p]);
         }
 
         int base = 0;
@@ -200,16 +212,7 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     if (base + u >= nr) break;
-                    float2 hc[NV];
-                    unpack<NV>(cur[u], hc);
-                    Raw<NV> y;
-#pragma unroll
-                    for (int v = 0; v < NV; ++v) {
-                        y.u[v] = f2_to_bf2(silu_pre(bb[v], w0[v], w1[v], w2[v], w3[v], h0[v], h1[v], h2[v], hc[v]));
-                        h0[v] = h1[v];
-                        h1[v] = h2[v];
-                        h2[v] = hc[v];
-                    }
+                    const Raw<NV> y = fwd_row<W, ACT, NV>(wt, bb, hw, cur[u]);
                     if (act) st_stream<NV>(orow + static_cast<int64_t>(base + u) * a.os, y);
                 }
             }
@@ -234,17 +237,7 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
                 }
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    float2 hc[NV];
-                    unpack<NV>(cur[u], hc);
-                    Raw<NV> y;
-#pragma unroll
-                    for (int v = 0; v < NV; ++v) {
-                        y.u[v] = f2_to_bf2(silu_pre(bb[v], w0[v], w1[v], w2[v], w3[v], h0[v], h1[v], h2[v], hc[v]));
-                        h0[v] = h1[v];
-                        h1[v] = h2[v];
-                        h2[v] = hc[v];
-                    }
-                    st_stream<NV>(op, y);
+                    st_stream<NV>(op, fwd_row<W, ACT, NV>(wt, bb, hw, cur[u]));
                     op += a.os;
                 }
                 xp = lp;
@@ -259,38 +252,34 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 if (base + u >= nr) break;
-                float2 hc[NV];
-                unpack<NV>(cur[u], hc);
-                Raw<NV> y;
-#pragma unroll
-                for (int v = 0; v < NV; ++v) {
-                    y.u[v] = f2_to_bf2(silu_pre(bb[v], w0[v], w1[v], w2[v], w3[v], h0[v], h1[v], h2[v], hc[v]));
-                    h0[v] = h1[v];
-                    h1[v] = h2[v];
-                    h2[v] = hc[v];
-                }
+                const Raw<NV> y = fwd_row<W, ACT, NV>(wt, bb, hw, cur[u]);
                 if (act) st_stream<NV>(orow + static_cast<int64_t>(base + u) * a.os, y);
             }
         }
 
-        // Final three raw history values h[L], h[L+1], h[L+2] -> positions
-        // 0:3, by the warp that read the initial ones (read before write).
+        // Final H raw history values h[L .. L+H) -> positions 0:H, by the
+        // warp that read the initial ones (read before write).
         if (o0 == 0 && pool && L > 0 && act) {
-            Raw<NV> init[3];
+            Raw<NV> init[H];
 #pragma unroll
-            for (int p = 0; p < 3; ++p) init[p] = raw_zero<NV>();
-            if (rd && L < 3) gather_state<NV>(a, q, c0, init);  // still unwritten
-            Raw<NV> fin[3];
+            for (int p = 0; p < H; ++p) init[p] = raw_zero<NV>();
+            if (rd && L < H)  // still unwritten
+                gather_state<NV, H>(a.state, a.st_slot, a.st_c, a.st_l, a.state_vec, q, 0, c0, init);
+            Raw<NV> fin[H];
 #pragma unroll
-            for (int p = 0; p < 3; ++p) {
+            for (int p = 0; p < H; ++p) {
                 const int idx = L + p;
-                if (idx >= 3) {
-                    fin[p] = ld_ro<NV>(a.x + static_cast<int64_t>(t.s + idx - 3) * a.xs + c0);
+                if (idx >= H) {
+                    fin[p] = ld_ro<NV>(a.x + static_cast<int64_t>(t.s + idx - H) * a.xs + c0);
                 } else {
-                    fin[p] = idx == 0 ? init[0] : (idx == 1 ? init[1] : init[2]);
+                    fin[p] = init[0];
+#pragma unroll
+                    for (int j = 1; j < H; ++j)
+                        if (idx == j) fin[p] = init[j];
                 }
             }
-            scatter_state<NV>(a, q, c0, fin);
+#pragma unroll
+            for (int p = 0; p < H; ++p) put_state<NV>(a.state, a.st_slot, a.st_c, a.st_l, a.state_vec, q, p, c0, fin[p]);
         }
     }
 }
@@ -302,37 +291,58 @@ constexpr size_t kFwdRingBytes =
                        kWarpsPerCta
                  : 0;
 
-// Opt in to more than 48 KB of dynamic shared memory, once per device.
-cudaError_t fwd_prepare() {
+template <int W, bool ACT>
+constexpr auto fwd_kernel_of() {
+    return fwd_kernel<kFwdVec, kFwdUnroll, kFwdRing, W, ACT>;
+}
+
+using FwdKernel = void (*)(const FwdArgs);
+
+// The instantiation for (width, activation); nullptr for an unsupported pair.
+FwdKernel fwd_kernel_for(int width, int act) {
+    switch (width * 2 + (act ? 1 : 0)) {
+        case 4: return fwd_kernel_of<2, false>();
+        case 5: return fwd_kernel_of<2, true>();
+        case 6: return fwd_kernel_of<3, false>();
+        case 7: return fwd_kernel_of<3, true>();
+        case 8: return fwd_kernel_of<4, false>();
+        case 9: return fwd_kernel_of<4, true>();
+        default: return nullptr;
+    }
+}
+
+// Opt in to more than 48 KB of dynamic shared memory, once per device and
+// instantiation.
+cudaError_t fwd_prepare(FwdKernel kern, int slot) {
     if (kFwdRingBytes <= 48 * 1024) return cudaSuccess;
-    static bool attr_set[64] = {};
+    static bool attr_set[64][6] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64 && attr_set[dev]) return cudaSuccess;
-    e = cudaFuncSetAttribute(fwd_kernel<kFwdVec, kFwdUnroll, kFwdRing>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kFwdRingBytes));
-    if (e == cudaSuccess && dev >= 0 && dev < 64) attr_set[dev] = true;
+    if (dev >= 0 && dev < 64 && attr_set[dev][slot]) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kFwdRingBytes));
+    if (e == cudaSuccess && dev >= 0 && dev < 64) attr_set[dev][slot] = true;
     return e;
 }
 
 int fwd_ctas_per_sm() {
     int n = 0;
-    if (fwd_prepare() != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_kernel<kFwdVec, kFwdUnroll, kFwdRing>, kCtaThreads,
-                                                      kFwdRingBytes) != cudaSuccess ||
-        n < 1)
+    const FwdKernel kern = fwd_kernel_for(4, 1);
+    if (fwd_prepare(kern, 5) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kCtaThreads, kFwdRingBytes) != cudaSuccess || n < 1)
         n = kFwdMinBlocks;
     return n;
 }
 
 cudaError_t launch_fwd(const FwdArgs &a, bool pdl, cudaStream_t st) {
+    const FwdKernel kern = fwd_kernel_for(a.width, a.act);
+    if (!kern) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(static_cast<int64_t>(a.slabs) * a.runs, kWarpsPerCta)));
     cfg.blockDim = dim3(kCtaThreads);
     cfg.dynamicSmemBytes = kFwdRingBytes;
     cfg.stream = st;
-    if (const cudaError_t e = fwd_prepare(); e != cudaSuccess) return e;
+    if (const cudaError_t e = fwd_prepare(kern, (a.width - 2) * 2 + (a.act ? 1 : 0)); e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
     if (pdl) {
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -340,7 +350,7 @@ cudaError_t launch_fwd(const FwdArgs &a, bool pdl, cudaStream_t st) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, fwd_kernel<kFwdVec, kFwdUnroll, kFwdRing>, a);
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 }  // namespace ccc

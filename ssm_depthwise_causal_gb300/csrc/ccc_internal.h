@@ -126,6 +126,8 @@ struct FwdArgs {
     int w_bf16;
     const void *b;
     int b_kind;  // 0 none, 1 FP32, 2 BF16
+    int width;   // taps W (2..4); W-1 history rows
+    int act;     // 1 SiLU, 0 none
     uint16_t *state;
     int n_slots;
     int64_t st_slot, st_c, st_l;
@@ -151,6 +153,8 @@ struct BwdArgs {
     int w_bf16;
     const void *b;
     int b_kind;
+    int width;   // taps W (2..4); W-1 history rows
+    int act;     // 1 SiLU, 0 none
     const uint16_t *hist;
     const int32_t *cu;
     int N;
@@ -162,10 +166,37 @@ struct BwdArgs {
     uint16_t *dx;
     int dxs;
     float *d_init;
-    float *part;  // [runs][5][C]
+    float *part;  // [runs][5][C]: rows 0..W-1 taps, row 4 bias
     const int32_t *map;
     int cap;
     int slabs, runs;
+};
+
+// The speculative / single-token decode update (ccc_update.cu).
+struct UpdArgs {
+    const uint16_t *x;
+    int64_t rows;
+    int C;
+    int xs;
+    const void *w;
+    int w_bf16;
+    const void *b;
+    int b_kind;
+    int width;
+    int act;
+    uint16_t *state;
+    int n_slots;
+    int L;
+    int64_t st_slot, st_c, st_l;
+    int state_vec;    // channel axis contiguous, 16-byte aligned rows
+    int state_stage;  // dense history-contiguous pool, L <= update_stage_max_len()
+    const int32_t *cu;
+    int N;
+    const int32_t *cache;
+    const int32_t *accepted;
+    uint16_t *out;
+    int os;
+    int slabs;
 };
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -188,11 +219,18 @@ inline int runs_per_slab(int64_t target_warps, int slabs, int64_t cap) {
 // warp, or a column of kBwdTmaWarps*128 channels per CTA for the bulk-copy
 // kernel) times `runs` runs per column; runs is also the number of FP32
 // partial rows per channel.  Both depend only on (rows, N, C).
-inline int bwd_columns(int C) { return kBwdTma ? static_cast<int>(ceil_div(C, kBwdTmaWarps * 128)) : slabs_of(C, kBwdVec); }
+// The bulk-copy backward (when built in) serves the width-4 SiLU contract of
+// causal_conv1d_fn; the other widths and the no-activation variant always
+// take the register-fed kernel.
+inline bool bwd_uses_tma(int width, int act) { return kBwdTma && width == 4 && act == 1; }
 
-inline int bwd_runs(int64_t rows, int N, int C) {
-    const int64_t target = kBwdTma ? int64_t{152} * kBwdTmaMinBlocks : kBwdTargetWarps;
-    return runs_per_slab(target, bwd_columns(C), item_capacity(rows, N, kBwdChunk));
+inline int bwd_columns(int C, bool tma) {
+    return tma ? static_cast<int>(ceil_div(C, kBwdTmaWarps * 128)) : slabs_of(C, kBwdVec);
+}
+
+inline int bwd_runs(int64_t rows, int N, int C, bool tma) {
+    const int64_t target = tma ? int64_t{152} * kBwdTmaMinBlocks : kBwdTargetWarps;
+    return runs_per_slab(target, bwd_columns(C, tma), item_capacity(rows, N, kBwdChunk));
 }
 
 cudaError_t launch_chunkmap(const int32_t *cu, int N, int64_t rows, int B, int empty_items,
@@ -202,7 +240,10 @@ cudaError_t launch_bwd(const BwdArgs &a, bool pdl, cudaStream_t st);
 cudaError_t launch_bwd_tma(const BwdArgs &a, bool pdl, cudaStream_t st);
 // Resident forward CTAs per SM on the current device (occupancy query).
 int fwd_ctas_per_sm();
-cudaError_t launch_reduce(const float *part, int G, int C, float *dweight, float *dbias,
+cudaError_t launch_reduce(const float *part, int G, int C, int width, float *dweight, float *dbias,
                           bool pdl, cudaStream_t st);
+int update_slabs(int C);
+int update_stage_max_len();
+cudaError_t launch_update(const UpdArgs &a, cudaStream_t st);
 
 }  // namespace ccc

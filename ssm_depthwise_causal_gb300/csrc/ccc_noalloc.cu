@@ -54,7 +54,8 @@ int scratch_address(void **out) {
 }  // namespace
 
 extern "C" int ccc_bwd_noalloc(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
-                               const void *weight, int32_t w_dtype, const void *bias, int32_t b_dtype,
+                               const void *weight, int32_t w_dtype, int32_t width,
+                               const void *bias, int32_t b_dtype, int32_t activation,
                                const void *saved_hist,
                                const int32_t *cu_seqlens, int32_t N,
                                const int32_t *cache_indices, const uint8_t *has_initial_state,
@@ -70,7 +71,8 @@ extern "C" int ccc_bwd_noalloc(const void *x, int64_t rows, int32_t C, int64_t x
         const int rc = scratch_address(&ws);
         if (rc != CCC_OK) return rc;
     }
-    return ccc_bwd(x, rows, C, x_row_stride, weight, w_dtype, bias, b_dtype, saved_hist, cu_seqlens, N,
+    return ccc_bwd(x, rows, C, x_row_stride, weight, w_dtype, width, bias, b_dtype, activation, saved_hist,
+                   cu_seqlens, N,
                    cache_indices, has_initial_state, dy, dy_row_stride, d_final_state, dx, dx_row_stride,
                    dweight, dbias, d_init_state, ws, need > 0 ? kScratchBytes : 0, cuda_stream);
 }

@@ -52,6 +52,7 @@ class Workload:
     fragments: int = 1             # >1: process as consecutive fragments
     training: bool = True          # forward + backward
     activation: Optional[str] = "silu"  # "silu" or None
+    num_accepted: Optional[torch.Tensor] = None    # int32 [N], decode steps only
 
     @property
     def width(self) -> int:
@@ -261,6 +262,37 @@ def long_context(seed=0, device="cpu", C=4096, T=1 << 20, fragments=8) -> Worklo
                     dy=dy, fragments=fragments)
 
 
+def decode(seed=0, device="cpu", C=8192, N=256, slots=512, draft=1, state_len=4,
+           n_minus_one=13) -> Workload:
+    """One decode step of the serving batch after its prefill: N 256
+    requests, `draft` new tokens each (1: plain decode; more: speculative
+    drafts), C 8192, pool [512, 8192, state_len] (history axis contiguous),
+    distinct random slots with 13 (5 %) set to -1, weight FP32, bias BF16;
+    accepted counts U{1..draft} from the previous step (all 1 for a plain
+    decode: the first step after a prefill)."""
+    rng = np.random.default_rng(seed)
+    lengths = np.full(N, draft, dtype=np.int64)
+    cache_np = rng.choice(slots, size=N, replace=False).astype(np.int32)
+    cache_np[rng.choice(N, size=n_minus_one, replace=False)] = -1
+    acc_np = rng.integers(1, draft + 1, size=N).astype(np.int32)
+    rows = int(lengths.sum())
+    g = _gen(seed, device)
+    x = normal_bf16((rows, C), g, device)
+    weight = uniform((C, 4), g, device, -0.5, 0.5, torch.float32)
+    bias = (torch.randn((C,), generator=g, device=device) * 0.1).to(torch.bfloat16)
+    state = normal_bf16((slots, C, state_len), g, device)
+    return Workload(f"decode N={N} draft={draft} C={C} pool=[{slots},{C},{state_len}]", rows, C, lengths,
+                    cu_from_lengths(lengths).to(device), x, weight, bias,
+                    state, torch.from_numpy(cache_np).to(device), None, None, training=False,
+                    num_accepted=torch.from_numpy(acc_np).to(device))
+
+
+def spec_decode(seed=0, device="cpu") -> Workload:
+    """A speculative decode step of the serving batch: 4 draft tokens per
+    request, pool [512, 8192, 6] (room for 4 + W - 2 values)."""
+    return decode(seed, device, draft=4, state_len=6)
+
+
 def packed_small(seed=0, device="cpu") -> Workload:
     """The packed workload at a quarter of the rows (16384 rows, 50
     sequences): each tensor is 235 MB, still larger than L2, for profiler
@@ -270,6 +302,8 @@ def packed_small(seed=0, device="cpu") -> Workload:
 
 WORKLOADS = {
     "tiny": tiny,
+    "decode": decode,
+    "spec_decode": spec_decode,
     "dense": dense,
     "packed": packed,
     "packed_small": packed_small,

@@ -62,22 +62,23 @@ def run_gpu(wl: workloads.Workload, *, backward=True, d_final=None, want_d_init=
     state = None
     if wl.conv_state is not None:
         state = wl.conv_state.clone() if pool_layout == "history" else channel_contiguous_pool(wl.conv_state)
+    H = wl.width - 1
     out = fill_sentinel(torch.empty((wl.rows, wl.C), dtype=torch.bfloat16, device=dev))
-    hist = fill_sentinel(torch.empty((wl.n_seqs, 3, wl.C), dtype=torch.bfloat16, device=dev))
+    hist = fill_sentinel(torch.empty((wl.n_seqs, H, wl.C), dtype=torch.bfloat16, device=dev))
     ws = torch.empty(max(1, ccc.ccc_workspace_size(wl.rows, wl.n_seqs, wl.C, False)),
                      dtype=torch.uint8, device=dev)
     ccc.ccc_fwd(x, wl.weight, wl.bias, state, wl.cu_seqlens, wl.cache_indices,
-                wl.has_initial_state, out, hist, ws)
+                wl.has_initial_state, out, hist, ws, activation=wl.activation)
     res = GpuResult(out=out, state=state, hist=hist)
     if backward:
         dx = fill_sentinel(torch.empty((wl.rows, wl.C), dtype=torch.bfloat16, device=dev))
-        dw = torch.full((wl.C, 4), float("nan"), device=dev)
+        dw = torch.full((wl.C, wl.width), float("nan"), device=dev)
         db = torch.full((wl.C,), float("nan"), device=dev) if wl.bias is not None else None
-        di = torch.full((wl.n_seqs, 3, wl.C), float("nan"), device=dev) if want_d_init else None
+        di = torch.full((wl.n_seqs, H, wl.C), float("nan"), device=dev) if want_d_init else None
         wsb = torch.empty(ccc.ccc_workspace_size(wl.rows, wl.n_seqs, wl.C, True), dtype=torch.uint8,
                           device=dev)
         ccc.ccc_bwd(x, wl.weight, wl.bias, hist, wl.cu_seqlens, wl.cache_indices,
-                    wl.has_initial_state, wl.dy, d_final, dx, dw, db, di, wsb)
+                    wl.has_initial_state, wl.dy, d_final, dx, dw, db, di, wsb, activation=wl.activation)
         res.dx, res.dweight, res.dbias, res.d_init = dx, dw, db, di
     torch.cuda.synchronize()
     return res
@@ -100,12 +101,14 @@ def subset(wl: workloads.Workload, chans) -> workloads.Workload:
 
 def run_oracle(wl_cpu: workloads.Workload, *, backward=True, d_final=None):
     out, state, hist = oracle.fwd(wl_cpu.x, wl_cpu.weight, wl_cpu.bias, wl_cpu.cu_seqlens,
-                                  wl_cpu.conv_state, wl_cpu.cache_indices, wl_cpu.has_initial_state)
+                                  wl_cpu.conv_state, wl_cpu.cache_indices, wl_cpu.has_initial_state,
+                                  activation=wl_cpu.activation)
     res = dict(out=out, state=state, hist=hist)
     if backward:
         h = hist if wl_cpu.conv_state is not None else None
         res.update(oracle.bwd(wl_cpu.x, wl_cpu.weight, wl_cpu.bias, wl_cpu.cu_seqlens, wl_cpu.dy,
-                              h, wl_cpu.cache_indices, wl_cpu.has_initial_state, d_final))
+                              h, wl_cpu.cache_indices, wl_cpu.has_initial_state, d_final,
+                              activation=wl_cpu.activation))
     return res
 
 

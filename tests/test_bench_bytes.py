@@ -1,0 +1,29 @@
+"""The byte counts behind bench.py's effective-bandwidth and roofline
+figures, checked by hand on small CPU workloads (no GPU needed)."""
+import numpy as np
+import torch
+
+import bench
+from ssm_depthwise_causal_gb300 import workloads
+
+
+def test_fwdbwd_bytes_packed_without_state():
+    wl = workloads.make_custom((5, 0, 7), 16, rows=15, seed=1, with_state=False,
+                               w_dtype=torch.bfloat16)
+    fwd, bwd = bench.algorithmic_bytes(wl)
+    T, C = 12, 16
+    assert fwd == T * C * 2 + T * C * 2 + C * 4 * 2 + C * 4
+    assert bwd == T * C * 4 + T * C * 2 + C * 4 * 2 + C * 4 + C * 5 * 4
+
+
+def test_update_bytes_by_hand():
+    wl = workloads.decode(device="cpu", C=16, N=6, slots=12, draft=3, state_len=6, n_minus_one=2)
+    alg, block = bench.update_algorithmic_bytes(wl)
+    C, L, H = 16, 6, 3
+    live = (wl.cache_indices.numpy() != -1)
+    n_live, n_dead = int(live.sum()), int((~live).sum())
+    per_live = 3 * 4 + 2 * H + 2 * min(3 + H - 1, L)          # x + out, state read, state write
+    expect = C * (n_live * per_live + n_dead * 3 * 2) + C * 4 * 4 + C * 2
+    assert alg == expect
+    assert block == C * (n_live * (3 * 4 + 4 * L) + n_dead * 3 * 2)
+    assert n_dead == 2 and np.all(wl.lengths == 3)

@@ -70,7 +70,7 @@ A = 1 << 20  # fake, 16-byte aligned, never dereferenced
 
 
 def fwd_args(**kw):
-    a = dict(x=A, rows=64, C=256, xs=256, w=A * 2, wd=0, b=None, bd=-1,
+    a = dict(x=A, rows=64, C=256, xs=256, w=A * 2, wd=0, W=4, b=None, bd=-1, act=1,
              state=None, slots=0, L=0, s0=0, s1=0, s2=0, cu=A * 3, N=4, ci=None, hi=None,
              out=A * 4, os=256, hist=None, ws=None, wsb=0, stream=None)
     a.update(kw)
@@ -78,8 +78,8 @@ def fwd_args(**kw):
 
 
 def call_fwd(lib, a):
-    return lib.ccc_fwd(P(a["x"]), a["rows"], a["C"], a["xs"], P(a["w"]), a["wd"], P(a["b"]), a["bd"],
-                       P(a["state"]), a["slots"], a["L"], a["s0"], a["s1"], a["s2"], P(a["cu"]), a["N"],
+    return lib.ccc_fwd(P(a["x"]), a["rows"], a["C"], a["xs"], P(a["w"]), a["wd"], a["W"], P(a["b"]), a["bd"],
+                       a["act"], P(a["state"]), a["slots"], a["L"], a["s0"], a["s1"], a["s2"], P(a["cu"]), a["N"],
                        P(a["ci"]), P(a["hi"]), P(a["out"]), a["os"], P(a["hist"]), P(a["ws"]), a["wsb"],
                        P(a["stream"]))
 
@@ -109,6 +109,13 @@ def call_fwd(lib, a):
     (dict(N=40, ws=A * 8, wsb=16), E_WS),
     (dict(rows=0), OK),                         # nothing to do, nothing launched
     (dict(N=0), OK),
+    (dict(W=5), E_SHAPE),                       # widths 2..4
+    (dict(W=1), E_SHAPE),
+    (dict(act=2), E_SHAPE),
+    (dict(W=2, rows=0), OK),
+    (dict(W=3, act=0, rows=0), OK),
+    (dict(W=3, state=A * 6, slots=8, L=1, s0=1024, s1=1, s2=1, ci=A * 7), E_SHAPE),   # L < W-1
+    (dict(W=2, rows=0, state=A * 6, slots=8, L=1, s0=256, s1=1, s2=1, ci=A * 7), OK),
 ])
 def test_fwd_host_checks(lib, kw, code):
     assert call_fwd(lib, fwd_args(**kw)) == code
@@ -123,12 +130,12 @@ def test_fwd_state_layouts_accepted_by_checks(lib):
 
 
 def call_bwd(lib, **kw):
-    a = dict(x=A, rows=64, C=256, xs=256, w=A * 2, wd=0, b=None, bd=-1, hist=None, cu=A * 3, N=4,
-             ci=None, hi=None, dy=A * 4, dys=256, df=None, dx=A * 5, dxs=256, dw=A * 6, db=None,
+    a = dict(x=A, rows=64, C=256, xs=256, w=A * 2, wd=0, W=4, b=None, bd=-1, act=1, hist=None, cu=A * 3,
+             N=4, ci=None, hi=None, dy=A * 4, dys=256, df=None, dx=A * 5, dxs=256, dw=A * 6, db=None,
              di=None, ws=A * 9, wsb=1 << 30, stream=None)
     a.update(kw)
-    return lib.ccc_bwd(P(a["x"]), a["rows"], a["C"], a["xs"], P(a["w"]), a["wd"], P(a["b"]), a["bd"],
-                       P(a["hist"]), P(a["cu"]), a["N"], P(a["ci"]), P(a["hi"]), P(a["dy"]), a["dys"],
+    return lib.ccc_bwd(P(a["x"]), a["rows"], a["C"], a["xs"], P(a["w"]), a["wd"], a["W"], P(a["b"]), a["bd"],
+                       a["act"], P(a["hist"]), P(a["cu"]), a["N"], P(a["ci"]), P(a["hi"]), P(a["dy"]), a["dys"],
                        P(a["df"]), P(a["dx"]), a["dxs"], P(a["dw"]), P(a["db"]), P(a["di"]), P(a["ws"]),
                        a["wsb"], P(a["stream"]))
 
@@ -145,6 +152,39 @@ def call_bwd(lib, **kw):
     (dict(dx=A + 128), E_ALIAS),          # dx overlaps x
     (dict(dw=A * 4 + 64), E_ALIAS),       # dweight inside dy
     (dict(di=A * 9 + 256), E_ALIAS),      # d_init inside the workspace
+    (dict(W=7), E_SHAPE),
+    (dict(act=-1), E_SHAPE),
+    (dict(W=4, dw=A * 4 - 256 * 2 * 4), E_ALIAS),   # dweight [C, 4] runs into dy
 ])
 def test_bwd_host_checks(lib, kw, code):
     assert call_bwd(lib, **kw) == code
+
+
+def call_update(lib, **kw):
+    a = dict(x=A, rows=64, C=256, xs=256, w=A * 2, wd=0, W=4, b=None, bd=-1, act=1,
+             state=A * 6, slots=8, L=4, s0=1024, s1=4, s2=1, cu=A * 3, N=4, ci=A * 7, na=None,
+             out=A * 4, os=256, stream=None)
+    a.update(kw)
+    return lib.ccc_update(P(a["x"]), a["rows"], a["C"], a["xs"], P(a["w"]), a["wd"], a["W"], P(a["b"]), a["bd"],
+                          a["act"], P(a["state"]), a["slots"], a["L"], a["s0"], a["s1"], a["s2"], P(a["cu"]),
+                          a["N"], P(a["ci"]), P(a["na"]), P(a["out"]), a["os"], P(a["stream"]))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(state=None), E_NULL),                 # the pool is required
+    (dict(ci=None), E_NULL),
+    (dict(out=None), E_NULL),
+    (dict(L=2), E_SHAPE),                       # L < W-1
+    (dict(W=2, L=0), E_SHAPE),
+    (dict(s1=2, s2=2), E_SHAPE),                # neither channel nor history axis contiguous
+    (dict(W=5), E_SHAPE),
+    (dict(act=3), E_SHAPE),
+    (dict(na=A * 8 + 2), E_ALIGN),
+    (dict(out=A + 64), E_ALIAS),                # out overlaps x
+    (dict(na=A * 6 + 64), E_ALIAS),             # accepted counts inside the pool (read-only operand vs written pool)
+    (dict(rows=0), OK),                         # nothing to do, nothing launched
+    (dict(N=0), OK),
+    (dict(W=2, L=1, s0=256, s1=1, s2=1, rows=0), OK),
+])
+def test_update_host_checks(lib, kw, code):
+    assert call_update(lib, **kw) == code

@@ -209,3 +209,99 @@ def test_long_context_split_equals_unsplit(cuda_device):
     # fragment-summed dweight within the reduction tolerance of the oracle
     H.assert_reduction_close(dw_s[chans].cpu().numpy(), ref["dweight"], ref["abs_dweight"],
                              "split dweight")
+
+
+# ------------------------------------------------ widths 2, 3 / no activation --
+# Megatron-Core core.ssm.causal_conv1d (causal_conv1d_cp: weight [D, W],
+# optional activation): the same kernels instantiated for W = 2, 3 and for
+# the identity activation, against the oracle at the same width.
+
+VARIANTS = [(2, "silu"), (2, None), (3, "silu"), (3, None), (4, None)]
+
+VARIANT_SHAPES = {
+    # lengths, C, kwargs
+    "short_and_empty": ((1, 2, 3, 4, 0, 5, 2), 264, dict(n_minus_one=1)),
+    "chunk_boundaries": ((63, 64, 65, 127, 129, 0, 1), 40, dict(n_minus_one=1, has_init_p=1.0)),
+    "n40_map": (tuple(int(v) for v in np.random.default_rng(7).integers(0, 90, 40)), 72,
+                dict(n_minus_one=4)),
+    "bf16_w_no_bias": ((33, 7, 90), 64, dict(w_dtype=torch.bfloat16, b_dtype=None)),
+}
+
+
+@pytest.mark.parametrize("shape", sorted(VARIANT_SHAPES))
+@pytest.mark.parametrize("width,act", VARIANTS)
+def test_width_activation_variants(cuda_device, width, act, shape):
+    lengths, C, kw = VARIANT_SHAPES[shape]
+    wl = workloads.make_custom(lengths, C, rows=sum(lengths) + 5, seed=17 + width, device=cuda_device,
+                               width=width, activation=act, **kw)
+    check(wl, H.run_gpu(wl))
+
+
+@pytest.mark.parametrize("width,act", VARIANTS)
+def test_variant_d_final_and_channel_pool(cuda_device, width, act):
+    wl = workloads.make_custom((40, 2, 0, 70, 1), 136, rows=120, seed=5, device=cuda_device,
+                               n_minus_one=1, has_init_p=0.6, width=width, activation=act)
+    g = torch.Generator(device=cuda_device).manual_seed(3)
+    d_final = torch.randn((wl.n_seqs, width - 1, wl.C), generator=g, device=cuda_device)
+    check(wl, H.run_gpu(wl, d_final=d_final), d_final=d_final)
+    res = H.run_gpu(wl, pool_layout="channel", x_pad_cols=8)
+    res.state = res.state.contiguous()
+    check(wl, res)
+
+
+@pytest.mark.parametrize("width,act", VARIANTS)
+def test_variant_split_equals_unsplit(cuda_device, width, act):
+    """A 24 576-token document in 4 fragments chained through a one-slot pool
+    (and d_init -> d_final backwards) equals the unsplit call bit for bit."""
+    import ssm_depthwise_causal_gb300 as ccc
+    dev = cuda_device
+    T, C, F = 24576, 520, 4
+    L = T // F
+    wl = workloads.make_custom((T,), C, seed=23, device=dev, with_state=False, width=width,
+                               activation=act)
+    Hh = width - 1
+    kw = dict(activation=act)
+    out_u = torch.empty_like(wl.x)
+    ccc.ccc_fwd(wl.x, wl.weight, wl.bias, None, wl.cu_seqlens, None, None, out_u, **kw)
+    dx_u = torch.empty_like(wl.x)
+    dw_u = torch.empty((C, width), device=dev)
+    db_u = torch.empty((C,), device=dev)
+    ws = torch.empty(ccc.ccc_workspace_size(T, 1, C, True), dtype=torch.uint8, device=dev)
+    ccc.ccc_bwd(wl.x, wl.weight, wl.bias, None, wl.cu_seqlens, None, None, wl.dy, None, dx_u, dw_u,
+                db_u, None, ws, **kw)
+    pool = torch.zeros((1, C, Hh), dtype=torch.bfloat16, device=dev)
+    cache = torch.zeros(1, dtype=torch.int32, device=dev)
+    cu_f = torch.tensor([0, L], dtype=torch.int32, device=dev)
+    out_s = torch.empty_like(wl.x)
+    hists = []
+    for k in range(F):
+        hist = torch.empty((1, Hh, C), dtype=torch.bfloat16, device=dev)
+        hi = torch.tensor([k > 0], device=dev)
+        ccc.ccc_fwd(wl.x[k * L:(k + 1) * L], wl.weight, wl.bias, pool, cu_f, cache, hi,
+                    out_s[k * L:(k + 1) * L], hist, **kw)
+        hists.append((hist, hi))
+    dx_s = torch.empty_like(wl.x)
+    wsf = torch.empty(ccc.ccc_workspace_size(L, 1, C, True), dtype=torch.uint8, device=dev)
+    d_carry = None
+    for k in reversed(range(F)):
+        hist, hi = hists[k]
+        dwk = torch.empty((C, width), device=dev)
+        dbk = torch.empty((C,), device=dev)
+        d_init = torch.empty((1, Hh, C), device=dev)
+        ccc.ccc_bwd(wl.x[k * L:(k + 1) * L], wl.weight, wl.bias, hist, cu_f, cache, hi,
+                    wl.dy[k * L:(k + 1) * L], d_carry, dx_s[k * L:(k + 1) * L], dwk, dbk, d_init, wsf, **kw)
+        d_carry = d_init
+    torch.cuda.synchronize()
+    assert torch.equal(out_s.view(torch.int16), out_u.view(torch.int16)), "split fwd != unsplit"
+    assert torch.equal(dx_s.view(torch.int16), dx_u.view(torch.int16)), "split dx != unsplit"
+    assert torch.equal(pool[0].view(torch.int16), wl.x[T - Hh:T].t().contiguous().view(torch.int16))
+    # the unsplit call against the oracle on a channel subset
+    chans = spread_channels(C, n=16)
+    sub = H.subset(wl, chans)
+    ref = H.run_oracle(sub)
+    res = H.GpuResult(out=out_u, state=None,
+                      hist=H.fill_sentinel(torch.empty((1, Hh, C), dtype=torch.bfloat16, device=dev)),
+                      dx=dx_u, dweight=dw_u, dbias=db_u, d_init=None)
+    got = H.gpu_numpy(res, chans)
+    got["hist"] = ref["hist"]  # no history was saved in the unsplit call
+    H.compare(sub, ref, got)
