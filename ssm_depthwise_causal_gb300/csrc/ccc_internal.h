@@ -34,6 +34,9 @@ namespace ccc {
 #ifndef CCC_BWD_MIN_BLOCKS
 #define CCC_BWD_MIN_BLOCKS 1
 #endif
+#ifndef CCC_UPD_MIN_BLOCKS
+#define CCC_UPD_MIN_BLOCKS 2
+#endif
 #ifndef CCC_BWD_TARGET_WARPS
 #define CCC_BWD_TARGET_WARPS 1216
 #endif
@@ -86,6 +89,8 @@ constexpr int kBwdUnroll = CCC_BWD_UNROLL;
 // Resident CTAs per SM the register budget is sized for.
 constexpr int kFwdMinBlocks = CCC_FWD_MIN_BLOCKS;
 constexpr int kBwdMinBlocks = CCC_BWD_MIN_BLOCKS;
+// Decode update: resident CTAs per SM the register budget is sized for.
+constexpr int kUpdMinBlocks = CCC_UPD_MIN_BLOCKS;
 // Forward: stages of the per-lane shared-memory ring (0 = load rows straight
 // into registers).
 constexpr int kFwdRing = CCC_FWD_RING;

@@ -19,16 +19,22 @@
 // this rule expects for a = 1.  A -1 slot gives zero output and no state
 // access; an empty sequence leaves its slot alone.
 //
-// Mapping.  One warp per (sequence, 32*VEC-channel slab): it reads the
-// window (registers), walks the sequence's tokens U at a time and writes the
-// slot.  Reads of the slot precede every write to it in the warp's program
-// order, and no other warp touches the slot's channels (live slots are
-// unique; slabs are disjoint), so the in-place update needs no
-// synchronisation.  For a dense history-contiguous pool ([slots][C][L],
-// L <= kUpdStageL) the warp moves the slot's whole [256 ch][L] block with
-// coalesced 16-byte copies through shared memory (lanes then pick single
-// positions there); a channel-contiguous pool is read and written one
-// 16-byte vector per lane and position; any other layout element by element.
+// Mapping.  One warp per (sequence, 32*VEC-channel slab); the 8 warps of a
+// CTA take 8 consecutive sequences on the same slab, so the slab's taps and
+// bias are staged once per CTA in shared memory (tap-major, coalesced global
+// reads) instead of once per warp.  A warp reads the window (registers),
+// walks the sequence's tokens U at a time and writes the slot.  Reads of the
+// slot precede every write to it in the warp's program order, and no other
+// warp touches the slot's channels (live slots are unique; slabs are
+// disjoint), so the in-place update needs no synchronisation beyond the
+// warp.  For a dense history-contiguous pool ([slots][C][L], L <=
+// kUpdStageL) the warp copies the slot's whole [256 ch][L] block with
+// coalesced 16-byte loads and transposes it into a position-major [L][256]
+// copy in shared memory, where every position of the lane's 8 channels is one
+// conflict-free 16-byte vector; the block goes back the same way (positions
+// not written keep their bits).  A channel-contiguous pool is read and
+// written one 16-byte vector per lane and position; any other layout element
+// by element.
 #include "ccc_device.cuh"
 #include "ccc_internal.h"
 
@@ -39,31 +45,6 @@ namespace {
 constexpr int kUpdVec = 8;
 constexpr int kUpdUnroll = 4;
 constexpr int kUpdStageL = 8;  // longest history the shared-memory path stages
-constexpr int kUpdStageBytes = 32 * kUpdVec * kUpdStageL * 2;  // per warp
-
-// Position p of this lane's VEC channels from the staged [256 ch][L] block.
-template <int NV>
-__device__ __forceinline__ Raw<NV> staged_get(const uint16_t *blk, int L, int lane, int p) {
-    Raw<NV> r;
-    const uint16_t *c = blk + lane * 2 * NV * L + p;
-#pragma unroll
-    for (int v = 0; v < NV; ++v) {
-        const uint32_t lo = c[(2 * v) * L];
-        const uint32_t hi = c[(2 * v + 1) * L];
-        r.u[v] = lo | (hi << 16);
-    }
-    return r;
-}
-
-template <int NV>
-__device__ __forceinline__ void staged_put(uint16_t *blk, int L, int lane, int p, const Raw<NV> &r) {
-    uint16_t *c = blk + lane * 2 * NV * L + p;
-#pragma unroll
-    for (int v = 0; v < NV; ++v) {
-        c[(2 * v) * L] = static_cast<uint16_t>(r.u[v] & 0xffffu);
-        c[(2 * v + 1) * L] = static_cast<uint16_t>(r.u[v] >> 16);
-    }
-}
 
 // Element (slot q, channels c0.., position p) for the general layouts.
 template <int NV>
@@ -94,29 +75,92 @@ __device__ __forceinline__ void state_put(const UpdArgs &a, int q, int p, int c0
     }
 }
 
-template <int W, bool ACT>
-__global__ void __launch_bounds__(kCtaThreads, 2) update_kernel(const UpdArgs a) {
+// LS > 0: the pool is dense history-contiguous with L = LS (a compile-time
+// constant, so the block transposition below is straight-line code); LS = 0:
+// any other layout, L from the arguments.
+template <int W, bool ACT, int LS>
+__global__ void __launch_bounds__(kCtaThreads, kUpdMinBlocks) update_kernel(const UpdArgs a) {
     constexpr int VEC = kUpdVec, NV = VEC / 2, U = kUpdUnroll;
     constexpr int H = W - 1;
-    __shared__ __align__(16) uint16_t stage_all[kWarpsPerCta][kUpdStageBytes / 2];
+    static_assert(LS == 0 || (LS >= H && LS <= kUpdStageL), "staged history length");
+    constexpr int SLAB = 32 * VEC;
+    __shared__ __align__(16) float s_tap[W + 1][SLAB];  // taps 0..W-1 and the bias of this slab
+    __shared__ __align__(16) uint16_t s_blk[kWarpsPerCta][(LS > 0 ? LS : 1) * SLAB];  // position-major
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + warp;
-    if (gw >= static_cast<int64_t>(a.slabs) * a.N) return;  // whole warp
-    const int n = static_cast<int>(gw / a.slabs), slab = static_cast<int>(gw % a.slabs);
+    const int slab = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.slabs));
+    const int n = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.slabs)) * kWarpsPerCta + warp;
+
     const int cv = slab * 32 + lane;
     const bool act = cv < a.C / VEC;
     const int c0 = act ? cv * VEC : 0;
-    uint16_t *blk = stage_all[warp];
+    uint16_t *blk = s_blk[warp];
 
-    // Offsets clamped to [0, rows] so a bad value cannot leave the buffers.
+    // Every load that does not depend on another is issued before the CTA
+    // barrier: this warp's offsets, slot and accepted count, the slab's taps
+    // and bias (one channel per thread), then the new tokens and the slot's
+    // block, so the step costs two dependent memory round trips.
+    // Offsets are clamped to [0, rows] so a bad value cannot leave the buffers.
+    const bool has_n = n < a.N;
     const int64_t rows = a.rows;
-    const int s = static_cast<int>(min(max(static_cast<int64_t>(__ldg(a.cu + n)), int64_t{0}), rows));
-    const int e = static_cast<int>(min(max(static_cast<int64_t>(__ldg(a.cu + n + 1)), static_cast<int64_t>(s)), rows));
+    int s = 0, e = 0, q = -1, acc = 1;
+    if (has_n) {
+        s = static_cast<int>(min(max(static_cast<int64_t>(__ldg(a.cu + n)), int64_t{0}), rows));
+        e = static_cast<int>(min(max(static_cast<int64_t>(__ldg(a.cu + n + 1)), static_cast<int64_t>(s)), rows));
+        q = __ldg(a.cache + n);
+        if (a.accepted) acc = __ldg(a.accepted + n);
+    }
+    float tv[W + 1];
+    {
+        const int c = slab * SLAB + static_cast<int>(threadIdx.x);
+        const bool ok = c < a.C;
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+            float t = 0.0f;
+            if (ok) {
+                t = a.w_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(a.w)[W * c + k])
+                             : __ldg(reinterpret_cast<const float *>(a.w) + W * c + k);
+            }
+            tv[k] = t;
+        }
+        float bv = 0.0f;
+        if (ok && a.b_kind == 1) bv = __ldg(reinterpret_cast<const float *>(a.b) + c);
+        if (ok && a.b_kind == 2) bv = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(a.b)[c]);
+        tv[W] = bv;
+    }
     const int len = e - s;
-    if (len == 0) return;
-    const int q = __ldg(a.cache + n);
+    const bool work = has_n && len > 0 && q != -1;
     const uint16_t *xrow = a.x + static_cast<int64_t>(s) * a.xs + c0;
     uint16_t *orow = a.out + static_cast<int64_t>(s) * a.os + c0;
+    Raw<NV> xr0[U];  // the first U new tokens (independent of the state)
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+        xr0[u] = (work && act && u < len) ? ld_ro<NV>(xrow + static_cast<int64_t>(u) * a.xs) : raw_zero<NV>();
+
+    const bool pool = work && q >= 0 && q < a.n_slots;
+    acc = min(max(acc, 1), a.L - H + 1);
+    const int n_write = min(len + H - 1, a.L);  // positions written
+    constexpr bool kStaged = LS > 0;
+    const bool staged = kStaged && pool;
+    const int L = kStaged ? LS : a.L;
+    // The staged block: this slab's channels x L positions of slot q,
+    // contiguous (channel-major) in a dense history-contiguous pool.
+    const int slab_ch = min(SLAB, a.C - slab * SLAB);
+    const int blk_vecs = slab_ch * L / 8;  // 16-byte vectors in the block
+    uint16_t *gblk = pool ? a.state + static_cast<int64_t>(q) * a.st_slot + static_cast<int64_t>(slab) * SLAB * L
+                          : nullptr;
+    uint4 bvec[kStaged ? LS : 1];  // vector lane + 32 k of the block
+    if constexpr (kStaged) {
+#pragma unroll
+        for (int k = 0; k < LS; ++k) {
+            const int i = lane + 32 * k;
+            bvec[k] = (staged && i < blk_vecs) ? reinterpret_cast<const uint4 *>(gblk)[i] : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+
+#pragma unroll
+    for (int k = 0; k <= W; ++k) s_tap[k][threadIdx.x] = tv[k];
+    __syncthreads();
+    if (!has_n || len == 0) return;  // whole warp, after the CTA barrier
     if (q == -1) {  // padded request: zero output, no state access
         if (act) {
             const Raw<NV> z = raw_zero<NV>();
@@ -124,29 +168,39 @@ __global__ void __launch_bounds__(kCtaThreads, 2) update_kernel(const UpdArgs a)
         }
         return;
     }
-    const bool pool = q >= 0 && q < a.n_slots;
-    int acc = a.accepted ? __ldg(a.accepted + n) : 1;
-    acc = min(max(acc, 1), a.L - H + 1);
-    const int n_write = min(len + H - 1, a.L);  // positions written
-    const bool staged = pool && a.state_stage;
-    // The staged block: this slab's channels [slab*256, +256) x L positions of
-    // slot q, contiguous in a dense history-contiguous pool.
-    const int slab_ch = min(32 * VEC, a.C - slab * 32 * VEC);
-    const int blk_vecs = slab_ch * a.L / 8;  // 16-byte vectors in the block
-    uint16_t *gblk = pool ? a.state + static_cast<int64_t>(q) * a.st_slot + static_cast<int64_t>(slab) * 32 * VEC * a.L
-                          : nullptr;
 
     // The W-1 values before the first new token.
     Raw<NV> hr[H];
 #pragma unroll
     for (int p = 0; p < H; ++p) hr[p] = raw_zero<NV>();
     if (staged) {
-        for (int i = lane; i < blk_vecs; i += 32)
-            reinterpret_cast<uint4 *>(blk)[i] = reinterpret_cast<const uint4 *>(gblk)[i];
+        // channel-major global block -> position-major blk[p][ch].  Vector
+        // i + 32k of the block starts at element 8 i + 256 k; with L known at
+        // compile time every (channel, position) below is a constant plus
+        // the lane's own start.
+        if constexpr (kStaged) {
+            const int ch_l = (8 * lane) / LS, p_l = (8 * lane) % LS;
+#pragma unroll
+            for (int k = 0; k < LS; ++k) {  // the block holds slab_ch * LS / 8 <= 32 * LS vectors
+                const int i = lane + 32 * k;
+                if (i < blk_vecs) {
+                    const uint4 v = bvec[k];
+                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        // element 8 i + t = 8 lane + (256 k + t)
+                        const int d = 256 * k + t;
+                        const int pp = p_l + d % LS, cc = ch_l + d / LS;
+                        const int p = pp >= LS ? pp - LS : pp, ch = pp >= LS ? cc + 1 : cc;
+                        blk[p * SLAB + ch] = static_cast<uint16_t>(t & 1 ? w4[t >> 1] >> 16 : w4[t >> 1] & 0xffffu);
+                    }
+                }
+            }
+        }
         __syncwarp();
         if (act)
 #pragma unroll
-            for (int p = 0; p < H; ++p) hr[p] = staged_get<NV>(blk, a.L, lane, acc - 1 + p);
+            for (int p = 0; p < H; ++p) hr[p] = ld_rw<NV>(blk + (acc - 1 + p) * SLAB + lane * VEC);
     } else if (pool && act) {
 #pragma unroll
         for (int p = 0; p < H; ++p) hr[p] = state_get<NV>(a, q, acc - 1 + p, c0);
@@ -158,7 +212,7 @@ __global__ void __launch_bounds__(kCtaThreads, 2) update_kernel(const UpdArgs a)
         for (int p = 0; p + 1 < H; ++p) {
             if (p < n_write) {
                 if (staged) {
-                    staged_put<NV>(blk, a.L, lane, p, hr[p + 1]);
+                    st_plain<NV>(blk + p * SLAB + lane * VEC, hr[p + 1]);
                 } else {
                     state_put<NV>(a, q, p, c0, hr[p + 1]);
                 }
@@ -167,16 +221,27 @@ __global__ void __launch_bounds__(kCtaThreads, 2) update_kernel(const UpdArgs a)
     }
 
     float2 wt[W][NV], bb[NV];
-    load_taps_w<NV, W>(a.w, a.w_bf16, a.b, a.b_kind, c0, act, wt, bb);
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+#pragma unroll
+        for (int k = 0; k < W; ++k) wt[k][v] = reinterpret_cast<const float2 *>(&s_tap[k][lane * VEC])[v];
+        bb[v] = reinterpret_cast<const float2 *>(&s_tap[W][lane * VEC])[v];
+    }
     float2 hw[H][NV];
 #pragma unroll
     for (int p = 0; p < H; ++p) unpack<NV>(hr[p], hw[p]);
 
     for (int base = 0; base < len; base += U) {
         Raw<NV> xr[U];
+        if (base == 0) {
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-            xr[u] = (act && base + u < len) ? ld_ro<NV>(xrow + static_cast<int64_t>(base + u) * a.xs) : raw_zero<NV>();
+            for (int u = 0; u < U; ++u) xr[u] = xr0[u];
+        } else {
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                xr[u] = (act && base + u < len) ? ld_ro<NV>(xrow + static_cast<int64_t>(base + u) * a.xs)
+                                                : raw_zero<NV>();
+        }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int j = base + u;
@@ -197,7 +262,7 @@ __global__ void __launch_bounds__(kCtaThreads, 2) update_kernel(const UpdArgs a)
                 const int p = H - 1 + j;
                 if (pool && p < n_write) {
                     if (staged) {
-                        staged_put<NV>(blk, a.L, lane, p, xr[u]);
+                        st_plain<NV>(blk + p * SLAB + lane * VEC, xr[u]);
                     } else {
                         state_put<NV>(a, q, p, c0, xr[u]);
                     }
@@ -207,24 +272,58 @@ __global__ void __launch_bounds__(kCtaThreads, 2) update_kernel(const UpdArgs a)
     }
 
     if (staged) {
-        // Write the block back whole (positions not written keep the bits
-        // they were read with).
+        // position-major blk -> channel-major global block, whole (positions
+        // not written keep the bits they were read with)
         __syncwarp();
-        for (int i = lane; i < blk_vecs; i += 32)
-            reinterpret_cast<uint4 *>(gblk)[i] = reinterpret_cast<const uint4 *>(blk)[i];
+        if constexpr (kStaged) {
+            const int ch_l = (8 * lane) / LS, p_l = (8 * lane) % LS;
+#pragma unroll
+            for (int k = 0; k < LS; ++k) {
+                const int i = lane + 32 * k;
+                if (i < blk_vecs) {
+                    uint32_t w4[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        const int d = 256 * k + t;
+                        const int pp = p_l + d % LS, cc = ch_l + d / LS;
+                        const int p = pp >= LS ? pp - LS : pp, ch = pp >= LS ? cc + 1 : cc;
+                        const uint32_t h = blk[p * SLAB + ch];
+                        w4[t >> 1] |= t & 1 ? h << 16 : h;
+                    }
+                    reinterpret_cast<uint4 *>(gblk)[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                }
+            }
+        }
     }
 }
 
 using UpdKernel = void (*)(const UpdArgs);
 
-UpdKernel update_kernel_for(int width, int act) {
+// The instantiation for (W, ACT) and a staged history length ls (0: none).
+template <int W, bool ACT>
+UpdKernel update_kernel_l(int ls) {
+    switch (ls) {
+        case 0: return update_kernel<W, ACT, 0>;
+        case 1: if constexpr (W - 1 <= 1) return update_kernel<W, ACT, (W - 1 <= 1 ? 1 : 0)>; else return nullptr;
+        case 2: if constexpr (W - 1 <= 2) return update_kernel<W, ACT, (W - 1 <= 2 ? 2 : 0)>; else return nullptr;
+        case 3: return update_kernel<W, ACT, 3>;
+        case 4: return update_kernel<W, ACT, 4>;
+        case 5: return update_kernel<W, ACT, 5>;
+        case 6: return update_kernel<W, ACT, 6>;
+        case 7: return update_kernel<W, ACT, 7>;
+        case 8: return update_kernel<W, ACT, 8>;
+        default: return nullptr;
+    }
+}
+
+UpdKernel update_kernel_for(int width, int act, int ls) {
     switch (width * 2 + (act ? 1 : 0)) {
-        case 4: return update_kernel<2, false>;
-        case 5: return update_kernel<2, true>;
-        case 6: return update_kernel<3, false>;
-        case 7: return update_kernel<3, true>;
-        case 8: return update_kernel<4, false>;
-        case 9: return update_kernel<4, true>;
+        case 4: return update_kernel_l<2, false>(ls);
+        case 5: return update_kernel_l<2, true>(ls);
+        case 6: return update_kernel_l<3, false>(ls);
+        case 7: return update_kernel_l<3, true>(ls);
+        case 8: return update_kernel_l<4, false>(ls);
+        case 9: return update_kernel_l<4, true>(ls);
         default: return nullptr;
     }
 }
@@ -236,10 +335,12 @@ int update_slabs(int C) { return slabs_of(C, kUpdVec); }
 int update_stage_max_len() { return kUpdStageL; }
 
 cudaError_t launch_update(const UpdArgs &a, cudaStream_t st) {
-    const UpdKernel kern = update_kernel_for(a.width, a.act);
+    const UpdKernel kern = update_kernel_for(a.width, a.act, a.state_stage ? a.L : 0);
     if (!kern) return cudaErrorInvalidValue;
-    const int64_t warps = static_cast<int64_t>(a.slabs) * a.N;
-    const dim3 grid(static_cast<unsigned>(ceil_div(warps, kWarpsPerCta)));
+    // CTA b: slab b % slabs, sequences (b / slabs) * 8 + warp.
+    const int64_t ctas = static_cast<int64_t>(a.slabs) * ceil_div(a.N, kWarpsPerCta);
+    if (ctas > INT32_MAX) return cudaErrorInvalidValue;
+    const dim3 grid(static_cast<unsigned>(ctas));
     kern<<<grid, kCtaThreads, 0, st>>>(a);
     return cudaGetLastError();
 }
