@@ -82,7 +82,7 @@ def measured_peak():
 
 
 def algorithmic_bytes(wl):
-    """Bytes the method must move (no halo re-reads, chunk map or partials).
+    """Bytes the method must move (no halo re-reads or partials).
 
     Forward: x read + out written for valid tokens of live sequences (-1
     sequences write zeros and read nothing), weights, bias, and 3 state rows
@@ -161,8 +161,7 @@ class ClockSampler:
 
 # The sources that decide what the backward launch does (kernel, helpers,
 # launch configuration): a change to any of them makes recorded counters stale.
-BWD_SOURCES = ("ccc_bwd.cu", "ccc_bwd_tma.cu", "ccc_device.cuh", "ccc_internal.h", "ccc_api.cu",
-               "ccc_chunkmap.cu")
+BWD_SOURCES = ("ccc_bwd.cu", "ccc_device.cuh", "ccc_internal.h", "ccc_api.cu")
 
 
 def kernel_source_hash():
@@ -387,7 +386,7 @@ def run_ours(args, ws, rank, local):
             "fwd_tokens_per_s": ws * T / (fwd_ms / 1e3),
             "effective_gbs": eff_gbs, "frac_of_nominal_8tbs": eff_gbs / NOMINAL_HBM_GBS,
             "frac_of_measured_hbm": eff_gbs / peak,
-            "roofline": {"kernel": "ccc_bwd call (chunk map + fused backward + ordered reduce)",
+            "roofline": {"kernel": "ccc_bwd call (fused backward + ordered reduce)",
                          "bound": "hbm", "achieved": bwd_gbs, "peak": peak, "peak_kind": peak_kind,
                          "unit": "GB/s", "frac": bwd_gbs / peak, "traffic": recorded_traffic(),
                          "algorithmic_bytes_per_launch": bb},

@@ -86,12 +86,14 @@ typedef enum {
  * (for_bwd != 0) needs for `rows` packed rows, `n_seqs` sequences and
  * `channels` channels.  Pure host arithmetic; no CUDA call.
  *
- * Forward: 0 for n_seqs <= 32 (the work items are derived in-kernel), else
- * the device chunk map (causal_conv1d_fn, workspace: rebuilt on every call).
- * Backward: the chunk map when n_seqs > 32, plus the FP32 partial sums of the
- * ordered weight/bias reduction.  The value depends only on the three sizes,
- * so a workspace sized for the largest shape can be reused (and captured in
- * a CUDA graph).  Returns 0 for invalid sizes.
+ * Forward: always 0.  The kernels split the valid rows into equal runs and
+ * find each run's first sequence themselves, on every call (the role of the
+ * chunk map of causal_conv1d_fn, workspace), so no scratch is needed.
+ * Backward: the FP32 partial sums of the ordered weight/bias reduction,
+ * R x 5 x C floats with R = 1216 / ceil(C / 256) -- at most about 6.2 MB.
+ * The value depends only on `channels` (0 for invalid sizes or an empty
+ * batch), so a workspace sized once can be reused (and captured in a CUDA
+ * graph).
  */
 size_t ccc_workspace_size(int64_t rows, int32_t n_seqs, int32_t channels, int32_t for_bwd);
 
@@ -125,8 +127,7 @@ size_t ccc_workspace_size(int64_t rows, int32_t n_seqs, int32_t channels, int32_
  *               sequence's initial history (what the forward read before it
  *               overwrote the slot; zeros for a -1 request) is stored, for
  *               ccc_bwd.  Rows of empty sequences are not written.
- *  workspace    [dev] >= ccc_workspace_size(rows, N, C, 0) bytes, 256-byte
- *               aligned (NULL allowed when that size is 0).
+ *  workspace    unused (ccc_workspace_size(..., 0) is 0); may be NULL.
  */
 int ccc_fwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
             const void *weight, int32_t w_dtype, int32_t width,
@@ -191,7 +192,8 @@ int ccc_bwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
  * CCC_NOALLOC_SCRATCH_BYTES compiled into the library, held by every GPU the
  * library is loaded on until the process exits; a shape whose
  * ccc_workspace_size(rows, N, C, 1) exceeds it returns CCC_ERR_WORKSPACE with
- * nothing enqueued.  The first call on a device looks up the array's device
+ * nothing enqueued (with the current kernels that size never exceeds about
+ * 6.2 MB, so every shape fits).  The first call on a device looks up the array's device
  * address (cudaGetSymbolAddress) and caches it; make that first call before
  * any stream capture on the device.  All calls share the array, so calls
  * whose GPU work overlaps (other streams, other host threads on the same

@@ -48,12 +48,6 @@ size_t mat_bytes(int64_t rows, int64_t stride, int C) {
     return rows > 0 ? static_cast<size_t>(((rows - 1) * stride + C) * 2) : 0;
 }
 
-size_t map_bytes(int64_t rows, int N, int B) {
-    if (N <= ccc::kMaxInlineSeqs || rows <= 0) return 0;
-    const int64_t cap = ccc::item_capacity(rows, N, B);
-    return round_up(static_cast<size_t>(1 + 2 * cap) * sizeof(int32_t), kAlignWs);
-}
-
 int dtype_size(int code) { return code == CCC_F32 ? 4 : (code == CCC_BF16 ? 2 : 0); }
 
 bool width_ok(int width) { return width >= 2 && width <= 4; }
@@ -107,12 +101,9 @@ extern "C" {
 size_t ccc_workspace_size(int64_t rows, int32_t n_seqs, int32_t channels, int32_t for_bwd) {
     if (rows < 0 || n_seqs < 0 || channels <= 0 || channels % 8) return 0;
     if (rows == 0 || n_seqs == 0) return 0;
-    if (!for_bwd) return map_bytes(rows, n_seqs, ccc::kFwdChunk);
-    const size_t mb = map_bytes(rows, n_seqs, ccc::kBwdChunk);
-    // Enough partial rows for whichever backward kernel the width picks.
-    int R = ccc::bwd_runs(rows, n_seqs, channels, false);
-    if (ccc::kBwdTma) R = std::max(R, ccc::bwd_runs(rows, n_seqs, channels, true));
-    return mb + round_up(static_cast<size_t>(R) * 5 * channels * sizeof(float), kAlignWs);
+    if (!for_bwd) return 0;  // the forward splits its work in-kernel: no scratch
+    const int R = ccc::bwd_runs(channels);
+    return round_up(static_cast<size_t>(R) * 5 * channels * sizeof(float), kAlignWs);
 }
 
 const char *ccc_status_string(int status) {
@@ -214,24 +205,10 @@ int ccc_fwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
     a.out = static_cast<uint16_t *>(out);
     a.os = static_cast<int>(out_row_stride);
     a.hist = static_cast<uint16_t *>(saved_hist);
-    a.cap = static_cast<int>(std::min<int64_t>(ccc::item_capacity(rows, N, ccc::kFwdChunk), INT32_MAX));
-    a.map = nullptr;
-
-    int launches = 0;
-    bool pdl = false;
-    if (N > ccc::kMaxInlineSeqs) {
-        int32_t *map = static_cast<int32_t *>(workspace);
-        if (ccc::launch_chunkmap(cu_seqlens, N, rows, ccc::kFwdChunk, 0, map, a.cap, st) != cudaSuccess)
-            return CCC_ERR_CUDA;
-        ++launches;
-        a.map = map;
-        pdl = true;
-    }
     a.slabs = ccc::slabs_of(C, ccc::kFwdVec);
-    a.runs = ccc::runs_per_slab(static_cast<int64_t>(sm_count()) * fwd_ctas() * ccc::kWarpsPerCta, a.slabs, a.cap);
-    if (ccc::launch_fwd(a, pdl, st) != cudaSuccess) return CCC_ERR_CUDA;
-    ++launches;
-    g_last_launches = launches;
+    a.runs = ccc::runs_per_slab(static_cast<int64_t>(sm_count()) * fwd_ctas() * ccc::kWarpsPerCta, a.slabs);
+    if (ccc::launch_fwd(a, st) != cudaSuccess) return CCC_ERR_CUDA;
+    g_last_launches = 1;
     return CCC_OK;
 }
 
@@ -320,29 +297,12 @@ int ccc_bwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
     a.dx = static_cast<uint16_t *>(dx);
     a.dxs = static_cast<int>(dx_row_stride);
     a.d_init = d_init_state;
-    a.cap = static_cast<int>(std::min<int64_t>(ccc::item_capacity(rows, N, ccc::kBwdChunk), INT32_MAX));
-    const size_t mb = map_bytes(rows, N, ccc::kBwdChunk);
-    a.part = reinterpret_cast<float *>(static_cast<char *>(workspace) + mb);
-    a.map = nullptr;
-
-    int launches = 0;
-    bool pdl = false;
-    if (N > ccc::kMaxInlineSeqs) {
-        int32_t *map = static_cast<int32_t *>(workspace);
-        if (ccc::launch_chunkmap(cu_seqlens, N, rows, ccc::kBwdChunk, 1, map, a.cap, st) != cudaSuccess)
-            return CCC_ERR_CUDA;
-        ++launches;
-        a.map = map;
-        pdl = true;
-    }
-    const bool tma = ccc::bwd_uses_tma(width, activation);
-    a.slabs = ccc::bwd_columns(C, tma);
-    a.runs = ccc::bwd_runs(rows, N, C, tma);
-    if ((tma ? ccc::launch_bwd_tma(a, pdl, st) : ccc::launch_bwd(a, pdl, st)) != cudaSuccess) return CCC_ERR_CUDA;
-    ++launches;
-    if (ccc::launch_reduce(a.part, a.runs, C, width, dweight, dbias, true, st) != cudaSuccess) return CCC_ERR_CUDA;
-    ++launches;
-    g_last_launches = launches;
+    a.part = static_cast<float *>(workspace);
+    a.slabs = ccc::bwd_slabs(C);
+    a.runs = ccc::bwd_runs(C);
+    if (ccc::launch_bwd(a, st) != cudaSuccess) return CCC_ERR_CUDA;
+    if (ccc::launch_reduce(a.part, a.runs, C, width, dweight, dbias, st) != cudaSuccess) return CCC_ERR_CUDA;
+    g_last_launches = 2;
     return CCC_OK;
 }
 

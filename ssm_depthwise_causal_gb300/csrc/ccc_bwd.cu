@@ -21,8 +21,9 @@
 // unsplit dx and d_init_state bit for bit.
 //
 // Mapping.  As in the forward: a warp owns a 32*VEC-channel slab, a lane
-// owns VEC channels, and each warp walks a contiguous run of work items.
-// Along consecutive items of one sequence the lane walks i = o0, o0+1, ...
+// owns VEC channels, and each warp walks a run of rows (an equal share of
+// the valid rows, RunWalker).  Along one sequence the lane walks i = o0,
+// o0+1, ...
 // without a break: it keeps a sliding window of 3 history rows and the 3
 // previous dz values in registers, emits dx for row i-3 once dz_i is known,
 // and accumulates dz_j * h[j+k] and dz_j of its own rows into 5*VEC FP32
@@ -35,9 +36,9 @@
 // causal_conv1d_cp, weight [D, W]) and the activation (SiLU, or none: then
 // dz = dy); W = 4 with SiLU is the contract above, and "3" reads W-1.
 //
-// Determinism.  The number of runs per slab R is fixed by (rows, N, C) only;
-// the warp with task (slab, run r) walks items [r*total/R, (r+1)*total/R) in
-// order and writes partial[r][k][c] for its channels, so every partial sum
+// Determinism.  The number of runs per slab R is fixed by C only; the warp
+// with task (slab, run r) walks rows [r*T/R, (r+1)*T/R) (T = cu_seqlens[N])
+// in order and writes partial[r][k][c] for its channels, so every partial sum
 // has a fixed operand order; the reduce kernel then sums the R partials of
 // every (k, c) in order r = 0..R-1.
 #include "ccc_device.cuh"
@@ -91,7 +92,7 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
     constexpr int H = W - 1;                            // history rows
     constexpr int VB = VEC * 2;                         // bytes per lane per row
     constexpr int RING_WARP = P * U * 2 * 32 * VB;      // ring bytes per warp
-    static_assert(P == 0 || kBwdChunk % U == 0, "items must be whole batches");
+    static_assert(P == 0 || kBwdChunk % U == 0, "segments must be whole batches");
     extern __shared__ __align__(16) unsigned char dyn_smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int gw = blockIdx.x * kWarpsPerCta + warp;  // this warp's task
@@ -113,30 +114,14 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
         gb[v] = f2_zero();
     }
 
-    grid_dependency_wait();  // the chunk map, when one was built
+    // This warp's run: a fixed share of the rows (the same for every slab),
+    // so the operand order of every partial sum is fixed.
+    RunWalker<kBwdChunk> walk;
+    walk.init(a.cu, a.N, a.rows, run, a.runs, H, true, lane);
 
-    ItemDecoder<kBwdChunk> dec;
-    dec.init(a.map, a.cap, a.cu, a.N, a.rows, true, lane);
-
-    // This warp's run: a contiguous, fixed range of items (same for every
-    // slab), so the operand order of every partial sum is fixed.
-    const int lo = static_cast<int>(static_cast<int64_t>(run) * dec.total / a.runs);
-    const int hi = static_cast<int>(static_cast<int64_t>(run + 1) * dec.total / a.runs);
-
-    // The run's last item (sequence, row after it): where its final walk
-    // stops reading ahead.
-    int last_n = -1, last_end = 0;
-    if (lo < hi) {
-        const Item l = dec.get(hi - 1, a.map, a.cu, a.rows);
-        last_n = l.n;
-        last_end = l.r0 + l.nr;
-    }
-
-    // Sliding windows, carried from one item to the next when the next item
-    // continues the same sequence: history rows h[i..i+H-1] and
-    // dz_{i-1..i-H}.
+    // Sliding windows, carried from one segment to the next along a walk:
+    // history rows h[i..i+H-1] and dz_{i-1..i-H}.
     float2 hw[H][NV], dwin[H][NV];
-    Item cur = {};
     bool live = true, read_state = false;
 
     // Ring state (P > 0): batch b of the current walk holds rows
@@ -168,20 +153,13 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
         p_row += U;
     };
 
-    for (int it = lo; it < hi; ++it) {
-        // The next item of the same sequence is the next B rows: only a new
-        // sequence needs the chunk map / offsets (and its flags) again.
-        const bool cont = it > lo && cur.r0 + cur.nr < cur.e;
-        if (cont) {
-            cur.r0 += cur.nr;
-            cur.nr = min(kBwdChunk, cur.e - cur.r0);
-        } else {
-            cur = dec.get(it, a.map, a.cu, a.rows);
-            live = !(a.cache && __ldg(a.cache + cur.n) == -1);
-            read_state = a.has_init != nullptr && __ldg(a.has_init + cur.n) != 0;
+    Item t;
+    bool cont, next_cont;
+    while (walk.next(a.cu, a.rows, lane, t, cont, next_cont)) {
+        if (!cont) {  // a new walk: the sequence's flags
+            live = !(a.cache && __ldg(a.cache + t.n) == -1);
+            read_state = a.has_init != nullptr && __ldg(a.has_init + t.n) != 0;
         }
-        const Item t = cur;
-        const bool next_cont = it + 1 < hi && t.r0 + t.nr < t.e;
         const int nr = t.nr;
         const int o0 = t.r0 - t.s, L = t.e - t.s;
         float *dinit = a.d_init ? a.d_init + static_cast<int64_t>(t.n) * H * a.C + c0 : nullptr;
@@ -203,17 +181,17 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
         if constexpr (P > 0) {
             if (!cont) {
                 // A new walk: the rows it will load are [t.r0, p_end) -- to the
-                // end of the sequence, or for the run's last sequence to H rows
-                // past the run (within the sequence).
+                // end of the sequence, or H rows past the run where the
+                // sequence goes on beyond it.
                 cp_async_wait(0);
                 p_row = t.r0;
-                p_end = t.n == last_n ? min(last_end + H, t.e) : t.e;
+                p_end = min(walk.R_hi + H, t.e);
                 issued = consumed = 0;
                 while (issued < P - 1 && p_row < p_end) issue();
             }
         }
         if (!cont) {
-            // History rows o0-H .. o0-1 (the initial history for a first item).
+            // History rows o0-H .. o0-1 (the initial history at a sequence's start).
             Raw<NV> hr[H];
 #pragma unroll
             for (int p = 0; p < H; ++p) hr[p] = raw_zero<NV>();
@@ -235,14 +213,14 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
                 for (int v = 0; v < NV; ++v) dwin[p][v] = f2_zero();
         }
 
-        // i = o0 + k.  Rows k < nr are this item's; when the next item does
-        // not continue the walk, H more steps finish dx of the last H rows
-        // (loading x / dy past the item while still inside the sequence).
+        // i = o0 + k.  Rows k < nr are this segment's; when no segment of the
+        // walk follows, H more steps finish dx of the last H rows (loading
+        // x / dy past the segment while still inside the sequence).
         const int iters = nr + (next_cont ? 0 : H);
         const int nload = L - o0 < iters ? L - o0 : iters;  // steps with i < L
         for (int base = 0; base < iters; base += U) {
             // Steady state: every step of the batch loads a row, is one of
-            // this item's tokens and emits dx of the row H back (no carry:
+            // this segment's tokens and emits dx of the row H back (no carry:
             // all i < L).  Such batches run guard-free; the first batch of a
             // walk and the tail take the general path.
             const bool fast = full && (cont || base >= H) && base + U <= nload && base + U <= nr;
@@ -334,7 +312,7 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
 #pragma unroll
                     for (int v = 0; v < NV; ++v) dz[v] = f2_zero();
                 }
-                if (k < nr) {  // this item's own token: weight / bias partials
+                if (k < nr) {  // this segment's own token: weight / bias partials
 #pragma unroll
                     for (int v = 0; v < NV; ++v) {
 #pragma unroll
@@ -346,7 +324,7 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
                 // dH[i] is complete now.  i < H: an initial-history gradient.
                 // Otherwise it is dx of row i-H, ours unless this is the first
                 // step of a walk that starts inside a sequence (then the
-                // previous item's owner finished that row).
+                // previous run finished that row).
                 const bool emit_init = i < H && dinit != nullptr;
                 const bool emit_dx = i >= H && (cont || k >= H);
                 if (emit_dx || emit_init) {
@@ -437,20 +415,13 @@ BwdKernel bwd_kernel_for(int width, int act) {
 
 }  // namespace
 
-cudaError_t launch_bwd(const BwdArgs &a, bool pdl, cudaStream_t st) {
+cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t st) {
     const BwdKernel kern = bwd_kernel_for(a.width, a.act);
     if (!kern) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(static_cast<int64_t>(a.slabs) * a.runs, kWarpsPerCta)));
     cfg.blockDim = dim3(kCtaThreads);
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    if (pdl) {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-    }
     constexpr int P = kBwdRing;
     constexpr size_t ring_bytes = static_cast<size_t>(P) * kBwdUnroll * 2 * 32 * kBwdVec * 2 * kWarpsPerCta;
     if (ring_bytes > 48 * 1024) {
@@ -471,19 +442,20 @@ cudaError_t launch_bwd(const BwdArgs &a, bool pdl, cudaStream_t st) {
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-cudaError_t launch_reduce(const float *part, int G, int C, int width, float *dweight, float *dbias, bool pdl,
+// The reduce is a programmatic dependent launch: it may become resident
+// while the backward grid drains (the backward triggers it after its walks)
+// and waits for the partials with griddepcontrol.wait.
+cudaError_t launch_reduce(const float *part, int G, int C, int width, float *dweight, float *dbias,
                           cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(5 * static_cast<int64_t>(C), 256)));
     cfg.blockDim = dim3(256);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
-    if (pdl) {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-    }
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, reduce_kernel, part, G, C, width, dweight, dbias);
 }
 

@@ -1,5 +1,5 @@
-// ccc_device.cuh -- device-side building blocks shared by the forward and
-// backward kernels of the packed width-4 causal depthwise Conv1d + SiLU.
+// ccc_device.cuh -- device-side building blocks shared by the forward,
+// backward and decode-update kernels of the packed causal depthwise Conv1d.
 //
 // Data layout (FlashInfer "flashinfer.mamba.causal_conv1d_fn", Parameters):
 // activations are BF16 [rows][C] with channels contiguous, so one lane owns
@@ -156,69 +156,6 @@ __device__ __forceinline__ Raw<NV> ld_shared(const unsigned char *p) {
     return r;
 }
 
-// Per-lane ring over a contiguous row stream [S0, S1) of NT tensors: stage k
-// holds rows S0 + k*U .. S0 + k*U + U-1 (zero-filled past S1) in slot k % P.
-// Each lane copies -- and later reads -- only its own VB bytes of a row, so
-// in-order completion of its cp.async groups is all the synchronisation
-// needed: no barrier, no cross-lane wait.  `src[t]` points at the lane's
-// bytes of row 0 of tensor t, `stride[t]` is that tensor's row stride in
-// elements.  Shared layout per warp: [P][U][NT][32 lanes][VB].
-template <int NV, int U, int P, int NT>
-struct LaneRing {
-    static constexpr int VB = NV * 4;
-    static constexpr int kWarpBytes = P * U * NT * 32 * VB;
-    uint32_t base;  // shared address of this lane's bytes in stage 0, row 0, tensor 0
-    int S0, S1;
-    int issued;     // stages issued so far
-    const uint16_t *src[NT];
-    int stride[NT];
-
-    __device__ __forceinline__ void start(int s0, int s1) {
-        cp_async_wait(0);  // nothing of a previous stream may still land
-        S0 = s0;
-        S1 = s1;
-        issued = 0;
-    }
-
-    __device__ __forceinline__ void issue(bool act) {
-        const int slot = issued % P;
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int r = S0 + issued * U + u;
-            const bool ok = act && r < S1;
-#pragma unroll
-            for (int t = 0; t < NT; ++t) {
-                const uint32_t dst = base + static_cast<uint32_t>(((slot * U + u) * NT + t) * 32 * VB);
-                cp_async<VB>(dst, ok ? src[t] + static_cast<int64_t>(r) * stride[t] : src[t], ok);
-            }
-        }
-        cp_async_commit();
-        ++issued;
-    }
-
-    // Keep the stages from the one holding row r on issued, P deep.
-    __device__ __forceinline__ void top_up(int r, bool act) {
-        const int k = (r - S0) / U;
-        while (issued < k + P && S0 + issued * U < S1) issue(act);
-    }
-
-    // Row r of tensor t (r in [S0, S1), stage already issued).
-    __device__ __forceinline__ Raw<NV> get(int r, int t) const {
-        const int j = r - S0, k = j / U;
-        cp_async_wait(issued - 1 - k);
-        const uint32_t addr = base + static_cast<uint32_t>((((k % P) * U + j % U) * NT + t) * 32 * VB);
-        Raw<NV> v;
-        if constexpr (NV == 4) {
-            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(v.u[0]), "=r"(v.u[1]), "=r"(v.u[2]), "=r"(v.u[3])
-                         : "r"(addr));
-        } else {
-            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.u[0]), "=r"(v.u[1]) : "r"(addr));
-        }
-        return v;
-    }
-};
-
 // ------------------------------------------------------------------ math --
 
 // Documented PTX approximations (PTX ISA: ex2.approx.ftz.f32, rcp.approx.ftz.f32).
@@ -246,61 +183,7 @@ __device__ __forceinline__ float2 sigmoid2(float2 z) {
 
 __device__ __forceinline__ float2 f2_zero() { return make_float2(0.0f, 0.0f); }
 
-// dz = dy * s * (1 + z * (1 - s)), s = sigmoid(z), for the recomputed
-// pre-activation z = b + w0 h0 + w1 h1 + w2 h2 + w3 hc (bias first, then the
-// four FMAs in tap order, exactly as the forward).
-__device__ __forceinline__ float2 silu_grad(float2 b, float2 w0, float2 w1, float2 w2, float2 w3, float2 h0,
-                                            float2 h1, float2 h2, float2 hc, float2 gy) {
-    float2 z = __ffma2_rn(w0, h0, b);
-    z = __ffma2_rn(w1, h1, z);
-    z = __ffma2_rn(w2, h2, z);
-    z = __ffma2_rn(w3, hc, z);
-    const float2 s = sigmoid2(z);
-    const float2 one = make_float2(1.0f, 1.0f);
-    const float2 oms = __ffma2_rn(s, make_float2(-1.0f, -1.0f), one);  // 1 - s
-    const float2 f = __ffma2_rn(z, oms, one);
-    return __fmul2_rn(gy, __fmul2_rn(s, f));
-}
-
-
 // ------------------------------------------------------ taps and bias --
-
-// Weights [C][4] FP32 or BF16 and bias [C] FP32 / BF16 / none, read once per
-// lane into packed pairs: w_k[v] holds tap k of channels c0+2v, c0+2v+1.
-template <int NV>
-__device__ __forceinline__ void load_taps(const void *w, int w_bf16, const void *b, int b_kind,
-                                          int c0, bool act, float2 (&w0)[NV], float2 (&w1)[NV],
-                                          float2 (&w2)[NV], float2 (&w3)[NV], float2 (&bb)[NV]) {
-#pragma unroll
-    for (int v = 0; v < NV; ++v) {
-        float t[2][4], bv[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int c = c0 + 2 * v + h;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                float val = 0.0f;
-                if (act) {
-                    if (w_bf16) {
-                        val = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(w)[4 * c + k]);
-                    } else {
-                        val = __ldg(reinterpret_cast<const float *>(w) + 4 * c + k);
-                    }
-                }
-                t[h][k] = val;
-            }
-            float bval = 0.0f;
-            if (act && b_kind == 1) bval = __ldg(reinterpret_cast<const float *>(b) + c);
-            if (act && b_kind == 2) bval = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(b)[c]);
-            bv[h] = bval;
-        }
-        w0[v] = make_float2(t[0][0], t[1][0]);
-        w1[v] = make_float2(t[0][1], t[1][1]);
-        w2[v] = make_float2(t[0][2], t[1][2]);
-        w3[v] = make_float2(t[0][3], t[1][3]);
-        bb[v] = make_float2(bv[0], bv[1]);
-    }
-}
 
 // Taps [C][W] (FP32 or BF16) and bias [C] (FP32 / BF16 / none) for a
 // width-W kernel, read once per lane: wt[k][v] holds tap k of channels
@@ -376,17 +259,31 @@ __device__ __forceinline__ float2 activate2_grad(float2 z, float2 gy) {
     }
 }
 
-// ---------------------------------------------------------- work items --
+// ---------------------------------------------------------- work split --
 //
-// A work item is (sequence n, first row r0, rows nr <= B) inside one
-// sequence; items of a sequence are consecutive B-row chunks in order, and
-// items are numbered sequence by sequence.  For n_seqs <= 32 every warp
-// derives the numbering itself from cu_seqlens with one shuffle scan, so
-// small batches need no scratch; otherwise the chunk-map kernel has written
-// (n, r0) pairs and the count to the workspace, afresh on each call
-// (causal_conv1d_fn, workspace).
-// `empty_items` gives each empty sequence one zero-row item (the backward
-// needs one to zero that sequence's d_init_state).
+// The valid rows of a packed batch are contiguous: sequence n owns rows
+// [cu[n], cu[n+1]) and together they fill [0, T), T = cu[N].  Run r of R
+// takes the rows [r*T/R, (r+1)*T/R) -- equal shares whatever the length mix
+// -- plus the empty sequences positioned in that range (the last run also
+// those at T).  Turning cu_seqlens into these balanced pieces of work
+// happens at the start of every kernel, on the device, every call (the
+// chunk-map role of FlashInfer "flashinfer.mamba.causal_conv1d_fn",
+// workspace; no scratch and no extra launch here): the warp finds the
+// sequence holding its first row with a 32-way search over cu_seqlens, then
+// walks forward.
+//
+// A boundary that falls inside the first H = W-1 rows of a sequence is moved
+// back to that sequence's first row (both runs apply the same rule), so a run
+// that starts inside a sequence starts at least H rows in: the H rows before
+// it are then rows of x, never initial state -- which only the run holding
+// the sequence's first row reads (and, in the forward, overwrites).
+//
+// The walker hands out segments in row order: at most B rows of one
+// sequence, clipped to the run.  Consecutive segments of one sequence form a
+// walk; a walk starts at the run's first row or at a sequence's first row,
+// and every segment but a walk's last has exactly B rows.  Empty sequences
+// come out as zero-row segments when asked for (the backward zeroes their
+// d_init_state).
 
 // Row indices fit in 32 bits (the host rejects rows > INT32_MAX: cu_seqlens
 // is int32); every address is formed in 64 bits from them.
@@ -396,142 +293,141 @@ struct Item {
     int nr;
 };
 
-// The decoder keeps three registers per lane for the in-kernel numbering
-// (lane n < N holds sequence n's clamped start, end and inclusive item
-// prefix); the chunk map, offsets and sizes are read from the kernel
-// parameters at each call, so they cost no registers across the loop.
 template <int B>
-struct ItemDecoder {
-    int ls, le, lincl;  // register scan state (no map)
-    int total;
+struct RunWalker {
+    int N;
+    int H;           // history rows: boundaries never fall in a sequence's first H rows
+    int R_lo, R_hi;  // this run's rows (R_hi before the move above; see next())
+    bool last;       // the last run (also takes empty sequences at T)
+    bool empties;    // hand out empty sequences
+    int n;           // current sequence
+    int s, e;        // its rows (clamped)
+    int r;           // its next row to hand out
+    bool fresh;      // nothing of sequence n handed out yet
+    int cbase;       // lane j caches the clamped cu[cbase + j]
+    int cval;
 
     __device__ __forceinline__ static int clamp_row(int v, int64_t rows) {
         return v < 0 ? 0 : (v > rows ? static_cast<int>(rows) : v);
     }
 
-    // The map is written by the chunk-map kernel while this grid may already
-    // be resident (programmatic dependent launch), so it is not read-only over
-    // this kernel's lifetime: it is read with L2-coherent loads (ld.global.cg),
-    // never through the non-coherent read-only path.
-    __device__ __forceinline__ void init(const int32_t *map, int cap, const int32_t *cu, int N, int64_t rows,
-                                         bool empty_items, int lane) {
-        if (map) {
-            const int cnt = __ldcg(map);
-            total = cnt < cap ? cnt : cap;
-            ls = le = lincl = 0;
+    __device__ __forceinline__ void refill(const int32_t *cu, int64_t rows, int base, int lane) {
+        cbase = base;
+        const int idx = base + lane;
+        cval = idx <= N ? clamp_row(__ldg(cu + idx), rows) : static_cast<int>(rows);
+    }
+
+    // Clamped cu[i] for cbase <= i < cbase + 32 (all lanes, same i).
+    __device__ __forceinline__ int cu_at(int i) const { return __shfl_sync(kFull, cval, i - cbase); }
+
+    // Clamped cu[i] for any i in [0, N] (all lanes, same i).
+    __device__ __forceinline__ int cu_get(const int32_t *cu, int64_t rows, int i, int lane) {
+        if (i < cbase || i >= cbase + 32) refill(cu, rows, i, lane);
+        return cu_at(i);
+    }
+
+    // Run `run` of `runs`.  All 32 lanes call with the same arguments.
+    __device__ __forceinline__ void init(const int32_t *cu, int n_seqs, int64_t rows, int run, int runs,
+                                         int hist_rows, bool want_empty, int lane) {
+        N = n_seqs;
+        H = hist_rows;
+        empties = want_empty;
+        last = run == runs - 1;
+        fresh = true;
+        s = e = r = 0;
+        n = 0;
+        refill(cu, rows, 0, lane);
+        if (N <= 0) {
+            R_lo = R_hi = 0;
             return;
         }
-        int s = 0, e = 0, ni = 0;
-        if (lane < N) {
-            s = clamp_row(__ldg(cu + lane), rows);
-            e = clamp_row(__ldg(cu + lane + 1), rows);
-            if (e < s) e = s;
-            ni = (e - s + B - 1) / B;
-            if (empty_items && ni == 0) ni = 1;
+        const int T = cu_get(cu, rows, N, lane);
+        R_lo = static_cast<int>(static_cast<int64_t>(run) * T / runs);
+        R_hi = static_cast<int>(static_cast<int64_t>(run + 1) * T / runs);
+        // n_a = first n in [0, N) with cu[n+1] >= R_lo (exists: cu[N] = T).
+        int lo = 0, hi = N - 1;
+        while (hi - lo >= 32) {
+            const int step = (hi - lo + 31) / 32;
+            const int idx = min(lo + lane * step, hi);
+            const int v = clamp_row(__ldg(cu + idx + 1), rows);
+            const unsigned m = __ballot_sync(kFull, v >= R_lo);
+            if (m == 0) {
+                lo = min(lo + 31 * step, hi) + 1;
+            } else {
+                const int j = __ffs(m) - 1;
+                const int new_hi = min(lo + j * step, hi);
+                if (j > 0) lo = min(lo + (j - 1) * step, hi) + 1;
+                hi = new_hi;
+            }
         }
-        int incl = ni;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int t = __shfl_up_sync(kFull, incl, off);
-            if (lane >= off) incl += t;
+        // hi - lo < 32: lane j tests n = lo + j with cu[lo + j + 1].
+        refill(cu, rows, lo + 1, lane);
+        const unsigned m = __ballot_sync(kFull, lane <= hi - lo && cval >= R_lo);
+        const int n_a = m ? lo + __ffs(m) - 1 : hi;
+        // A nonempty sequence ending exactly at R_lo belongs to the previous
+        // run; one holding R_lo within its first H rows starts this run.
+        n = n_a;
+        if (n < N) {
+            const int sa = cu_get(cu, rows, n, lane), ea = cu_get(cu, rows, n + 1, lane);
+            if (ea == R_lo && sa < R_lo) {
+                ++n;
+            } else if (sa < R_lo && ea > R_lo && R_lo - sa < H) {
+                R_lo = sa;
+            }
         }
-        ls = s;
-        le = e;
-        lincl = incl;
-        total = __shfl_sync(kFull, incl, 31);
+        if (n < N) load_seq(cu, rows, lane);
     }
 
-    // Sequence and first row of item `it` (all 32 lanes, same `it`).
-    __device__ __forceinline__ void head(int it, const int32_t *map, int &n, int &r0) const {
-        if (map) {
-            n = __ldcg(map + 1 + 2 * it);
-            r0 = __ldcg(map + 2 + 2 * it);
-        } else {
-            // Sequences whose items all precede `it` form a lane prefix.
-            n = __popc(__ballot_sync(kFull, lincl <= it));
-            const int s = __shfl_sync(kFull, ls, n), e = __shfl_sync(kFull, le, n);
-            const int incl = __shfl_sync(kFull, lincl, n);
-            const int ni = max((e - s + B - 1) / B, 1);
-            r0 = s + (it - (incl - ni)) * B;
-        }
+    __device__ __forceinline__ void load_seq(const int32_t *cu, int64_t rows, int lane) {
+        s = cu_get(cu, rows, n, lane);
+        e = cu_get(cu, rows, n + 1, lane);
+        if (e < s) e = s;
+        r = s > R_lo ? s : R_lo;
+        if (r > e) r = e;
+        fresh = true;
     }
 
-    __device__ __forceinline__ Item get(int it, const int32_t *map, const int32_t *cu, int64_t rows) const {
-        Item t;
-        head(it, map, t.n, t.r0);
-        if (map) {
-            t.s = clamp_row(__ldg(cu + t.n), rows);
-            t.e = clamp_row(__ldg(cu + t.n + 1), rows);
-            if (t.e < t.s) t.e = t.s;
-            t.r0 = t.r0 < t.s ? t.s : (t.r0 > t.e ? t.e : t.r0);
-        } else {
-            t.s = __shfl_sync(kFull, ls, t.n);
-            t.e = __shfl_sync(kFull, le, t.n);
+    // The next segment; false when the run is done.  `cont`: the segment
+    // continues the previous one's walk (same sequence, next rows).
+    // `more`: another segment of this walk follows it.
+    __device__ __forceinline__ bool next(const int32_t *cu, int64_t rows, int lane, Item &t, bool &cont,
+                                         bool &more) {
+        while (n < N) {
+            if (fresh) {
+                if (!(s < R_hi || (last && s == R_hi))) return false;  // starts past the run
+                if (s < R_hi && e > R_hi && R_hi - s < H) return false;  // the next run starts at s
+            }
+            const int stop = e < R_hi ? e : R_hi;
+            if (s == e) {  // empty sequence
+                if (fresh && empties) {
+                    t.n = n; t.s = s; t.e = e; t.r0 = s; t.nr = 0;
+                    cont = false;
+                    more = false;
+                    fresh = false;
+                    ++n;
+                    if (n < N) load_seq(cu, rows, lane);
+                    return true;
+                }
+            } else if (r < stop) {
+                t.n = n; t.s = s; t.e = e; t.r0 = r;
+                t.nr = stop - r < B ? stop - r : B;
+                cont = !fresh;
+                fresh = false;
+                r += t.nr;
+                more = r < stop;
+                return true;
+            }
+            if (e > R_hi) return false;  // the sequence continues in the next run
+            ++n;
+            if (n < N) load_seq(cu, rows, lane);
         }
-        const int left = t.e - t.r0;
-        t.nr = left < B ? left : B;
-        return t;
+        return false;
     }
 };
 
-// ------------------------------------------------ mbarrier + bulk copies --
-//
-// Shared-memory mbarriers (PTX mbarrier.*) and the bulk-copy engine
-// (cp.async.bulk, global -> shared, completion counted in bytes on an
-// mbarrier).  Every wait is bounded: after kSpinLimit polls (each one a
-// try_wait that may suspend for up to kSuspendNs) it gives up and returns
-// false, so a broken handshake ends the kernel instead of hanging the GPU.
+// ------------------------------------------------------- L2 prefetch --
 
-constexpr int kSpinLimit = 1 << 22;
-constexpr uint32_t kSuspendNs = 1000;
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-// Make initialised barriers visible to the async (bulk-copy) proxy.
-__device__ __forceinline__ void mbar_init_fence() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-// true once the barrier phase with this parity has completed.
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(bar), "r"(parity), "r"(kSuspendNs)
-        : "memory");
-    return done != 0;
-}
-
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    for (int i = 0; i < kSpinLimit; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
-}
-
-// One bulk copy global -> shared; `bytes` and both addresses are multiples of
-// 16.  Completion is reported to `bar` as `bytes` transaction bytes.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-
-// Ask the bulk-copy engine to bring `bytes` (a multiple of 16, 16-byte
-// aligned) into L2; nothing is written to shared memory and nothing waits.
+// Ask L2 to fetch `bytes` (a multiple of 16) at the 16-byte aligned `p`.
 __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }

@@ -13,24 +13,24 @@
 // and the activation (SiLU or none, the same page's `activation`); W = 4
 // with SiLU is FlashInfer's contract.
 //
-// Mapping.  A warp owns one (work item, 32*VEC-channel slab): up to B rows
-// of one sequence.  Lane l holds channels [c0, c0+VEC) with c0 = (slab*32 +
-// l)*VEC, keeps the three previous rows in registers as FP32 pairs, and
-// streams its rows U at a time (U independent 16-byte loads in flight per
-// lane before any math).  The three rows before a sequence's first item come
-// from the state slot (or are zeros).  The warp that runs a
-// sequence's first item is the only one that touches that slot: it reads the
-// initial history and, after its own rows, writes the final three values (for
-// len >= 3 these are x's last three rows, re-read from global; for shorter
-// sequences they mix the initial history and x), so the read always precedes
-// the write in program order and no other warp can race with it.
+// Mapping.  A warp owns one task: a 32*VEC-channel slab and a run of rows
+// (RunWalker: equal shares of the valid rows).  Lane l holds channels
+// [c0, c0+VEC) with c0 = (slab*32 + l)*VEC, keeps the H = W-1 previous rows in
+// registers as FP32 pairs, and streams its rows U at a time (U independent
+// 16-byte loads in flight per lane before any math; lanes 0..U-1 also ask L2
+// to prefetch the warp's slab a few rows ahead).  The window is carried from
+// one segment to the next along a sequence, so the H rows before a walk are
+// re-read (from L2: the neighbouring run) only where a run starts inside a
+// sequence.  The rows before a sequence's first row come from the state slot
+// (or are zeros).  The warp whose run holds a sequence's first row is the
+// only one that touches that slot: it reads the initial history and, after
+// its own rows, writes the final values (for len >= H these are x's last H
+// rows, re-read from global; for shorter sequences they mix the initial
+// history and x), so the read always precedes the write in program order and
+// no other warp can race with it.
 //
-// The grid is one resident wave of CTAs of 8 warps; each warp owns a
-// (slab, item run) task (ccc_internal.h, runs_per_slab) and walks its
-// contiguous run of items and carries its 3-row window from one item to the
-// next when they continue the same sequence, so the 3 rows before a walk are
-// re-read (from L2: the neighbouring warp's run) only where a run starts
-// inside a sequence.
+// The grid is one resident wave of CTAs of 8 warps; warp g takes slab
+// g % slabs and run g / slabs.
 #include "ccc_device.cuh"
 #include "ccc_internal.h"
 
@@ -94,14 +94,10 @@ __device__ __forceinline__ Raw<NV> fwd_row(const float2 (&wt)[W][NV], const floa
     return y;
 }
 
-// P = 0: rows are loaded straight into registers, U per batch.  P > 0: each
-// lane streams its run's rows through a P-stage shared-memory ring
-// (LaneRing, cp.async), so loads run ahead of the math.
-template <int VEC, int U, int P, int W, bool ACT>
+template <int VEC, int U, int W, bool ACT>
 __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const FwdArgs a) {
     constexpr int NV = VEC / 2;
     constexpr int H = W - 1;  // history rows
-    extern __shared__ __align__(16) unsigned char fwd_smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int gw = blockIdx.x * kWarpsPerCta + warp;  // this warp's task
     if (gw >= a.slabs * a.runs) return;               // (whole warp) no task in the last CTA
@@ -114,50 +110,20 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
     float2 wt[W][NV], bb[NV];
     load_taps_w<NV, W>(a.w, a.w_bf16, a.b, a.b_kind, c0, act, wt, bb);
 
-    grid_dependency_wait();  // the chunk map, when one was built
-
-    ItemDecoder<kFwdChunk> dec;
-    dec.init(a.map, a.cap, a.cu, a.N, a.rows, false, lane);
-
-    // This warp's run of consecutive items (the same rows for every slab).
-    const int lo = static_cast<int>(static_cast<int64_t>(run) * dec.total / a.runs);
-    const int hi = static_cast<int>(static_cast<int64_t>(run + 1) * dec.total / a.runs);
+    RunWalker<kFwdChunk> walk;
+    walk.init(a.cu, a.N, a.rows, run, a.runs, H, false, lane);
 
     float2 hw[H][NV];  // the H rows before the current one, oldest first
 
-    using Ring = LaneRing<NV, U, (P > 0 ? P : 1), 1>;
-    Ring ring;
-    if constexpr (P > 0) {
-        ring.base = smem_addr(fwd_smem + warp * Ring::kWarpBytes) + lane * Ring::VB;
-        ring.src[0] = a.x + c0;
-        ring.stride[0] = a.xs;
-        if (lo < hi) {
-            // The run's rows: from its first item (and the H rows before it
-            // when it starts inside a sequence) to the end of its last item.
-            const Item f = dec.get(lo, a.map, a.cu, a.rows);
-            const Item l = dec.get(hi - 1, a.map, a.cu, a.rows);
-            ring.start(f.r0 > f.s ? f.r0 - H : f.r0, l.r0 + l.nr);
-        } else {
-            ring.start(0, 0);
-        }
-    }
-
-    Item cur = {};
+    Item t;
+    bool cont, more;
     int q = -2;
     bool has_init_n = false;
-    for (int it = lo; it < hi; ++it) {
-        // The next item of the same sequence is the next B rows: only a new
-        // sequence needs the chunk map / offsets (and its slot) again.
-        const bool cont = it > lo && cur.r0 + cur.nr < cur.e;
-        if (cont) {
-            cur.r0 += cur.nr;
-            cur.nr = min(kFwdChunk, cur.e - cur.r0);
-        } else {
-            cur = dec.get(it, a.map, a.cu, a.rows);
-            q = a.cache ? __ldg(a.cache + cur.n) : -2;
-            has_init_n = a.has_init != nullptr && __ldg(a.has_init + cur.n) != 0;
+    while (walk.next(a.cu, a.rows, lane, t, cont, more)) {
+        if (!cont) {  // a new sequence (or the run's first rows): its slot and flag
+            q = a.cache ? __ldg(a.cache + t.n) : -2;
+            has_init_n = a.has_init != nullptr && __ldg(a.has_init + t.n) != 0;
         }
-        const Item t = cur;
         const int nr = t.nr;
         if (nr <= 0) continue;
         const int o0 = t.r0 - t.s, L = t.e - t.s;
@@ -180,7 +146,7 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
 
         if (!cont) {
             // The H history rows before r0 (raw BF16 bits): the initial
-            // state (or zeros) for a sequence's first item, else x rows.
+            // state (or zeros) for a sequence's first rows, else x rows.
             Raw<NV> hr[H];
 #pragma unroll
             for (int p = 0; p < H; ++p) hr[p] = raw_zero<NV>();
@@ -190,10 +156,6 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
 #pragma unroll
                     for (int p = 0; p < H; ++p)
                         st_plain<NV>(a.hist + (static_cast<int64_t>(t.n) * H + p) * a.C + c0, hr[p]);
-            } else if constexpr (P > 0) {
-                ring.top_up(t.r0 - H, act);
-#pragma unroll
-                for (int p = 0; p < H; ++p) hr[p] = ring.get(t.r0 - H + p, 0);
             } else if (act) {
 #pragma unroll
                 for (int p = 0; p < H; ++p) hr[p] = ld_ro<NV>(xrow - static_cast<int64_t>(H - p) * a.xs);
@@ -203,22 +165,8 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
         }
 
         int base = 0;
-        if constexpr (P > 0) {
-            for (; base < nr; base += U) {
-                ring.top_up(t.r0 + base, act);
-                Raw<NV> cur[U];
-#pragma unroll
-                for (int u = 0; u < U; ++u) cur[u] = base + u < nr ? ring.get(t.r0 + base + u, 0) : raw_zero<NV>();
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    if (base + u >= nr) break;
-                    const Raw<NV> y = fwd_row<W, ACT, NV>(wt, bb, hw, cur[u]);
-                    if (act) st_stream<NV>(orow + static_cast<int64_t>(base + u) * a.os, y);
-                }
-            }
-        }
-        if (full && P == 0) {
-            // Every lane active and the batch inside the item: no guards.
+        if (full) {
+            // Every lane active and the batch inside the segment: no guards.
             const uint16_t *xp = xrow;
             uint16_t *op = orow;
             for (; base + U <= nr; base += U) {
@@ -258,7 +206,8 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
         }
 
         // Final H raw history values h[L .. L+H) -> positions 0:H, by the
-        // warp that read the initial ones (read before write).
+        // warp that read the initial ones (read before write; the values
+        // come from x, whoever computes those rows).
         if (o0 == 0 && pool && L > 0 && act) {
             Raw<NV> init[H];
 #pragma unroll
@@ -286,14 +235,13 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
 
 }  // namespace
 
-constexpr size_t kFwdRingBytes =
-    kFwdRing > 0 ? static_cast<size_t>(LaneRing<kFwdVec / 2, kFwdUnroll, (kFwdRing > 0 ? kFwdRing : 1), 1>::kWarpBytes) *
-                       kWarpsPerCta
-                 : 0;
+// Rows per batch: a multiple of the history length where that is cheap (the
+// sliding window then returns to the same registers every batch).
+constexpr int fwd_unroll(int W) { return W == 4 ? kFwdUnrollW4 : kFwdUnroll; }
 
 template <int W, bool ACT>
 constexpr auto fwd_kernel_of() {
-    return fwd_kernel<kFwdVec, kFwdUnroll, kFwdRing, W, ACT>;
+    return fwd_kernel<kFwdVec, fwd_unroll(W), W, ACT>;
 }
 
 using FwdKernel = void (*)(const FwdArgs);
@@ -311,46 +259,20 @@ FwdKernel fwd_kernel_for(int width, int act) {
     }
 }
 
-// Opt in to more than 48 KB of dynamic shared memory, once per device and
-// instantiation.
-cudaError_t fwd_prepare(FwdKernel kern, int slot) {
-    if (kFwdRingBytes <= 48 * 1024) return cudaSuccess;
-    static bool attr_set[64][6] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64 && attr_set[dev][slot]) return cudaSuccess;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kFwdRingBytes));
-    if (e == cudaSuccess && dev >= 0 && dev < 64) attr_set[dev][slot] = true;
-    return e;
-}
-
 int fwd_ctas_per_sm() {
     int n = 0;
-    const FwdKernel kern = fwd_kernel_for(4, 1);
-    if (fwd_prepare(kern, 5) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kCtaThreads, kFwdRingBytes) != cudaSuccess || n < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_kernel_for(4, 1), kCtaThreads, 0) != cudaSuccess ||
+        n < 1)
         n = kFwdMinBlocks;
     return n;
 }
 
-cudaError_t launch_fwd(const FwdArgs &a, bool pdl, cudaStream_t st) {
+cudaError_t launch_fwd(const FwdArgs &a, cudaStream_t st) {
     const FwdKernel kern = fwd_kernel_for(a.width, a.act);
     if (!kern) return cudaErrorInvalidValue;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(static_cast<int64_t>(a.slabs) * a.runs, kWarpsPerCta)));
-    cfg.blockDim = dim3(kCtaThreads);
-    cfg.dynamicSmemBytes = kFwdRingBytes;
-    cfg.stream = st;
-    if (const cudaError_t e = fwd_prepare(kern, (a.width - 2) * 2 + (a.act ? 1 : 0)); e != cudaSuccess) return e;
-    cudaLaunchAttribute attr[1];
-    if (pdl) {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-    }
-    return cudaLaunchKernelEx(&cfg, kern, a);
+    const dim3 grid(static_cast<unsigned>(ceil_div(static_cast<int64_t>(a.slabs) * a.runs, kWarpsPerCta)));
+    kern<<<grid, kCtaThreads, 0, st>>>(a);
+    return cudaGetLastError();
 }
 
 }  // namespace ccc

@@ -17,8 +17,10 @@
 // therefore come before any stream capture on it.
 //
 // Every call uses the same array and leaves its contents behind for the next
-// call.  Nothing in it has to start at zero: the backward writes the chunk-map
-// count and every partial sum before reading them.  Two calls whose work
+// call.  Nothing in it has to start at zero: the backward writes every
+// partial sum before the reduction reads it.  The backward's scratch is
+// R x 5 x C floats with R x ceil(C / 256) <= 1216, at most about 6.2 MB, so
+// every shape fits; the size check stays as a guard.  Two calls whose work
 // overlaps on the GPU (different streams, or different host threads on the
 // same device) race on the array; callers must serialize them.
 #include <mutex>

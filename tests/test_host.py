@@ -47,22 +47,29 @@ def test_status_strings(lib):
 
 def test_workspace_size_rules(lib):
     ws = ccc.ccc_workspace_size
-    # forward: no scratch up to 32 sequences (in-kernel item scan)
+    # forward: never any scratch (the work split is found in-kernel)
     assert ws(16384, 4, 4096, False) == 0
-    assert ws(16384, 32, 4096, False) == 0
-    # forward, N > 32: 1 + 2 * (ceil(rows/64) + N) int32, rounded to 256 bytes
-    n = (1 + 2 * ((65536 + 63) // 64 + 200)) * 4
-    assert ws(65536, 200, 7168, False) == (n + 255) // 256 * 256
-    # backward always carries the FP32 partial sums
-    assert ws(16384, 4, 4096, True) > 0
-    assert ws(65536, 200, 7168, True) > ws(65536, 200, 7168, False)
+    assert ws(65536, 200, 7168, False) == 0
+    assert ws(1 << 24, 100000, 8192, False) == 0
+    # backward: the FP32 partial sums, R = 1216 // ceil(C / 256) rows of
+    # [5][C] floats, rounded up to 256 bytes; independent of rows and N
+    for C in (8, 256, 264, 4096, 7168, 8192):
+        R = max(1, 1216 // ((C + 255) // 256))
+        assert ws(65536, 200, C, True) == (R * 5 * C * 4 + 255) // 256 * 256, C
+        assert ws(16, 1, C, True) == ws(1 << 24, 9999, C, True)
     # degenerate / invalid
     assert ws(0, 4, 4096, True) == 0
     assert ws(100, 0, 4096, False) == 0
     assert ws(100, 4, 12, False) == 0
     assert ws(-1, 4, 4096, False) == 0
-    # grows monotonically with the problem and depends only on the sizes
-    assert ws(65536, 200, 7168, True) == ws(65536, 200, 7168, True)
+
+
+def test_noalloc_scratch_holds_every_shape(lib):
+    """The backward's scratch is R * 5 * C floats with R * ceil(C/256) <= 1216,
+    at most ~6.2 MB: every shape fits the fixed array behind
+    ccc_bwd_noalloc."""
+    worst = max(ccc.ccc_workspace_size(1 << 20, 1000, C, True) for C in range(8, 70000, 8))
+    assert worst <= _lib.NOALLOC_SCRATCH_BYTES
 
 
 P = ctypes.c_void_p
@@ -105,8 +112,7 @@ def call_fwd(lib, a):
     (dict(state=A * 6, slots=8, L=4, s0=1024, s1=4, s2=1, ci=None), E_NULL),
     (dict(out=A + 64 * 2), E_ALIAS),            # out overlaps x
     (dict(hist=A + 256, N=4), E_ALIAS),         # saved_hist inside x
-    (dict(N=40, ws=None), E_WS),                # N > 32 needs the chunk map
-    (dict(N=40, ws=A * 8, wsb=16), E_WS),
+    (dict(N=40, ws=None, rows=0), OK),          # the forward needs no workspace
     (dict(rows=0), OK),                         # nothing to do, nothing launched
     (dict(N=0), OK),
     (dict(W=5), E_SHAPE),                       # widths 2..4
