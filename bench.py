@@ -326,7 +326,11 @@ def run_ours(args, ws, rank, local):
     eff_gbs = (fb + bb) / (ms_step / 1e3) / 1e9
     bwd_gbs = bb / (bwd_ms / 1e3) / 1e9
 
-    # ---- end to end: pinned host inputs in, results out, every step
+    # ---- end to end: every step copies its inputs in from pinned host memory
+    # and its results out, through the public API.  Steps are pipelined the
+    # way a caller would run them: two device buffer sets, one stream per
+    # direction of copy and one for compute, so step k+1's inputs travel in
+    # while step k computes and step k-1's results travel out.
     hx = torch.empty(wl.x.shape, dtype=wl.x.dtype, pin_memory=True)
     hdy = torch.empty(wl.dy.shape, dtype=wl.dy.dtype, pin_memory=True)
     hx.copy_(wl.x)
@@ -335,33 +339,70 @@ def run_ours(args, ws, rank, local):
     hdx = torch.empty(dx.shape, dtype=dx.dtype, pin_memory=True)
     hdw = torch.empty(dw.shape, dtype=dw.dtype, pin_memory=True)
     hdb = torch.empty(db.shape, dtype=db.dtype, pin_memory=True)
-    dxin = torch.empty_like(wl.x)
-    ddyin = torch.empty_like(wl.dy)
+    sets = []
+    for _ in range(2):
+        sets.append(dict(x=torch.empty_like(wl.x), dy=torch.empty_like(wl.dy), out=torch.empty_like(wl.x),
+                         dx=torch.empty_like(wl.x), hist=torch.empty_like(hist), dw=torch.empty_like(dw),
+                         db=torch.empty_like(db)))
     h2d = hx.numel() * 2 + hdy.numel() * 2
     d2h = hout.numel() * 2 + hdx.numel() * 2 + hdw.numel() * 4 + hdb.numel() * 4
-    e2e_steps = max(1, min(K, 5))
+    e2e_steps = max(4, min(K, 10))
+    s_in = torch.cuda.Stream(device=dev)
+    s_out = torch.cuda.Stream(device=dev)
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    in_free = [None, None]   # compute of the step two back is done with set b's inputs
+    out_free = [None, None]  # results of the step two back have left set b
 
-    def e2e_step():
-        dxin.copy_(hx, non_blocking=True)
-        ddyin.copy_(hdy, non_blocking=True)
-        step(dxin, ddyin, stream)
-        hout.copy_(out, non_blocking=True)
-        hdx.copy_(dx, non_blocking=True)
-        hdw.copy_(dw, non_blocking=True)
-        hdb.copy_(db, non_blocking=True)
+    def e2e_step(k):
+        b = k % 2
+        d = sets[b]
+        with torch.cuda.stream(s_in):
+            if in_free[b] is not None:
+                s_in.wait_event(in_free[b])
+            d["x"].copy_(hx, non_blocking=True)
+            d["dy"].copy_(hdy, non_blocking=True)
+            in_ready = ev()
+            in_ready.record(s_in)
+        with torch.cuda.stream(stream):
+            stream.wait_event(in_ready)
+            if out_free[b] is not None:
+                stream.wait_event(out_free[b])
+            ccc.ccc_fwd(d["x"], wl.weight, wl.bias, None, wl.cu_seqlens, None, None, d["out"], d["hist"], ws_f,
+                        stream=stream)
+            fwd_done = ev()
+            fwd_done.record(stream)
+            ccc.ccc_bwd(d["x"], wl.weight, wl.bias, d["hist"], wl.cu_seqlens, None, None, d["dy"], None, d["dx"],
+                        d["dw"], d["db"], None, ws_b, stream=stream)
+            bwd_done = ev()
+            bwd_done.record(stream)
+            in_free[b] = bwd_done
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(fwd_done)
+            hout.copy_(d["out"], non_blocking=True)
+            s_out.wait_event(bwd_done)
+            hdx.copy_(d["dx"], non_blocking=True)
+            hdw.copy_(d["dw"], non_blocking=True)
+            hdb.copy_(d["db"], non_blocking=True)
+            done = ev()
+            done.record(s_out)
+            out_free[b] = done
 
-    with torch.cuda.stream(stream):
-        e2e_step()
+    for k in range(2):  # warm the pipeline's buffers and streams
+        e2e_step(k)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record(stream)
+    in_free[:] = [None, None]
+    out_free[:] = [None, None]
+    e0.record(s_in)
+    s_out.wait_stream(s_in)
+    stream.wait_stream(s_in)
+    for k in range(e2e_steps):
+        e2e_step(k)
+    s_out.wait_stream(stream)
+    e1.record(s_out)
     torch.cuda.synchronize()
     e2e_ms = job_max(e0.elapsed_time(e1) / e2e_steps, dist, dev)
     e2e_val = job_throughput(ws, T, e2e_ms)
@@ -392,7 +433,9 @@ def run_ours(args, ws, rank, local):
                          "algorithmic_bytes_per_launch": bb},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_ms, "steps": e2e_steps},
+                    "ms_per_step": e2e_ms, "steps": e2e_steps,
+                    "how": "pinned host x, dy in and out, dx, dweight, dbias back every step; steps pipelined "
+                           "over two device buffer sets with separate copy-in, compute and copy-out streams"},
             "gpu_launches": gpu_launches,
             "clocks": clk,
         }
