@@ -129,6 +129,8 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
     const uint32_t ring = smem_addr(dyn_smem + warp * RING_WARP) + lane * VB;
     const unsigned char *ring_p = dyn_smem + warp * RING_WARP + lane * VB;
     int p_row = 0, p_end = 0, issued = 0, consumed = 0;
+    int st_in = 0, st_out = 0;            // ring stage of the next issue / the next batch consumed
+    const uint16_t *px = a.x, *pg = a.dy;  // this lane's bytes of row p_row
     auto issue = [&]() {
         if constexpr (kBwdPrefetch > 0) {
             // lanes 0..2U-1: the warp's slab of x / dy rows PF ahead into L2
@@ -139,18 +141,33 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
                 prefetch_l2(base_ptr + slab * 32 * VEC, 32 * VEC * 2);
             }
         }
-        const int st = issued % (P > 0 ? P : 1);
+        const uint32_t stage = ring + static_cast<uint32_t>(st_in * U * 2 * 32 * VB);
+        if (act && p_row + U <= p_end) {  // the whole batch inside the walk: plain copies
+            const uint16_t *qx = px, *qg = pg;
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int row = p_row + u;
-            const bool ok = act && row < p_end;
-            const uint32_t off = static_cast<uint32_t>(((st * U + u) * 2) * 32 * VB);
-            cp_async<VB>(ring + off, ok ? a.x + static_cast<int64_t>(row) * a.xs + c0 : a.x, ok);
-            cp_async<VB>(ring + off + 32 * VB, ok ? a.dy + static_cast<int64_t>(row) * a.dys + c0 : a.dy, ok);
+            for (int u = 0; u < U; ++u) {
+                const uint32_t off = static_cast<uint32_t>((u * 2) * 32 * VB);
+                cp_async<VB>(stage + off, qx, true);
+                cp_async<VB>(stage + off + 32 * VB, qg, true);
+                qx += a.xs;
+                qg += a.dys;
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int row = p_row + u;
+                const bool ok = act && row < p_end;
+                const uint32_t off = static_cast<uint32_t>((u * 2) * 32 * VB);
+                cp_async<VB>(stage + off, ok ? px + static_cast<int64_t>(u) * a.xs : a.x, ok);
+                cp_async<VB>(stage + off + 32 * VB, ok ? pg + static_cast<int64_t>(u) * a.dys : a.dy, ok);
+            }
         }
         cp_async_commit();
         ++issued;
+        st_in = st_in + 1 == (P > 0 ? P : 1) ? 0 : st_in + 1;
         p_row += U;
+        px += static_cast<int64_t>(U) * a.xs;
+        pg += static_cast<int64_t>(U) * a.dys;
     };
 
     Item t;
@@ -187,6 +204,9 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
                 p_row = t.r0;
                 p_end = min(walk.R_hi + H, t.e);
                 issued = consumed = 0;
+                st_in = st_out = 0;
+                px = a.x + static_cast<int64_t>(p_row) * a.xs + c0;
+                pg = a.dy + static_cast<int64_t>(p_row) * a.dys + c0;
                 while (issued < P - 1 && p_row < p_end) issue();
             }
         }
@@ -256,8 +276,13 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
                 }
             } else {
                 if (base < nload) {  // the next batch of the walk (zero-filled past p_end)
-                    cp_async_wait(issued - consumed - 1);
-                    const unsigned char *src = ring_p + (consumed % P) * U * 2 * 32 * VB;
+                    if (issued - consumed == P - 1) {
+                        cp_async_wait(P - 2);  // steady state: the oldest of P-1 batches in flight
+                    } else {
+                        cp_async_wait(issued - consumed - 1);
+                    }
+                    const unsigned char *src = ring_p + st_out * U * 2 * 32 * VB;
+                    st_out = st_out + 1 == P ? 0 : st_out + 1;
 #pragma unroll
                     for (int u = 0; u < U; ++u) {
                         xr[u] = ld_shared<NV>(src + (u * 2) * 32 * VB);
