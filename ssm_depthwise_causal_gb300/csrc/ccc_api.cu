@@ -372,6 +372,7 @@ int ccc_update(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
     a.out = static_cast<uint16_t *>(out);
     a.os = static_cast<int>(out_row_stride);
     a.slabs = ccc::update_slabs(C);
+    a.groups = ccc::update_groups(N, a.slabs, sm_count());
     if (ccc::launch_update(a, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return CCC_ERR_CUDA;
     g_last_launches = 1;
     return CCC_OK;

@@ -168,6 +168,7 @@ struct UpdArgs {
     uint16_t *out;
     int os;
     int slabs;
+    int groups;  // sequence groups per slab (CTA b: slab b % slabs, group b / slabs)
 };
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -201,6 +202,7 @@ cudaError_t launch_reduce(const float *part, int G, int C, int width, float *dwe
                           cudaStream_t st);
 int update_slabs(int C);
 int update_stage_max_len();
+int update_groups(int N, int slabs, int sms);
 cudaError_t launch_update(const UpdArgs &a, cudaStream_t st);
 
 }  // namespace ccc
