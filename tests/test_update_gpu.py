@@ -130,6 +130,15 @@ def test_decode_chain_variants(cuda_device, width, act):
                steps=4, seed=20 + width, b_dtype=None)
 
 
+@pytest.mark.parametrize("width,L", [(4, 3), (4, 4), (4, 8), (3, 2), (3, 4), (2, 1), (2, 2), (2, 8)])
+def test_dense_pool_every_length(cuda_device, width, L):
+    """The dense history-contiguous pool at every staged length the kernel
+    specialises for (G = 8 / gcd(L, 8) channels per thread), drafts up to
+    L - W + 2 tokens so every position can be written."""
+    _run_chain(cuda_device, width=width, act="silu" if L % 2 else None, layout="dense", C=264, N=11, L=L,
+               kmax=L - width + 2, steps=6, seed=60 + 10 * width + L)
+
+
 def test_plain_decode_one_token(cuda_device):
     """k = 1 every step, accepted count omitted (= 1): the ordinary decode
     shift; the pool is exactly L = W-1 long."""
