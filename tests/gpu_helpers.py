@@ -50,20 +50,26 @@ def channel_contiguous_pool(pool: torch.Tensor) -> torch.Tensor:
     return pool.transpose(1, 2).contiguous().transpose(1, 2)
 
 
+def _wide(t: torch.Tensor, pad: int) -> torch.Tensor:
+    """`t` [rows, C] as a column slice of a wider buffer (row stride C + pad)."""
+    wide = torch.zeros((t.shape[0], t.shape[1] + pad), dtype=t.dtype, device=t.device)
+    wide[:, :t.shape[1]] = t
+    return wide[:, :t.shape[1]]
+
+
 def run_gpu(wl: workloads.Workload, *, backward=True, d_final=None, want_d_init=True,
-            pool_layout="history", x_pad_cols=0) -> GpuResult:
-    """One forward (+ backward) of a device-resident workload through the C ABI."""
+            pool_layout="history", x_pad_cols=0, out_pad_cols=0) -> GpuResult:
+    """One forward (+ backward) of a device-resident workload through the C ABI.
+    `x_pad_cols` / `out_pad_cols` give x and dy / out and dx row strides
+    larger than C."""
     dev = wl.x.device
-    x = wl.x
-    if x_pad_cols:  # x as a column slice of a wider buffer (row stride > C)
-        wide = torch.zeros((wl.rows, wl.C + x_pad_cols), dtype=torch.bfloat16, device=dev)
-        wide[:, :wl.C] = wl.x
-        x = wide[:, :wl.C]
+    x = _wide(wl.x, x_pad_cols) if x_pad_cols else wl.x
     state = None
     if wl.conv_state is not None:
         state = wl.conv_state.clone() if pool_layout == "history" else channel_contiguous_pool(wl.conv_state)
     H = wl.width - 1
-    out = fill_sentinel(torch.empty((wl.rows, wl.C), dtype=torch.bfloat16, device=dev))
+    out = fill_sentinel(torch.empty((wl.rows, wl.C + out_pad_cols), dtype=torch.bfloat16, device=dev))
+    out = out[:, :wl.C]
     hist = fill_sentinel(torch.empty((wl.n_seqs, H, wl.C), dtype=torch.bfloat16, device=dev))
     ws = torch.empty(max(1, ccc.ccc_workspace_size(wl.rows, wl.n_seqs, wl.C, False)),
                      dtype=torch.uint8, device=dev)
@@ -71,14 +77,16 @@ def run_gpu(wl: workloads.Workload, *, backward=True, d_final=None, want_d_init=
                 wl.has_initial_state, out, hist, ws, activation=wl.activation)
     res = GpuResult(out=out, state=state, hist=hist)
     if backward:
-        dx = fill_sentinel(torch.empty((wl.rows, wl.C), dtype=torch.bfloat16, device=dev))
+        dx = fill_sentinel(torch.empty((wl.rows, wl.C + out_pad_cols), dtype=torch.bfloat16, device=dev))
+        dx = dx[:, :wl.C]
+        dy = _wide(wl.dy, x_pad_cols) if x_pad_cols else wl.dy
         dw = torch.full((wl.C, wl.width), float("nan"), device=dev)
         db = torch.full((wl.C,), float("nan"), device=dev) if wl.bias is not None else None
         di = torch.full((wl.n_seqs, H, wl.C), float("nan"), device=dev) if want_d_init else None
         wsb = torch.empty(ccc.ccc_workspace_size(wl.rows, wl.n_seqs, wl.C, True), dtype=torch.uint8,
                           device=dev)
         ccc.ccc_bwd(x, wl.weight, wl.bias, hist, wl.cu_seqlens, wl.cache_indices,
-                    wl.has_initial_state, wl.dy, d_final, dx, dw, db, di, wsb, activation=wl.activation)
+                    wl.has_initial_state, dy, d_final, dx, dw, db, di, wsb, activation=wl.activation)
         res.dx, res.dweight, res.dbias, res.d_init = dx, dw, db, di
     torch.cuda.synchronize()
     return res

@@ -305,3 +305,14 @@ def test_variant_split_equals_unsplit(cuda_device, width, act):
     got = H.gpu_numpy(res, chans)
     got["hist"] = ref["hist"]  # no history was saved in the unsplit call
     H.compare(sub, ref, got)
+
+
+@pytest.mark.parametrize("width,act", [(4, "silu"), (3, None), (2, "silu")])
+def test_all_row_strides(cuda_device, width, act):
+    """x, dy, out and dx as column slices of wider buffers (row strides C + 24
+    and C + 40: GDP feeds the conv a slice of the in_proj output,
+    gdp_context_parallel), with N > 32 and a partial slab."""
+    lengths = tuple(int(v) for v in np.random.default_rng(9).integers(0, 70, 45))
+    wl = workloads.make_custom(lengths, 264, rows=sum(lengths) + 3, seed=31, device=cuda_device,
+                               n_minus_one=3, width=width, activation=act)
+    check(wl, H.run_gpu(wl, x_pad_cols=24, out_pad_cols=40))
