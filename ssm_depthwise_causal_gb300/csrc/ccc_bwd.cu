@@ -48,38 +48,47 @@ namespace ccc {
 
 namespace {
 
-// One step of the walk for one channel pair: dz of the current row, the
-// dH accumulation (carry first, then tap k on dz_{i-k}: dz, dwin[0] =
-// dz_{i-1}, ...), all with the forward's operand order.
-template <int W, bool ACT, int NV>
-__device__ __forceinline__ float2 bwd_dz(const float2 (&wt)[W][NV], float2 b, const float2 (&hw)[W - 1][NV],
-                                         float2 hc, float2 gy, int v) {
+// Sliding windows as rings.  Row k of a walk keeps its history value and its
+// dz in slot k % RS of two RS-slot rings (RS = the batch size U >= W).  A
+// walk's batches start at multiples of U from the walk's first row, so row
+// u of a batch always sits in slot u: every index below is a compile-time
+// constant and nothing moves between rows.
+// dz of row u for one channel pair: the pre-activation (bias, then tap k on
+// history row u-H+k, then tap H on the current row -- the forward's operand
+// order) through the activation's derivative.
+template <int W, bool ACT, int RS, int NV>
+__device__ __forceinline__ float2 ring_dz(const float2 (&wt)[W][NV], float2 b, const float2 (&hr)[RS][NV], float2 hc,
+                                          float2 gy, int u, int v) {
     if constexpr (ACT) {
-        return activate2_grad<true>(conv_pre<W, NV>(wt, b, hw, hc, v), gy);
+        float2 z = b;
+#pragma unroll
+        for (int k = 0; k < W - 1; ++k) z = __ffma2_rn(wt[k][v], hr[slot<RS>(u, W - 1 - k)][v], z);
+        z = __ffma2_rn(wt[W - 1][v], hc, z);
+        return activate2_grad<true>(z, gy);
     } else {
         return gy;
     }
 }
 
-template <int W, int NV>
-__device__ __forceinline__ float2 bwd_dh(const float2 (&wt)[W][NV], float2 carry, float2 dz,
-                                         const float2 (&dwin)[W - 1][NV], int v) {
+// dH of row u: the carry first, then tap k on dz of row u-k (k = 0: dz).
+template <int W, int RS, int NV>
+__device__ __forceinline__ float2 ring_dh(const float2 (&wt)[W][NV], float2 carry, float2 dz,
+                                          const float2 (&dr)[RS][NV], int u, int v) {
     float2 c = __ffma2_rn(wt[0][v], dz, carry);
 #pragma unroll
-    for (int k = 1; k < W; ++k) c = __ffma2_rn(wt[k][v], dwin[k - 1][v], c);
+    for (int k = 1; k < W; ++k) c = __ffma2_rn(wt[k][v], dr[slot<RS>(u, k)][v], c);
     return c;
 }
 
-// Move both windows one row on: dwin[0] = dz_i, hw[H-1] = h of row i.
-template <int W, int NV>
-__device__ __forceinline__ void bwd_shift(float2 (&hw)[W - 1][NV], float2 (&dwin)[W - 1][NV], float2 hc, float2 dz,
-                                          int v) {
+// The weight / bias partial sums of row u: dz * h[u-H+k] for k < H, dz * h[u],
+// and dz itself.
+template <int W, int RS, int NV>
+__device__ __forceinline__ void ring_partials(float2 (&g)[W][NV], float2 (&gb)[NV], float2 dz,
+                                              const float2 (&hr)[RS][NV], float2 hc, int u, int v) {
 #pragma unroll
-    for (int k = W - 2; k > 0; --k) dwin[k][v] = dwin[k - 1][v];
-    dwin[0][v] = dz;
-#pragma unroll
-    for (int k = 0; k + 1 < W - 1; ++k) hw[k][v] = hw[k + 1][v];
-    hw[W - 2][v] = hc;
+    for (int k = 0; k < W - 1; ++k) g[k][v] = __ffma2_rn(dz, hr[slot<RS>(u, W - 1 - k)][v], g[k][v]);
+    g[W - 1][v] = __ffma2_rn(dz, hc, g[W - 1][v]);
+    gb[v] = __fadd2_rn(gb[v], dz);
 }
 
 // P = 0: each lane loads its U rows of x and dy straight into registers.
@@ -119,9 +128,11 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
     RunWalker<kBwdChunk> walk;
     walk.init(a.cu, a.N, a.rows, run, a.runs, H, true, lane);
 
-    // Sliding windows, carried from one segment to the next along a walk:
-    // history rows h[i..i+H-1] and dz_{i-1..i-H}.
-    float2 hw[H][NV], dwin[H][NV];
+    // The rings of history values and dz, carried from one segment to the
+    // next along a walk (slot = walk row % RS).
+    constexpr int RS = U;
+    static_assert(RS >= W, "the ring must hold the current row and the W-1 before it");
+    float2 hring[RS][NV], dring[RS][NV];
     bool live = true, read_state = false;
 
     // Ring state (P > 0): batch b of the current walk holds rows
@@ -225,12 +236,13 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
                         hr[p] = ld_ro<NV>(a.hist + (static_cast<int64_t>(t.n) * H + p) * a.C + c0);
                 }
             }
+            // history row p (oldest first) is walk row p - H: slot RS - H + p
 #pragma unroll
-            for (int p = 0; p < H; ++p) unpack<NV>(hr[p], hw[p]);
+            for (int p = 0; p < H; ++p) unpack<NV>(hr[p], hring[slot<RS>(0, H - p)]);
 #pragma unroll
-            for (int p = 0; p < H; ++p)
+            for (int p = 0; p < RS; ++p)
 #pragma unroll
-                for (int v = 0; v < NV; ++v) dwin[p][v] = f2_zero();
+                for (int v = 0; v < NV; ++v) dring[p][v] = f2_zero();
         }
 
         // i = o0 + k.  Rows k < nr are this segment's; when no segment of the
@@ -306,14 +318,12 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
                     Raw<NV> o;
 #pragma unroll
                     for (int v = 0; v < NV; ++v) {
-                        const float2 dz = bwd_dz<W, ACT, NV>(wt, bb[v], hw, hc[v], gy[v], v);
-#pragma unroll
-                        for (int k = 0; k < H; ++k) g[k][v] = __ffma2_rn(dz, hw[k][v], g[k][v]);
-                        g[H][v] = __ffma2_rn(dz, hc[v], g[H][v]);
-                        gb[v] = __fadd2_rn(gb[v], dz);
+                        const float2 dz = ring_dz<W, ACT, RS, NV>(wt, bb[v], hring, hc[v], gy[v], u, v);
+                        ring_partials<W, RS, NV>(g, gb, dz, hring, hc[v], u, v);
                         // no carry (same op as the general path)
-                        o.u[v] = f2_to_bf2(bwd_dh<W, NV>(wt, f2_zero(), dz, dwin, v));
-                        bwd_shift<W, NV>(hw, dwin, hc[v], dz, v);
+                        o.u[v] = f2_to_bf2(ring_dh<W, RS, NV>(wt, f2_zero(), dz, dring, u, v));
+                        hring[u][v] = hc[v];
+                        dring[u][v] = dz;
                     }
                     st_stream<NV>(dxp, o);
                     dxp += a.dxs;
@@ -332,19 +342,14 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
                     float2 gy[NV];
                     unpack<NV>(gr[u], gy);
 #pragma unroll
-                    for (int v = 0; v < NV; ++v) dz[v] = bwd_dz<W, ACT, NV>(wt, bb[v], hw, hc[v], gy[v], v);
+                    for (int v = 0; v < NV; ++v) dz[v] = ring_dz<W, ACT, RS, NV>(wt, bb[v], hring, hc[v], gy[v], u, v);
                 } else {
 #pragma unroll
                     for (int v = 0; v < NV; ++v) dz[v] = f2_zero();
                 }
                 if (k < nr) {  // this segment's own token: weight / bias partials
 #pragma unroll
-                    for (int v = 0; v < NV; ++v) {
-#pragma unroll
-                        for (int j = 0; j < H; ++j) g[j][v] = __ffma2_rn(dz[v], hw[j][v], g[j][v]);
-                        g[H][v] = __ffma2_rn(dz[v], hc[v], g[H][v]);
-                        gb[v] = __fadd2_rn(gb[v], dz[v]);
-                    }
+                    for (int v = 0; v < NV; ++v) ring_partials<W, RS, NV>(g, gb, dz[v], hring, hc[v], u, v);
                 }
                 // dH[i] is complete now.  i < H: an initial-history gradient.
                 // Otherwise it is dx of row i-H, ours unless this is the first
@@ -360,7 +365,7 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
                     float2 acc[NV];
 #pragma unroll
                     for (int v = 0; v < NV; ++v)
-                        acc[v] = bwd_dh<W, NV>(wt, (carry && act) ? __ldg(cp + v) : f2_zero(), dz[v], dwin, v);
+                        acc[v] = ring_dh<W, RS, NV>(wt, (carry && act) ? __ldg(cp + v) : f2_zero(), dz[v], dring, u, v);
                     if (act) {
                         if (emit_dx) {
                             Raw<NV> o;
@@ -375,7 +380,10 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
                     }
                 }
 #pragma unroll
-                for (int v = 0; v < NV; ++v) bwd_shift<W, NV>(hw, dwin, hc[v], dz[v], v);
+                for (int v = 0; v < NV; ++v) {
+                    hring[u][v] = hc[v];
+                    dring[u][v] = dz[v];
+                }
             }
         }
     }

@@ -234,6 +234,12 @@ __device__ __forceinline__ float2 conv_pre(const float2 (&wt)[W][NV], float2 b, 
     return __ffma2_rn(wt[W - 1][v], hc, z);
 }
 
+// Slot of the row `back` rows before row u in an RS-slot ring of rows (row
+// k of a walk in slot k % RS); u and back are compile-time constants at every
+// use, so the ring never costs a register move.
+template <int RS>
+__device__ __forceinline__ constexpr int slot(int u, int back) { return (u - back + 2 * RS) % RS; }
+
 // Output of the activation: SiLU z * sigmoid(z), or z itself.
 template <bool ACT>
 __device__ __forceinline__ float2 activate2(float2 z) {
