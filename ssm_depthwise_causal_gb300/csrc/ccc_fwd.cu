@@ -94,26 +94,6 @@ __device__ __forceinline__ Raw<NV> fwd_row(const float2 (&wt)[W][NV], const floa
     return y;
 }
 
-// The same row with the history in an RS-slot ring (row k of a walk in slot
-// k % RS; u = this row's slot): no register moves between rows.
-template <int W, bool ACT, int RS, int NV>
-__device__ __forceinline__ Raw<NV> fwd_row_ring(const float2 (&wt)[W][NV], const float2 (&bb)[NV],
-                                                float2 (&hr)[RS][NV], const Raw<NV> &xr, int u) {
-    float2 hc[NV];
-    unpack<NV>(xr, hc);
-    Raw<NV> y;
-#pragma unroll
-    for (int v = 0; v < NV; ++v) {
-        float2 z = bb[v];
-#pragma unroll
-        for (int k = 0; k < W - 1; ++k) z = __ffma2_rn(wt[k][v], hr[slot<RS>(u, W - 1 - k)][v], z);
-        z = __ffma2_rn(wt[W - 1][v], hc[v], z);
-        y.u[v] = f2_to_bf2(activate2<ACT>(z));
-        hr[u][v] = hc[v];
-    }
-    return y;
-}
-
 template <int VEC, int U, int W, bool ACT>
 __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const FwdArgs a) {
     constexpr int NV = VEC / 2;
@@ -133,13 +113,10 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
     RunWalker<kFwdChunk> walk;
     walk.init(a.cu, a.N, a.rows, run, a.runs, H, false, lane);
 
-    // The H rows before the current one: a shifting window (oldest first), or
-    // with kFwdRingWin a U-slot ring indexed by walk row (batches start at
-    // multiples of U from a walk's first row: segments are whole batches).
-    constexpr bool RW = kFwdRingWin && U >= W && kFwdChunk % U == 0;
-    constexpr int RS = RW ? U : 1;
+    // The H rows before the current one, oldest first.  (With 3-row batches
+    // the window comes back to the same registers every batch; a ring
+    // indexed by walk row, as in the backward, measured no faster here.)
     float2 hw[H][NV];
-    float2 hring[RS][NV];
 
     Item t;
     bool cont, more;
@@ -186,13 +163,8 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
 #pragma unroll
                 for (int p = 0; p < H; ++p) hr[p] = ld_ro<NV>(xrow - static_cast<int64_t>(H - p) * a.xs);
             }
-            if constexpr (RW) {
 #pragma unroll
-                for (int p = 0; p < H; ++p) unpack<NV>(hr[p], hring[slot<RS>(0, H - p)]);
-            } else {
-#pragma unroll
-                for (int p = 0; p < H; ++p) unpack<NV>(hr[p], hw[p]);
-            }
+            for (int p = 0; p < H; ++p) unpack<NV>(hr[p], hw[p]);
         }
 
         int base = 0;
@@ -216,11 +188,7 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
                 }
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    if constexpr (RW) {
-                        st_stream<NV>(op, fwd_row_ring<W, ACT, RS, NV>(wt, bb, hring, cur[u], u));
-                    } else {
-                        st_stream<NV>(op, fwd_row<W, ACT, NV>(wt, bb, hw, cur[u]));
-                    }
+                    st_stream<NV>(op, fwd_row<W, ACT, NV>(wt, bb, hw, cur[u]));
                     op += a.os;
                 }
                 xp = lp;
@@ -235,12 +203,7 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 if (base + u >= nr) break;
-                Raw<NV> y;
-                if constexpr (RW) {
-                    y = fwd_row_ring<W, ACT, RS, NV>(wt, bb, hring, cur[u], u);
-                } else {
-                    y = fwd_row<W, ACT, NV>(wt, bb, hw, cur[u]);
-                }
+                const Raw<NV> y = fwd_row<W, ACT, NV>(wt, bb, hw, cur[u]);
                 if (act) st_stream<NV>(orow + static_cast<int64_t>(base + u) * a.os, y);
             }
         }

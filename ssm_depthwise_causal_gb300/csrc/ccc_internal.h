@@ -28,9 +28,7 @@ namespace ccc {
 #ifndef CCC_FWD_UNROLL_W4
 #define CCC_FWD_UNROLL_W4 3
 #endif
-#ifndef CCC_FWD_RINGWIN
-#define CCC_FWD_RINGWIN 0
-#endif
+
 #ifndef CCC_BWD_UNROLL
 #define CCC_BWD_UNROLL 4
 #endif
@@ -73,9 +71,7 @@ constexpr int kBwdVec = CCC_BWD_VEC;
 // back to the same registers every batch (no register shuffling).
 constexpr int kFwdUnroll = CCC_FWD_UNROLL;
 constexpr int kFwdUnrollW4 = CCC_FWD_UNROLL_W4;
-// Forward history as a ring indexed by walk row instead of a shifting window
-// (needs batches of at least W rows).
-constexpr bool kFwdRingWin = CCC_FWD_RINGWIN != 0;
+
 constexpr int kBwdUnroll = CCC_BWD_UNROLL;
 // Resident CTAs per SM the register budget is sized for.
 constexpr int kFwdMinBlocks = CCC_FWD_MIN_BLOCKS;
