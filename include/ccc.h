@@ -17,9 +17,10 @@
  *
  * (tap 3 multiplies the current token; the bias is added before the four
  * FMAs, which run in the order k = 0, 1, 2, 3).  cache_indices[n] == -1
- * produces a zero output and no state access.  Each nonempty live sequence
- * writes its final three raw history values to its slot's positions 0:3
- * (position 0 = oldest); nothing else in the pool changes.  Rows after
+ * produces a zero output and no state access.  A live sequence with at
+ * least one token leaves the last three inputs of its history (unactivated)
+ * in its slot at positions 0, 1, 2, oldest first; nothing else in the pool
+ * changes.  Rows after
  * cu_seqlens[N] are never written.
  *
  * The backward (FlashInfer "cake_causal_conv1d_train.cake_causal_conv1d_kcp",
@@ -67,7 +68,7 @@ extern "C" {
 typedef enum { CCC_F32 = 0, CCC_BF16 = 1, CCC_NONE = -1 } ccc_dtype;
 
 /* Activation after the convolution (Megatron-Core "core.ssm.causal_conv1d",
- * causal_conv1d_cp: optional activation passed to causal_conv1d_fn). */
+ * causal_conv1d_cp: the caller may ask for an activation or none). */
 typedef enum { CCC_ACT_NONE = 0, CCC_ACT_SILU = 1 } ccc_activation;
 
 typedef enum {
@@ -215,9 +216,9 @@ int ccc_bwd_noalloc(const void *x, int64_t rows, int32_t C, int64_t x_row_stride
                     void *cuda_stream);
 
 /*
- * Speculative / single-token decode step (causal_conv1d_fn, Notes: "after
- * prefill, the first speculative update uses accepted count 1"; the pages
- * define nothing more, so the rule below is this library's reading of it).
+ * Speculative / single-token decode step (causal_conv1d_fn, Notes: the
+ * speculative step that follows a prefill takes an accepted count of 1; the
+ * pages define nothing more, so the rule below is this library's reading).
  *
  * Sequence n feeds len = cu_seqlens[n+1] - cu_seqlens[n] new tokens (1 for a
  * plain decode step, the draft tokens for a speculative one).  With

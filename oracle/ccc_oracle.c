@@ -41,8 +41,8 @@
  *   k = 0, 1, ..., W-1); the same order in the GPU kernels makes a sequence
  *   split into fragments reproduce the unsplit result.
  *
- *   Speculative state update (causal_conv1d_fn, Notes: after a prefill the
- *   first speculative update uses accepted count 1).  Each step feeds
+ *   Speculative state update (causal_conv1d_fn, Notes: the speculative
+ *   step right after a prefill is given an accepted count of one).  Each step feeds
  *   len >= 1 draft tokens per sequence; a = accepted[n] >= 1 says how many
  *   tokens of the previous step were kept.  Reading: the slot keeps a run of
  *   raw history values in time order, and the previous step left its

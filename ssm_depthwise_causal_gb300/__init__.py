@@ -234,7 +234,8 @@ def causal_conv1d_fn(x, weight, conv_state=None, cu_seqlens=None, cache_indices=
                      has_initial_state=None, *, bias=None, activation="silu", out=None,
                      workspace=None, saved_hist=None, stream=None) -> torch.Tensor:
     """Allocating forward: ``out`` and the workspace are created when omitted
-    (unused trailing rows of an allocated ``out`` are unspecified).  ``x`` is
+    (rows past cu_seqlens[-1] of an ``out`` made here hold whatever the
+    allocator left).  ``x`` is
     packed ``[rows, C]`` with ``cu_seqlens``, or ``[B, T, D]``."""
     x2, cu, unpack = _packed(x, cu_seqlens)
     rows, C = x2.shape

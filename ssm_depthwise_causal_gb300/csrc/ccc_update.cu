@@ -2,8 +2,8 @@
 // depthwise Conv1d (+ SiLU) of a few new tokens per sequence from the
 // history held in the conv_state pool, and the pool update for the next step.
 //
-// FlashInfer "flashinfer.mamba.causal_conv1d_fn" (Notes): after a prefill,
-// the first speculative update uses accepted count 1.  Reading of that rule
+// FlashInfer "flashinfer.mamba.causal_conv1d_fn" (Notes): the speculative step
+// right after a prefill is given an accepted count of one.  Reading of that rule
 // (the pages give no more): slot q keeps raw history values in time order;
 // the previous step left value h[p + 1] of its own history at position p.
 // For sequence n with a = num_accepted[n] (1 if none given) and len new

@@ -1,8 +1,8 @@
 """The speculative / single-token decode step (ccc_update) against the
 float64 oracle, through the C ABI.
 
-Reading under test (FlashInfer causal_conv1d_fn, Notes: after a prefill the
-first speculative update uses accepted count 1): the step reads the W-1
+Reading under test (FlashInfer causal_conv1d_fn, Notes: the speculative step
+right after a prefill is given an accepted count of one): the step reads the W-1
 values at positions a-1 .. of the slot and leaves history value h[p+1] at
 position p for p < len + W-2.  The oracle's pins tie that rule to torch
 conv1d over the kept token stream; here the GPU follows the oracle step by
