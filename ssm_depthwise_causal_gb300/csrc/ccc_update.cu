@@ -19,27 +19,30 @@
 // this rule expects for a = 1.  A -1 slot gives zero output and no state
 // access; an empty sequence leaves its slot alone.
 //
-// Mapping.  A CTA owns one 32*VEC-channel slab and a contiguous group of
-// sequences; its 8 warps take the group's sequences in turn (warp w: the
-// group's w-th, (w+8)-th, ... sequence).  The slab's taps and bias are staged
-// once per CTA in shared memory (coalesced global reads).  For each of its
-// sequences a warp reads the window, walks the new tokens U at a time and
-// writes the slot.  Reads of the slot precede every write to it in the
-// warp's program order, and no other warp touches the slot's channels (live
-// slots are unique; slabs are disjoint), so the in-place update needs no
-// synchronisation beyond the warp.
+// Two kernels.  For a dense history-contiguous pool ([slots][C][L] with
+// L <= 8: the common serving layout) `update_block_kernel` gives every
+// (sequence, 256-channel slab) pair its own warp: lane l holds the 8 channels
+// c0 .. c0+7 of the slot, whose 8 L values are consecutive in memory
+// (16 L bytes, 16-byte aligned), in L vector registers.  Picking position p
+// of a channel pair, and rebuilding the block after the step, are byte
+// permutes with compile-time selectors, so the block never goes through
+// shared memory.  A warp's only dependent round trips are the sequence's
+// offsets / slot / accepted count, then the block and its new tokens; the
+// grid holds every pair at once, so those trips overlap across warps instead
+// of queueing inside one.  The block is written back (every position; the
+// ones not rewritten keep their bits) before the outputs are computed, which
+// frees its registers for the arithmetic.
 //
-// For a dense history-contiguous pool ([slots][C][L], L <= kUpdStageL) the
-// warp moves the slot's whole [256 ch][L] block: cp.async lands it (and the
-// first U new tokens) in shared memory with coalesced 16-byte copies, the
-// warp transposes it into a position-major [L][256] copy where every
-// position of a lane's 8 channels is one conflict-free 16-byte vector, and
-// writes the block back the same way (positions not written keep their
-// bits).  The copies for a warp's next sequence are issued as soon as the
-// current one has been transposed, and the offsets, slot and accepted count
-// are loaded two sequences ahead, so a warp's memory round trips overlap its
-// arithmetic.  A channel-contiguous pool is read and written one 16-byte
-// vector per lane and position; any other layout element by element.
+// Any other layout takes `update_kernel`: a CTA per (slab, group of
+// sequences), its 8 warps taking the group's sequences in turn, reading and
+// writing the W-1 positions it needs -- one 16-byte vector per lane and
+// position for a channel-contiguous pool, single elements otherwise.
+//
+// In both kernels the slab's taps and bias are staged once per CTA in shared
+// memory (coalesced global reads).  Reads of a slot precede every write to
+// it in the lane's program order, and no other lane touches the same
+// elements (live slots are unique, lanes' channels disjoint), so the in-place
+// update needs no synchronisation.
 #include "ccc_device.cuh"
 #include "ccc_internal.h"
 
@@ -55,13 +58,20 @@ constexpr int kUpdVec = 8;
 #define CCC_UPD_CTAS_PER_SM 4
 #endif
 constexpr int kUpdUnroll = CCC_UPD_UNROLL;
-// CTAs the sequence groups are sized for, per SM (more groups: more CTAs,
-// fewer requests per warp).
+// CTAs the sequence groups of update_kernel are sized for, per SM (more
+// groups: more CTAs, fewer requests per warp).
 constexpr int kUpdCtasPerSm = CCC_UPD_CTAS_PER_SM;
-constexpr int kUpdStageL = 8;  // longest history the shared-memory path stages
+#ifdef CCC_UPD_BLOCK_MIN_BLOCKS
+constexpr int upd_block_min_blocks(int) { return CCC_UPD_BLOCK_MIN_BLOCKS; }
+#else
+// Resident CTAs per SM update_block_kernel is compiled for: the register cap
+// under which a lane's block (4 LS words) and its new tokens stay unspilled.
+constexpr int upd_block_min_blocks(int ls) { return ls <= 4 ? 4 : (ls <= 6 ? 3 : 2); }
+#endif
+constexpr int kUpdBlockMaxL = 8;  // longest history update_block_kernel keeps in registers
 constexpr int kUpdSlab = 32 * kUpdVec;
 
-// Element (slot q, channels c0.., position p) for the unstaged layouts.
+// Element (slot q, channels c0.., position p) of any pool layout.
 template <int NV>
 __device__ __forceinline__ Raw<NV> state_get(const UpdArgs &a, int q, int p, int c0) {
     const uint16_t *base = a.state + static_cast<int64_t>(q) * a.st_slot + static_cast<int64_t>(p) * a.st_l;
@@ -109,56 +119,73 @@ __device__ __forceinline__ Req load_req(const UpdArgs &a, int n, int n_end) {
     return r;
 }
 
-// The request's slot block is staged (dense pool, live slot, new tokens).
-__device__ __forceinline__ bool req_staged(const UpdArgs &a, const Req &r) {
-    return r.n >= 0 && r.e > r.s && r.q >= 0 && r.q < a.n_slots;
+// The slab's taps 0..W-1 and bias as FP32, one channel per thread of the
+// CTA, read from global memory (load) and then stored to shared memory
+// (store, after the caller has issued its own loads).
+template <int W>
+struct TapStage {
+    float t[W + 1];
+    __device__ __forceinline__ void load(const UpdArgs &a, int slab) {
+        const int c = slab * kUpdSlab + static_cast<int>(threadIdx.x);
+        const bool ok = c < a.C;
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+            float v = 0.0f;
+            if (ok) {
+                v = a.w_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(a.w)[W * c + k])
+                             : __ldg(reinterpret_cast<const float *>(a.w) + W * c + k);
+            }
+            t[k] = v;
+        }
+        float bv = 0.0f;
+        if (ok && a.b_kind == 1) bv = __ldg(reinterpret_cast<const float *>(a.b) + c);
+        if (ok && a.b_kind == 2) bv = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(a.b)[c]);
+        t[W] = bv;
+    }
+    __device__ __forceinline__ void store(float (&s_tap)[W + 1][kUpdSlab]) const {
+#pragma unroll
+        for (int k = 0; k <= W; ++k) s_tap[k][threadIdx.x] = t[k];
+    }
+};
+
+// One new token of a lane's 8 channels: y from the history hw (oldest
+// first) and the token xr, then hw shifts by one.
+template <int W, bool ACT, int NV>
+__device__ __forceinline__ Raw<NV> update_token(const float2 (&wt)[W][NV], const float2 (&bb)[NV],
+                                                float2 (&hw)[W - 1][NV], const Raw<NV> &xr) {
+    constexpr int H = W - 1;
+    float2 hc[NV];
+    unpack<NV>(xr, hc);
+    Raw<NV> y;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        y.u[v] = f2_to_bf2(activate2<ACT>(conv_pre<W, NV>(wt, bb[v], hw, hc[v], v)));
+#pragma unroll
+        for (int k = 0; k + 1 < H; ++k) hw[k][v] = hw[k + 1][v];
+        hw[H - 1][v] = hc[v];
+    }
+    return y;
 }
 
-// LS > 0: the pool is dense history-contiguous with L = LS (a compile-time
-// constant, so the block transposition below is straight-line code); LS = 0:
-// any other layout, L from the arguments.
-template <int W, bool ACT, int LS>
+// Any pool layout: a CTA per (slab, group of sequences), each warp looping
+// over its sequences (the group's w-th, (w+8)-th, ...).
+template <int W, bool ACT>
 __global__ void __launch_bounds__(kCtaThreads, kUpdMinBlocks) update_kernel(const UpdArgs a) {
     constexpr int VEC = kUpdVec, NV = VEC / 2, U = kUpdUnroll;
     constexpr int H = W - 1;
-    constexpr int SLAB = kUpdSlab;
-    constexpr bool kStaged = LS > 0;
-    constexpr int LB = kStaged ? LS : 1;
-    static_assert(LS == 0 || (LS >= H && LS <= kUpdStageL), "staged history length");
-    __shared__ __align__(16) float s_tap[W + 1][SLAB];  // taps 0..W-1 and the bias
-    // Dynamic shared memory (staged layout only), per warp: the landing copy
-    // of a slot block (channel-major), the working copy (position-major) and
-    // the first U new tokens.
-    extern __shared__ __align__(16) uint16_t upd_dyn[];
+    __shared__ __align__(16) float s_tap[W + 1][kUpdSlab];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int slab = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.slabs));
     const int grp = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.slabs));
     const int n_beg = static_cast<int>(static_cast<int64_t>(grp) * a.N / a.groups);
     const int n_end = static_cast<int>(static_cast<int64_t>(grp + 1) * a.N / a.groups);
 
-    // Requests in flight: the current one and the next two (loads issued
-    // before the taps' barrier).
     int n = n_beg + warp;
     Req cur = load_req(a, n, n_end);
-    Req nx1 = load_req(a, n + kWarpsPerCta, n_end);
-
-    // The slab's taps and bias, one channel per thread (FP32 in shared memory).
     {
-        const int c = slab * SLAB + static_cast<int>(threadIdx.x);
-        const bool ok = c < a.C;
-#pragma unroll
-        for (int k = 0; k < W; ++k) {
-            float t = 0.0f;
-            if (ok) {
-                t = a.w_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(a.w)[W * c + k])
-                             : __ldg(reinterpret_cast<const float *>(a.w) + W * c + k);
-            }
-            s_tap[k][threadIdx.x] = t;
-        }
-        float bv = 0.0f;
-        if (ok && a.b_kind == 1) bv = __ldg(reinterpret_cast<const float *>(a.b) + c);
-        if (ok && a.b_kind == 2) bv = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(a.b)[c]);
-        s_tap[W][threadIdx.x] = bv;
+        TapStage<W> ts;
+        ts.load(a, slab);
+        ts.store(s_tap);
     }
     __syncthreads();
     if (cur.n < 0) return;  // whole warp, after the CTA barrier
@@ -166,226 +193,269 @@ __global__ void __launch_bounds__(kCtaThreads, kUpdMinBlocks) update_kernel(cons
     const int cv = slab * 32 + lane;
     const bool act = cv < a.C / VEC;
     const int c0 = act ? cv * VEC : 0;
-    const int slab_ch = min(SLAB, a.C - slab * SLAB);
-    const int blk_vecs = kStaged ? slab_ch * LS / 8 : 0;  // 16-byte vectors in a slot's block
-    uint16_t *raw = upd_dyn + warp * (2 * LB + U) * SLAB;
-    uint16_t *blk = raw + LB * SLAB;
-    uint16_t *sx = blk + LB * SLAB;
-    const uint32_t raw_sa = smem_addr(raw), sx_sa = smem_addr(sx);
-
-    // cp.async of request r's block and first U new tokens (staged layout).
-    auto issue = [&](const Req &r) {
-        if constexpr (kStaged) {
-            if (req_staged(a, r)) {
-                const uint16_t *g = a.state + static_cast<int64_t>(r.q) * a.st_slot + static_cast<int64_t>(slab) * SLAB * LS;
+    float2 wt[W][NV], bb[NV];
 #pragma unroll
-                for (int k = 0; k < LS; ++k) {
-                    const int i = lane + 32 * k;
-                    if (i < blk_vecs) cp_async<16>(raw_sa + 16 * i, g + 8 * i, true);
-                }
+    for (int v = 0; v < NV; ++v) {
 #pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const bool ok = act && r.s + u < r.e;
-                    cp_async<16>(sx_sa + 2 * (u * SLAB + lane * VEC),
-                                 ok ? a.x + static_cast<int64_t>(r.s + u) * a.xs + c0 : a.x, ok);
-                }
-            }
-            cp_async_commit();
-        }
-    };
-    issue(cur);
+        for (int k = 0; k < W; ++k) wt[k][v] = reinterpret_cast<const float2 *>(&s_tap[k][lane * VEC])[v];
+        bb[v] = reinterpret_cast<const float2 *>(&s_tap[W][lane * VEC])[v];
+    }
 
     while (true) {
-        const Req nx2 = load_req(a, n + 2 * kWarpsPerCta, n_end);  // used two iterations on
+        const Req nx = load_req(a, n + kWarpsPerCta, n_end);  // one sequence ahead
         const int len = cur.e - cur.s;
         const int q = cur.q;
         const uint16_t *xrow = a.x + static_cast<int64_t>(cur.s) * a.xs + c0;
         uint16_t *orow = a.out + static_cast<int64_t>(cur.s) * a.os + c0;
         const bool pool = len > 0 && q >= 0 && q < a.n_slots;
-        const bool staged = kStaged && pool;
         const int acc = min(max(cur.acc, 1), a.L - H + 1);
         const int n_write = min(len + H - 1, a.L);  // positions written
-
-        Raw<NV> xr0[U];  // the first U new tokens
-        Raw<NV> hr[H];   // the W-1 values before them
-#pragma unroll
-        for (int p = 0; p < H; ++p) hr[p] = raw_zero<NV>();
-        if constexpr (kStaged) {
-            cp_async_wait(0);
-            __syncwarp();
-            if (staged) {
-                // channel-major raw -> position-major blk.  Vector i + 32 k of
-                // the block starts at element 8 i + 256 k; with L known at
-                // compile time every (channel, position) is a constant plus
-                // the lane's own start.
-                const int ch_l = (8 * lane) / LS, p_l = (8 * lane) % LS;
-#pragma unroll
-                for (int k = 0; k < LS; ++k) {
-                    const int i = lane + 32 * k;
-                    if (i < blk_vecs) {
-                        const uint4 v = *reinterpret_cast<const uint4 *>(raw + 8 * i);
-                        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                        for (int t = 0; t < 8; ++t) {
-                            const int d = 256 * k + t;
-                            const int pp = p_l + d % LS, cc = ch_l + d / LS;
-                            const int p = pp >= LS ? pp - LS : pp, ch = pp >= LS ? cc + 1 : cc;
-                            blk[p * SLAB + ch] = static_cast<uint16_t>(t & 1 ? w4[t >> 1] >> 16 : w4[t >> 1] & 0xffffu);
-                        }
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < U; ++u) xr0[u] = ld_rw<NV>(sx + u * SLAB + lane * VEC);
-            } else {
-#pragma unroll
-                for (int u = 0; u < U; ++u)
-                    xr0[u] = (act && q != -1 && u < len) ? ld_ro<NV>(xrow + static_cast<int64_t>(u) * a.xs)
-                                                         : raw_zero<NV>();
-            }
-            __syncwarp();  // the landing buffers are free: start the next request's copies
-            issue(nx1);
-            if (staged && act)
-#pragma unroll
-                for (int p = 0; p < H; ++p) hr[p] = ld_rw<NV>(blk + (acc - 1 + p) * SLAB + lane * VEC);
-        } else {
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                xr0[u] = (act && q != -1 && u < len) ? ld_ro<NV>(xrow + static_cast<int64_t>(u) * a.xs)
-                                                     : raw_zero<NV>();
-            if (pool && act)
-#pragma unroll
-                for (int p = 0; p < H; ++p) hr[p] = state_get<NV>(a, q, acc - 1 + p, c0);
-        }
 
         if (len > 0 && q == -1) {  // padded request: zero output, no state access
             if (act) {
                 const Raw<NV> z = raw_zero<NV>();
                 for (int r = 0; r < len; ++r) st_stream<NV>(orow + static_cast<int64_t>(r) * a.os, z);
             }
-        } else if (len > 0) {
+        } else if (len > 0 && act) {
+            Raw<NV> hr[H];  // the W-1 values before the first new token
+#pragma unroll
+            for (int p = 0; p < H; ++p) hr[p] = pool ? state_get<NV>(a, q, acc - 1 + p, c0) : raw_zero<NV>();
             // Positions 0 .. W-3: the 2nd .. last value just read.
-            if (pool && act) {
+            if (pool) {
 #pragma unroll
-                for (int p = 0; p + 1 < H; ++p) {
-                    if (p < n_write) {
-                        if (staged) {
-                            st_plain<NV>(blk + p * SLAB + lane * VEC, hr[p + 1]);
-                        } else {
-                            state_put<NV>(a, q, p, c0, hr[p + 1]);
-                        }
-                    }
-                }
-            }
-            float2 wt[W][NV], bb[NV];
-#pragma unroll
-            for (int v = 0; v < NV; ++v) {
-#pragma unroll
-                for (int k = 0; k < W; ++k) wt[k][v] = reinterpret_cast<const float2 *>(&s_tap[k][lane * VEC])[v];
-                bb[v] = reinterpret_cast<const float2 *>(&s_tap[W][lane * VEC])[v];
+                for (int p = 0; p + 1 < H; ++p)
+                    if (p < n_write) state_put<NV>(a, q, p, c0, hr[p + 1]);
             }
             float2 hw[H][NV];
 #pragma unroll
             for (int p = 0; p < H; ++p) unpack<NV>(hr[p], hw[p]);
             for (int base = 0; base < len; base += U) {
                 Raw<NV> xr[U];
-                if (base == 0) {
 #pragma unroll
-                    for (int u = 0; u < U; ++u) xr[u] = xr0[u];
-                } else {
-#pragma unroll
-                    for (int u = 0; u < U; ++u)
-                        xr[u] = (act && base + u < len) ? ld_ro<NV>(xrow + static_cast<int64_t>(base + u) * a.xs)
-                                                        : raw_zero<NV>();
-                }
+                for (int u = 0; u < U; ++u)
+                    xr[u] = base + u < len ? ld_ro<NV>(xrow + static_cast<int64_t>(base + u) * a.xs) : raw_zero<NV>();
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int j = base + u;
                     if (j >= len) break;
-                    float2 hc[NV];
-                    unpack<NV>(xr[u], hc);
-                    Raw<NV> y;
-#pragma unroll
-                    for (int v = 0; v < NV; ++v) {
-                        y.u[v] = f2_to_bf2(activate2<ACT>(conv_pre<W, NV>(wt, bb[v], hw, hc[v], v)));
-#pragma unroll
-                        for (int k = 0; k + 1 < H; ++k) hw[k][v] = hw[k + 1][v];
-                        hw[H - 1][v] = hc[v];
-                    }
-                    if (act) {
-                        st_stream<NV>(orow + static_cast<int64_t>(j) * a.os, y);
-                        // token j is history value H + j: position H - 1 + j
-                        const int p = H - 1 + j;
-                        if (pool && p < n_write) {
-                            if (staged) {
-                                st_plain<NV>(blk + p * SLAB + lane * VEC, xr[u]);
-                            } else {
-                                state_put<NV>(a, q, p, c0, xr[u]);
-                            }
-                        }
-                    }
-                }
-            }
-            if constexpr (kStaged) {
-                if (staged) {
-                    // position-major blk -> channel-major global block, whole
-                    // (positions not written keep the bits they were read with)
-                    __syncwarp();
-                    uint16_t *g = a.state + static_cast<int64_t>(q) * a.st_slot + static_cast<int64_t>(slab) * SLAB * LS;
-                    const int ch_l = (8 * lane) / LS, p_l = (8 * lane) % LS;
-#pragma unroll
-                    for (int k = 0; k < LS; ++k) {
-                        const int i = lane + 32 * k;
-                        if (i < blk_vecs) {
-                            uint32_t w4[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-                            for (int t = 0; t < 8; ++t) {
-                                const int d = 256 * k + t;
-                                const int pp = p_l + d % LS, cc = ch_l + d / LS;
-                                const int p = pp >= LS ? pp - LS : pp, ch = pp >= LS ? cc + 1 : cc;
-                                const uint32_t h = blk[p * SLAB + ch];
-                                w4[t >> 1] |= t & 1 ? h << 16 : h;
-                            }
-                            reinterpret_cast<uint4 *>(g)[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                        }
-                    }
+                    st_stream<NV>(orow + static_cast<int64_t>(j) * a.os, update_token<W, ACT, NV>(wt, bb, hw, xr[u]));
+                    // token j is history value H + j: position H - 1 + j
+                    if (pool && H - 1 + j < n_write) state_put<NV>(a, q, H - 1 + j, c0, xr[u]);
                 }
             }
         }
-        __syncwarp();  // blk is rewritten by the next request's transposition
         n += kWarpsPerCta;
-        if (nx1.n < 0) break;
-        cur = nx1;
-        nx1 = nx2;
+        if (nx.n < 0) break;
+        cur = nx;
+    }
+}
+
+// Pre-activation of the lane's channel pair v for one token: taps and bias
+// from the CTA's shared copy, history hv (oldest first), token xc -- the
+// same FMA order as every other kernel (conv_pre).
+template <int W>
+__device__ __forceinline__ float2 pair_pre(const float (&s_tap)[W + 1][kUpdSlab], int lane, int v,
+                                          const float2 (&hv)[W - 1], float2 xc) {
+    float2 wv[W][1], h1[W - 1][1];
+#pragma unroll
+    for (int k = 0; k < W; ++k) wv[k][0] = reinterpret_cast<const float2 *>(&s_tap[k][lane * kUpdVec])[v];
+#pragma unroll
+    for (int k = 0; k + 1 < W; ++k) h1[k][0] = hv[k];
+    const float2 b = reinterpret_cast<const float2 *>(&s_tap[W][lane * kUpdVec])[v];
+    return conv_pre<W, 1>(wv, b, h1, xc, 0);
+}
+
+// Pair word (channels 2v, 2v+1 of the lane at position p) of a lane's
+// channel-major block: element ch * LS + p is half (ch * LS + p) & 1 of word
+// (ch * LS + p) >> 1.  p and v are compile-time constants at every use.
+template <int LS>
+__device__ __forceinline__ uint32_t block_pair(const uint32_t (&u)[4 * LS], int p, int v) {
+    const int e0 = 2 * v * LS + p, e1 = (2 * v + 1) * LS + p;
+    const unsigned sel = ((e0 & 1) ? 0x32u : 0x10u) | (((e1 & 1) ? 0x76u : 0x54u) << 8);
+    return __byte_perm(u[e0 >> 1], u[e1 >> 1], sel);
+}
+
+// Dense history-contiguous pool with L = LS <= 8: a warp per (sequence,
+// slab), lane l owning channels c0 .. c0+7 and their whole 16*LS-byte block.
+template <int W, bool ACT, int LS>
+__global__ void __launch_bounds__(kCtaThreads, upd_block_min_blocks(LS)) update_block_kernel(const UpdArgs a) {
+    constexpr int VEC = kUpdVec, NV = VEC / 2;
+    constexpr int H = W - 1;
+    constexpr int T0 = LS - H + 1;  // new tokens a slot keeps raw: positions H-1 .. LS-1
+    constexpr int NW = 4 * LS;      // 32-bit words of a lane's block
+    static_assert(LS >= H && LS <= kUpdBlockMaxL, "history length of the register block");
+    __shared__ __align__(16) float s_tap[W + 1][kUpdSlab];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int slab = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.slabs));
+    const int grp = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.slabs));
+    const Req r = load_req(a, grp * kWarpsPerCta + warp, a.N);
+    TapStage<W> ts;
+    ts.load(a, slab);
+
+    // The block and the first T0 new tokens, loaded before the CTA barrier.
+    const int cv = slab * 32 + lane;
+    const bool act = cv < a.C / VEC;
+    const int c0 = act ? cv * VEC : 0;
+    const int len = r.e - r.s;
+    const int q = r.q;
+    const bool pool = r.n >= 0 && len > 0 && q >= 0 && q < a.n_slots;
+    uint16_t *blk_g = a.state + static_cast<int64_t>(pool ? q : 0) * a.st_slot + static_cast<int64_t>(c0) * LS;
+    uint32_t blk[NW];
+#pragma unroll
+    for (int k = 0; k < LS; ++k) {
+        uint4 t = make_uint4(0u, 0u, 0u, 0u);
+        if (pool && act) t = *reinterpret_cast<const uint4 *>(blk_g + 8 * k);
+        blk[4 * k] = t.x; blk[4 * k + 1] = t.y; blk[4 * k + 2] = t.z; blk[4 * k + 3] = t.w;
+    }
+    const uint16_t *xrow = a.x + static_cast<int64_t>(r.s) * a.xs + c0;
+    Raw<NV> tok[T0];
+#pragma unroll
+    for (int j = 0; j < T0; ++j)
+        tok[j] = (r.n >= 0 && act && q != -1 && j < len) ? ld_ro<NV>(xrow + static_cast<int64_t>(j) * a.xs)
+                                                         : raw_zero<NV>();
+    ts.store(s_tap);
+    __syncthreads();
+    if (r.n < 0 || len <= 0 || !act) return;
+    uint16_t *orow = a.out + static_cast<int64_t>(r.s) * a.os + c0;
+    if (q == -1) {  // padded request: zero output, no state access
+        const Raw<NV> z = raw_zero<NV>();
+        for (int j = 0; j < len; ++j) st_stream<NV>(orow + static_cast<int64_t>(j) * a.os, z);
+        return;
+    }
+
+    // The W-1 values before the first new token: positions acc-1 .. acc+H-2.
+    // Without accepted counts acc = 1; otherwise they are picked by selects
+    // over the T0 possible offsets (the empty asm hides each candidate's
+    // origin, so the compiler cannot fold the selects into a run-time index
+    // of the block, which would put the block in local memory).
+    Raw<NV> hr[H];
+#pragma unroll
+    for (int i = 0; i < H; ++i)
+#pragma unroll
+        for (int v = 0; v < NV; ++v) hr[i].u[v] = block_pair<LS>(blk, i, v);
+    if (T0 > 1 && a.accepted) {
+        const int acc = min(max(r.acc, 1), T0);
+#pragma unroll
+        for (int a0 = 1; a0 < T0; ++a0) {
+#pragma unroll
+            for (int i = 0; i < H; ++i)
+#pragma unroll
+                for (int v = 0; v < NV; ++v) {
+                    uint32_t cand = block_pair<LS>(blk, a0 + i, v);
+                    asm("" : "+r"(cand));
+                    hr[i].u[v] = acc - 1 == a0 ? cand : hr[i].u[v];
+                }
+        }
+    }
+
+    // The new block: position p < n_write gets history value h[p + 1] (the
+    // 2nd .. last value read, then the new tokens); the others keep their
+    // bits.  Word w of the block holds elements 2w, 2w+1 (channel e / LS,
+    // position e % LS): one byte permute gathers both new halves, and a
+    // mask per position keeps the old half where nothing is written.
+    if (pool) {
+        const int n_write = min(len + H - 1, LS);
+        uint32_t keep_lo[LS], keep_hi[LS];
+#pragma unroll
+        for (int p = 0; p < LS; ++p) {
+            keep_lo[p] = p < n_write ? 0u : 0x0000ffffu;
+            keep_hi[p] = p < n_write ? 0u : 0xffff0000u;
+        }
+        uint32_t nb[NW];
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const int e0 = 2 * w, e1 = 2 * w + 1;
+            const int ch0 = e0 / LS, p0 = e0 % LS, ch1 = e1 / LS, p1 = e1 % LS;
+            const uint32_t src0 = p0 < H - 1 ? hr[p0 + 1].u[ch0 >> 1] : tok[p0 - H + 1].u[ch0 >> 1];
+            const uint32_t src1 = p1 < H - 1 ? hr[p1 + 1].u[ch1 >> 1] : tok[p1 - H + 1].u[ch1 >> 1];
+            const unsigned sel = ((ch0 & 1) ? 0x32u : 0x10u) | (((ch1 & 1) ? 0x76u : 0x54u) << 8);
+            const uint32_t fresh = __byte_perm(src0, src1, sel);
+            const uint32_t keep = keep_lo[p0] | keep_hi[p1];
+            nb[w] = (blk[w] & keep) | (fresh & ~keep);
+        }
+#pragma unroll
+        for (int k = 0; k < LS; ++k)
+            *reinterpret_cast<uint4 *>(blk_g + 8 * k) = make_uint4(nb[4 * k], nb[4 * k + 1], nb[4 * k + 2], nb[4 * k + 3]);
+    }
+
+    // The block's registers are dead from here on: keep the taps' shared
+    // loads below its stores.
+    asm volatile("" ::: "memory");
+
+    // The first min(len, T0) tokens (held in registers), channel pair by
+    // channel pair: each pair's taps, history and outputs are its own.
+    Raw<NV> y[T0];
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        float2 hv[H];
+#pragma unroll
+        for (int i = 0; i < H; ++i) hv[i] = bf2_to_f2(hr[i].u[v]);
+#pragma unroll
+        for (int j = 0; j < T0; ++j) {
+            if (j < len) {
+                const float2 xc = bf2_to_f2(tok[j].u[v]);
+                y[j].u[v] = f2_to_bf2(activate2<ACT>(pair_pre<W>(s_tap, lane, v, hv, xc)));
+#pragma unroll
+                for (int i = 0; i + 1 < H; ++i) hv[i] = hv[i + 1];
+                hv[H - 1] = xc;
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < T0; ++j)
+        if (j < len) st_stream<NV>(orow + static_cast<int64_t>(j) * a.os, y[j]);
+
+    // Tokens past what the slot keeps (a step longer than the pool allows):
+    // one at a time, the history kept as raw BF16 values (exact).
+    if (len > T0) {
+        Raw<NV> hraw[H];  // history values T0 .. T0+H-1: the read values, then tokens
+#pragma unroll
+        for (int i = 0; i < H; ++i) hraw[i] = T0 + i < H ? hr[T0 + i] : tok[T0 + i - H];
+        for (int j = T0; j < len; ++j) {
+            const Raw<NV> xr = ld_ro<NV>(xrow + static_cast<int64_t>(j) * a.xs);
+            Raw<NV> yj;
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                float2 hv[H];
+#pragma unroll
+                for (int i = 0; i < H; ++i) hv[i] = bf2_to_f2(hraw[i].u[v]);
+                yj.u[v] = f2_to_bf2(activate2<ACT>(pair_pre<W>(s_tap, lane, v, hv, bf2_to_f2(xr.u[v]))));
+            }
+            st_stream<NV>(orow + static_cast<int64_t>(j) * a.os, yj);
+#pragma unroll
+            for (int i = 0; i + 1 < H; ++i) hraw[i] = hraw[i + 1];
+            hraw[H - 1] = xr;
+        }
     }
 }
 
 using UpdKernel = void (*)(const UpdArgs);
 
-// The instantiation for (W, ACT) and a staged history length ls (0: none).
+// update_block_kernel for (W, ACT) and history length ls (nullptr if none).
 template <int W, bool ACT>
-UpdKernel update_kernel_l(int ls) {
+UpdKernel update_block_kernel_l(int ls) {
     switch (ls) {
-        case 0: return update_kernel<W, ACT, 0>;
-        case 1: if constexpr (W - 1 <= 1) return update_kernel<W, ACT, (W - 1 <= 1 ? 1 : 0)>; else return nullptr;
-        case 2: if constexpr (W - 1 <= 2) return update_kernel<W, ACT, (W - 1 <= 2 ? 2 : 0)>; else return nullptr;
-        case 3: return update_kernel<W, ACT, 3>;
-        case 4: return update_kernel<W, ACT, 4>;
-        case 5: return update_kernel<W, ACT, 5>;
-        case 6: return update_kernel<W, ACT, 6>;
-        case 7: return update_kernel<W, ACT, 7>;
-        case 8: return update_kernel<W, ACT, 8>;
+        case 1: if constexpr (W - 1 <= 1) return update_block_kernel<W, ACT, (W - 1 <= 1 ? 1 : 8)>; else return nullptr;
+        case 2: if constexpr (W - 1 <= 2) return update_block_kernel<W, ACT, (W - 1 <= 2 ? 2 : 8)>; else return nullptr;
+        case 3: return update_block_kernel<W, ACT, 3>;
+        case 4: return update_block_kernel<W, ACT, 4>;
+        case 5: return update_block_kernel<W, ACT, 5>;
+        case 6: return update_block_kernel<W, ACT, 6>;
+        case 7: return update_block_kernel<W, ACT, 7>;
+        case 8: return update_block_kernel<W, ACT, 8>;
         default: return nullptr;
     }
 }
 
+// ls > 0: update_block_kernel with that history length; 0: update_kernel.
 UpdKernel update_kernel_for(int width, int act, int ls) {
     switch (width * 2 + (act ? 1 : 0)) {
-        case 4: return update_kernel_l<2, false>(ls);
-        case 5: return update_kernel_l<2, true>(ls);
-        case 6: return update_kernel_l<3, false>(ls);
-        case 7: return update_kernel_l<3, true>(ls);
-        case 8: return update_kernel_l<4, false>(ls);
-        case 9: return update_kernel_l<4, true>(ls);
+        case 4: return ls ? update_block_kernel_l<2, false>(ls) : update_kernel<2, false>;
+        case 5: return ls ? update_block_kernel_l<2, true>(ls) : update_kernel<2, true>;
+        case 6: return ls ? update_block_kernel_l<3, false>(ls) : update_kernel<3, false>;
+        case 7: return ls ? update_block_kernel_l<3, true>(ls) : update_kernel<3, true>;
+        case 8: return ls ? update_block_kernel_l<4, false>(ls) : update_kernel<4, false>;
+        case 9: return ls ? update_block_kernel_l<4, true>(ls) : update_kernel<4, true>;
         default: return nullptr;
     }
 }
@@ -394,10 +464,10 @@ UpdKernel update_kernel_for(int width, int act, int ls) {
 
 int update_slabs(int C) { return slabs_of(C, kUpdVec); }
 
-int update_stage_max_len() { return kUpdStageL; }
+int update_stage_max_len() { return kUpdBlockMaxL; }
 
-// Sequence groups per slab: enough CTAs for about two per SM, each warp with
-// at least one request.
+// Sequence groups per slab for update_kernel: enough CTAs for about
+// kUpdCtasPerSm per SM, each warp with at least one request.
 int update_groups(int N, int slabs, int sms) {
     const int64_t want = (static_cast<int64_t>(kUpdCtasPerSm) * sms + slabs - 1) / slabs;
     const int64_t most = ceil_div(N, kWarpsPerCta);
@@ -409,26 +479,13 @@ cudaError_t launch_update(const UpdArgs &a, cudaStream_t st) {
     const int ls = a.state_stage ? a.L : 0;
     const UpdKernel kern = update_kernel_for(a.width, a.act, ls);
     if (!kern) return cudaErrorInvalidValue;
-    const size_t dyn = ls > 0 ? static_cast<size_t>(kWarpsPerCta) * (2 * ls + kUpdUnroll) * kUpdSlab * 2 : 0;
-    if (dyn > 0) {
-        // Opt in to this much dynamic shared memory (with the static taps it
-        // can pass the 48 KB default), once per device and instantiation
-        // (width, activation, staged length).
-        static bool attr_set[64][6][kUpdStageL + 1] = {};
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e != cudaSuccess) return e;
-        const int slot = (a.width - 2) * 2 + (a.act ? 1 : 0);
-        if (dev < 0 || dev >= 64 || !attr_set[dev][slot][ls]) {
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(dyn));
-            if (e != cudaSuccess) return e;
-            if (dev >= 0 && dev < 64) attr_set[dev][slot][ls] = true;
-        }
-    }
-    // CTA b: slab b % slabs, sequence group b / slabs.
-    const int64_t ctas = static_cast<int64_t>(a.slabs) * a.groups;
+    // CTA b: slab b % slabs and, for update_block_kernel, sequences
+    // 8 (b / slabs) .. 8 (b / slabs) + 7 (one per warp); for update_kernel,
+    // sequence group b / slabs.
+    const int64_t groups = ls > 0 ? ceil_div(a.N, kWarpsPerCta) : a.groups;
+    const int64_t ctas = static_cast<int64_t>(a.slabs) * groups;
     if (ctas > INT32_MAX) return cudaErrorInvalidValue;
-    kern<<<dim3(static_cast<unsigned>(ctas)), kCtaThreads, dyn, st>>>(a);
+    kern<<<dim3(static_cast<unsigned>(ctas)), kCtaThreads, 0, st>>>(a);
     return cudaGetLastError();
 }
 
