@@ -406,6 +406,10 @@ def run_ours(args, ws, rank, local):
     torch.cuda.synchronize()
     e2e_ms = job_max(e0.elapsed_time(e1) / e2e_steps, dist, dev)
     e2e_val = job_throughput(ws, T, e2e_ms)
+    link = measure_link([(sets[0]["x"], hx), (sets[0]["dy"], hdy)],
+                        [(hout, sets[0]["out"]), (hdx, sets[0]["dx"])], s_in, s_out)
+    link["e2e_copy_gbs"] = (h2d + d2h) / (e2e_ms / 1e3) / 1e9
+    link["frac"] = link["e2e_copy_gbs"] / link["both_gbs"]
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -435,7 +439,8 @@ def run_ours(args, ws, rank, local):
             "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms, "steps": e2e_steps,
                     "how": "pinned host x, dy in and out, dx, dweight, dbias back every step; steps pipelined "
-                           "over two device buffer sets with separate copy-in, compute and copy-out streams"},
+                           "over two device buffer sets with separate copy-in, compute and copy-out streams",
+                    "link": link},
             "gpu_launches": gpu_launches,
             "clocks": clk,
         }
@@ -443,6 +448,31 @@ def run_ours(args, ws, rank, local):
     if dist:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def measure_link(h2d_pairs, d2h_pairs, s_in, s_out, reps=3):
+    """The host link's ceiling on the e2e step's own pinned buffers: the
+    step's input copies alone, its result copies alone, and both at once on
+    separate streams (which the pipelined step overlaps).  GB/s, best of
+    `reps`; pairs are (dst, src)."""
+    def run(pairs_in, pairs_out):
+        best = None
+        nbytes = sum(d.numel() * d.element_size() for d, _ in pairs_in + pairs_out)
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            with torch.cuda.stream(s_in):
+                for d, h in pairs_in:
+                    d.copy_(h, non_blocking=True)
+            with torch.cuda.stream(s_out):
+                for h, d in pairs_out:
+                    h.copy_(d, non_blocking=True)
+            torch.cuda.synchronize()
+            dt = time.perf_counter() - t0
+            best = dt if best is None else min(best, dt)
+        return nbytes / best / 1e9
+    return {"h2d_gbs": run(h2d_pairs, []), "d2h_gbs": run([], d2h_pairs), "both_gbs": run(h2d_pairs, d2h_pairs),
+            "how": "pinned-host copies of the step's x, dy in and out, dx back, on separate copy streams"}
 
 
 UPDATE_METRIC = "decode-step tokens/s and effective HBM GB/s of ccc_update (serving pool, C=8192)"

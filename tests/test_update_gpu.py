@@ -6,9 +6,9 @@ right after a prefill is given an accepted count of one): the step reads the W-1
 values at positions a-1 .. of the slot and leaves history value h[p+1] at
 position p for p < len + W-2.  The oracle's pins tie that rule to torch
 conv1d over the kept token stream; here the GPU follows the oracle step by
-step on its own state, for the three pool layouts the kernel handles
-differently (dense history-contiguous, staged through shared memory;
-channel-contiguous, 16-byte vectors; any other strides, element by element).
+step on its own state, for the three pool layouts the kernels handle
+differently (dense history-contiguous: a lane's whole block in registers;
+channel-contiguous: 16-byte vectors; any other strides: element by element).
 """
 import numpy as np
 import pytest
@@ -130,13 +130,15 @@ def test_decode_chain_variants(cuda_device, width, act):
                steps=4, seed=20 + width, b_dtype=None)
 
 
-@pytest.mark.parametrize("width,L", [(4, 3), (4, 4), (4, 8), (3, 2), (3, 4), (2, 1), (2, 2), (2, 8)])
+@pytest.mark.parametrize("width,L", [(w, L) for w in (2, 3, 4) for L in range(w - 1, 9)])
 def test_dense_pool_every_length(cuda_device, width, L):
-    """The dense history-contiguous pool at every staged length the kernel
-    specialises for (G = 8 / gcd(L, 8) channels per thread), drafts up to
-    L - W + 2 tokens so every position can be written."""
+    """The dense history-contiguous pool at every length the register-block
+    kernel is compiled for (L = W-1 .. 8), with drafts up to two tokens
+    longer than the L - W + 2 the slot can keep: every position is written,
+    every accepted offset is read, and the tokens past the slot's capacity
+    take the kernel's one-token-at-a-time tail."""
     _run_chain(cuda_device, width=width, act="silu" if L % 2 else None, layout="dense", C=264, N=11, L=L,
-               kmax=L - width + 2, steps=6, seed=60 + 10 * width + L)
+               kmax=L - width + 4, steps=6, seed=60 + 10 * width + L)
 
 
 def test_plain_decode_one_token(cuda_device):
