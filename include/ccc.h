@@ -257,6 +257,54 @@ int ccc_update(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
                const int32_t *cache_indices, const int32_t *num_accepted,
                void *out, int64_t out_row_stride, void *cuda_stream);
 
+/*
+ * Device-side check of the caller-owned metadata.  The pages leave the
+ * values in cu_seqlens, cache_indices (and, for the decode step,
+ * num_accepted) unchecked: no host read, no validation synchronization
+ * (causal_conv1d_fn, Notes), and invalid values are the caller's fault.
+ * The kernels above never read or write outside the buffers they are given
+ * whatever those values are (offsets are clamped to [0, rows], slot IDs
+ * outside [0, n_slots) are skipped), but their results are then
+ * meaningless.  This call finds such values on the device, still without a
+ * host synchronization, for callers that want to check a batch (in tests,
+ * or once per new batch layout).  The pages have no counterpart.
+ *
+ * It clears `status` and ORs into status[0] one CCC_CHECK_* bit per kind of
+ * violation found (0: every value is valid); nothing traps.  The caller
+ * reads status[0] after the stream reaches that point.
+ *
+ *  rows          rows of the packed x the metadata will be used with.
+ *  cu_seqlens    [dev] int32 [N + 1], required.  Checked: cu[0] == 0,
+ *                nondecreasing, every offset in [0, rows].
+ *  cache_indices [dev] int32 [N] or NULL (not checked).  Checked: every
+ *                value is -1 or in [0, n_slots); no live slot appears twice.
+ *  num_accepted  [dev] int32 [N] or NULL (not checked).  Checked: every
+ *                value in [1, max_accepted] (ccc_update: max_accepted =
+ *                state_len - width + 2).
+ *  status        [dev] uint32 [status_words], caller-owned, with
+ *                status_words >= ccc_check_status_words(n_slots): word 0 is
+ *                the result, the rest a bitmap of live slots (scratch).
+ * Returns CCC_ERR_NULL / CCC_ERR_SHAPE / CCC_ERR_WORKSPACE (status too
+ * small) / CCC_ERR_ALIAS with nothing enqueued; otherwise one memset and one
+ * kernel launch on cuda_stream.
+ */
+enum {
+    CCC_CHECK_CU_START = 1 << 0,   /* cu_seqlens[0] != 0 */
+    CCC_CHECK_CU_ORDER = 1 << 1,   /* an offset smaller than the one before it */
+    CCC_CHECK_CU_RANGE = 1 << 2,   /* an offset outside [0, rows] */
+    CCC_CHECK_SLOT_RANGE = 1 << 3, /* a cache index outside [-1, n_slots) */
+    CCC_CHECK_SLOT_DUP = 1 << 4,   /* a live slot used by two sequences */
+    CCC_CHECK_ACCEPTED = 1 << 5    /* an accepted count outside [1, max_accepted] */
+};
+
+/* Words of the status array ccc_check needs: 1 + ceil(n_slots / 32). */
+size_t ccc_check_status_words(int32_t n_slots);
+
+int ccc_check(int64_t rows, const int32_t *cu_seqlens, int32_t N,
+              const int32_t *cache_indices, int32_t n_slots,
+              const int32_t *num_accepted, int32_t max_accepted,
+              uint32_t *status, size_t status_words, void *cuda_stream);
+
 /* Name of a ccc_status value ("CCC_OK", ...); "unknown" otherwise. */
 const char *ccc_status_string(int status);
 

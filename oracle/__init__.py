@@ -275,3 +275,49 @@ def threads() -> int:
         return len(os.sched_getaffinity(0))
     except AttributeError:  # pragma: no cover
         return os.cpu_count() or 1
+
+
+# Violation bits of the metadata check (the same values as the library's
+# CCC_CHECK_* status bits, restated here so the oracle imports nothing from it).
+CU_START, CU_ORDER, CU_RANGE, SLOT_RANGE, SLOT_DUP, ACCEPTED = 1, 2, 4, 8, 16, 32
+
+
+def check_metadata(rows, cu_seqlens, cache_indices=None, n_slots=0, accepted=None, max_accepted=0) -> int:
+    """The caller-owned constraints of FlashInfer causal_conv1d_fn
+    (Parameters: the offsets begin at 0, never decrease and end at or before
+    row `rows`, so each lies in [0, rows]; a cache index is -1 or a slot in
+    [0, n_slots), and no slot serves two sequences), and the accepted count
+    of the decode step in [1, max_accepted]: the OR of one bit per kind of
+    violation, 0 when all hold.  Plain loops over the values."""
+    cu = [int(v) for v in np.asarray(_host(cu_seqlens)).reshape(-1)]
+    bits = 0
+    if cu and cu[0] != 0:
+        bits |= CU_START
+    for i, v in enumerate(cu):
+        if v < 0 or v > rows:
+            bits |= CU_RANGE
+        if i > 0 and v < cu[i - 1]:
+            bits |= CU_ORDER
+    if cache_indices is not None:
+        seen = set()
+        for q in (int(v) for v in np.asarray(_host(cache_indices)).reshape(-1)):
+            if q == -1:
+                continue
+            if q < 0 or q >= n_slots:
+                bits |= SLOT_RANGE
+            elif q in seen:
+                bits |= SLOT_DUP
+            else:
+                seen.add(q)
+    if accepted is not None:
+        for a in (int(v) for v in np.asarray(_host(accepted)).reshape(-1)):
+            if a < 1 or a > max_accepted:
+                bits |= ACCEPTED
+    return bits
+
+
+def _host(a):
+    """numpy view of a CPU or CUDA tensor (or array-like)."""
+    if hasattr(a, "detach"):
+        return a.detach().cpu().numpy()
+    return a

@@ -37,10 +37,14 @@ from . import _lib
 
 CCC_F32, CCC_BF16, CCC_NONE = 0, 1, -1
 CCC_ACT_NONE, CCC_ACT_SILU = 0, 1
+# Status bits of ccc_check (include/ccc.h).
+CHECK_CU_START, CHECK_CU_ORDER, CHECK_CU_RANGE = 1, 2, 4
+CHECK_SLOT_RANGE, CHECK_SLOT_DUP, CHECK_ACCEPTED = 8, 16, 32
 
 __all__ = ["ccc_workspace_size", "ccc_fwd", "ccc_bwd", "ccc_bwd_noalloc", "ccc_update",
            "causal_conv1d_fn", "causal_conv1d_bwd", "causal_conv1d_update", "recompute_fwd",
-           "CausalConv1dFn", "causal_conv1d", "CCCError", "library_path", "last_launch_count"]
+           "CausalConv1dFn", "causal_conv1d", "CCCError", "library_path", "last_launch_count",
+           "ccc_check", "check_metadata"]
 
 
 class CCCError(RuntimeError):
@@ -202,6 +206,33 @@ def ccc_update(x, weight, bias, conv_state, cu_seqlens, cache_indices, num_accep
         _ptr(o2), os_, _stream(stream))
     if rc != 0:
         raise CCCError(rc, "ccc_update")
+
+
+def ccc_check(rows, cu_seqlens, cache_indices=None, n_slots=0, num_accepted=None, max_accepted=0,
+              status=None, stream=None) -> torch.Tensor:
+    """Device-side check of the metadata (include/ccc.h, ccc_check): returns
+    the int32-viewed status array whose word 0 receives the CCC_CHECK_* bits
+    once the stream gets there (no synchronization here)."""
+    N = cu_seqlens.numel() - 1
+    words = int(_lib.lib().ccc_check_status_words(int(n_slots))) if cache_indices is not None else 1
+    if status is None:
+        status = torch.empty(words, dtype=torch.int32, device=cu_seqlens.device)
+    if status.dtype != torch.int32 or not status.is_contiguous():
+        raise ValueError("status must be a contiguous int32 tensor")
+    rc = _lib.lib().ccc_check(int(rows), _ptr(cu_seqlens), N, _ptr(cache_indices), int(n_slots),
+                              _ptr(num_accepted), int(max_accepted), _ptr(status), status.numel(),
+                              _stream(stream))
+    if rc != 0:
+        raise CCCError(rc, "ccc_check")
+    return status
+
+
+def check_metadata(rows, cu_seqlens, cache_indices=None, n_slots=0, num_accepted=None,
+                   max_accepted=0) -> int:
+    """ccc_check, then a host read of the result (synchronizes the current
+    stream): 0 when every value is valid, else the OR of CHECK_* bits."""
+    st = ccc_check(rows, cu_seqlens, cache_indices, n_slots, num_accepted, max_accepted)
+    return int(st[0].item()) & 0xffffffff
 
 
 def _workspace(rows, N, C, for_bwd, device, given):

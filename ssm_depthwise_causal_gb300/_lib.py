@@ -15,7 +15,7 @@ _lock = threading.Lock()
 _handle = None
 
 EXPORTS = ("ccc_workspace_size", "ccc_fwd", "ccc_bwd", "ccc_bwd_noalloc", "ccc_update",
-           "ccc_status_string", "ccc_last_launch_count")
+           "ccc_check_status_words", "ccc_check", "ccc_status_string", "ccc_last_launch_count")
 
 # Size of the fixed scratch array behind ccc_bwd_noalloc (CCC_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -51,6 +51,10 @@ def lib() -> ctypes.CDLL:
             h.ccc_update.argtypes = [P, i64, i32, i64, P, i32, i32, P, i32, i32, P, i32, i32, i64, i64, i64,
                                      P, i32, P, P, P, i64, P]
             h.ccc_update.restype = ctypes.c_int
+            h.ccc_check_status_words.argtypes = [i32]
+            h.ccc_check_status_words.restype = sz
+            h.ccc_check.argtypes = [i64, P, i32, P, i32, P, i32, P, sz, P]
+            h.ccc_check.restype = ctypes.c_int
             h.ccc_status_string.argtypes = [ctypes.c_int]
             h.ccc_status_string.restype = ctypes.c_char_p
             h.ccc_last_launch_count.argtypes = []

@@ -194,3 +194,28 @@ def call_update(lib, **kw):
 ])
 def test_update_host_checks(lib, kw, code):
     assert call_update(lib, **kw) == code
+
+
+def test_check_status_words(lib):
+    w = lib.ccc_check_status_words
+    assert [w(0), w(1), w(32), w(33), w(100000)] == [1, 2, 2, 3, 1 + 3125]
+
+
+def test_check_host_errors(lib):
+    """ccc_check's host checks fail before any CUDA call (the fake device
+    addresses are never dereferenced)."""
+    P = ctypes.c_void_p
+    cu, cache, acc, st = P(0x10000), P(0x20000), P(0x30000), P(0x40000)
+    chk = lib.ccc_check
+    assert chk(10, None, 2, None, 0, None, 0, st, 1, None) == E_NULL
+    assert chk(10, cu, 2, None, 0, None, 0, None, 1, None) == E_NULL
+    assert chk(-1, cu, 2, None, 0, None, 0, st, 1, None) == E_SHAPE
+    assert chk(10, cu, -1, None, 0, None, 0, st, 1, None) == E_SHAPE
+    assert chk(10, cu, 2, cache, -1, None, 0, st, 9, None) == E_SHAPE
+    assert chk(10, cu, 2, None, 0, acc, 0, st, 1, None) == E_SHAPE          # max_accepted < 1
+    assert chk(10, P(0x10001), 2, None, 0, None, 0, st, 1, None) == E_ALIGN
+    assert chk(10, cu, 2, cache, 0, None, 0, P(0x40002), 1, None) == E_ALIGN
+    assert chk(10, cu, 2, cache, 100, None, 0, st, 4, None) == E_WS         # needs 1 + 4 words
+    assert chk(10, cu, 2, None, 0, None, 0, st, 0, None) == E_WS
+    assert chk(10, cu, 2, None, 0, None, 0, P(0x10008), 1, None) == E_ALIAS  # status inside cu_seqlens
+    assert chk(10, cu, 2, cache, 64, None, 0, P(0x1fffc), 3, None) == E_ALIAS  # bitmap runs into cache
