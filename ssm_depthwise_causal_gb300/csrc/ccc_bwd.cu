@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
     auto issue = [&]() {
         if constexpr (kBwdPrefetch > 0) {
             // lanes 0..2U-1: the warp's slab of x / dy rows PF ahead into L2
-            const int pr = p_row + kBwdPrefetch + (lane >> 1);
+            const int64_t pr = static_cast<int64_t>(p_row) + kBwdPrefetch + (lane >> 1);
             if (full && lane < 2 * U && pr < p_end) {
                 const uint16_t *base_ptr = (lane & 1) ? a.dy + static_cast<int64_t>(pr) * a.dys
                                                       : a.x + static_cast<int64_t>(pr) * a.xs;
@@ -153,7 +153,8 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
             }
         }
         const uint32_t stage = ring + static_cast<uint32_t>(st_in * U * 2 * 32 * VB);
-        if (act && p_row + U <= p_end) {  // the whole batch inside the walk: plain copies
+        // (row arithmetic as differences: p_end may be 2^31 - 1)
+        if (act && p_end - p_row >= U) {  // the whole batch inside the walk: plain copies
             const uint16_t *qx = px, *qg = pg;
 #pragma unroll
             for (int u = 0; u < U; ++u) {
@@ -166,8 +167,7 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
         } else {
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const int row = p_row + u;
-                const bool ok = act && row < p_end;
+                const bool ok = act && u < p_end - p_row;
                 const uint32_t off = static_cast<uint32_t>((u * 2) * 32 * VB);
                 cp_async<VB>(stage + off, ok ? px + static_cast<int64_t>(u) * a.xs : a.x, ok);
                 cp_async<VB>(stage + off + 32 * VB, ok ? pg + static_cast<int64_t>(u) * a.dys : a.dy, ok);
@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
         cp_async_commit();
         ++issued;
         st_in = st_in + 1 == (P > 0 ? P : 1) ? 0 : st_in + 1;
-        p_row += U;
+        p_row = p_end - p_row > U ? p_row + U : p_end;  // saturates: never past p_end
         px += static_cast<int64_t>(U) * a.xs;
         pg += static_cast<int64_t>(U) * a.dys;
     };
@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
                 // sequence goes on beyond it.
                 cp_async_wait(0);
                 p_row = t.r0;
-                p_end = min(walk.R_hi + H, t.e);
+                p_end = t.e - walk.R_hi > H ? walk.R_hi + H : t.e;  // min(R_hi + H, e) without overflow
                 issued = consumed = 0;
                 st_in = st_out = 0;
                 px = a.x + static_cast<int64_t>(p_row) * a.xs + c0;
@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
                 if (fast) {  // all lanes, all rows: unconditional loads, stepping row pointers
                     if constexpr (kBwdPrefetch > 0) {
                         // lanes 0..2U-1: the warp's slab of x / dy rows PF ahead into L2
-                        const int pr = t.r0 + base + kBwdPrefetch + (lane >> 1);
+                        const int64_t pr = static_cast<int64_t>(t.r0) + base + kBwdPrefetch + (lane >> 1);
                         if (lane < 2 * U && pr < t.e) {
                             const uint16_t *pp = (lane & 1) ? a.dy + static_cast<int64_t>(pr) * a.dys
                                                             : a.x + static_cast<int64_t>(pr) * a.xs;
@@ -281,7 +281,7 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
 #pragma unroll
                     for (int u = 0; u < U; ++u) {
                         const bool ld = act && base + u < nload;
-                        const int row = t.r0 + base + u;
+                        const int64_t row = static_cast<int64_t>(t.r0) + base + u;
                         xr[u] = ld ? ld_ro<NV>(a.x + static_cast<int64_t>(row) * a.xs + c0) : raw_zero<NV>();
                         gr[u] = ld ? ld_ro<NV>(a.dy + static_cast<int64_t>(row) * a.dys + c0) : raw_zero<NV>();
                     }
@@ -335,7 +335,7 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
             for (int u = 0; u < U; ++u) {
                 const int k = base + u;
                 if (k >= iters) break;
-                const int i = o0 + k;
+                const int64_t i = static_cast<int64_t>(o0) + k;  // up to L + H - 1 (L may be 2^31 - 1)
                 float2 hc[NV], dz[NV];
                 unpack<NV>(xr[u], hc);
                 if (k < nload) {
@@ -371,9 +371,9 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
                             Raw<NV> o;
 #pragma unroll
                             for (int v = 0; v < NV; ++v) o.u[v] = f2_to_bf2(acc[v]);
-                            st_stream<NV>(a.dx + static_cast<int64_t>(t.s + i - H) * a.dxs + c0, o);
+                            st_stream<NV>(a.dx + (t.s + i - H) * a.dxs + c0, o);
                         } else {
-                            float2 *dp = reinterpret_cast<float2 *>(dinit + static_cast<int64_t>(i) * a.C);
+                            float2 *dp = reinterpret_cast<float2 *>(dinit + i * a.C);
 #pragma unroll
                             for (int v = 0; v < NV; ++v) dp[v] = read_state ? acc[v] : f2_zero();
                         }

@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
     const bool act = cv < a.C / VEC;
     const bool full = (slab + 1) * 32 * VEC <= a.C;  // warp-uniform: all lanes have channels
     const int c0 = act ? cv * VEC : 0;
+    const int rows_i = static_cast<int>(a.rows);  // host-checked <= 2^31 - 1
 
     float2 wt[W][NV], bb[NV];
     load_taps_w<NV, W>(a.w, a.w_bf16, a.b, a.b_kind, c0, act, wt, bb);
@@ -175,9 +176,10 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
             for (; base + U <= nr; base += U) {
                 if constexpr (kFwdPrefetch > 0) {
                     // lanes 0..U-1: the warp's slab of row r0+base+PF+lane into L2
-                    const int pr = t.r0 + base + kFwdPrefetch + lane;
-                    if (lane < U && pr < a.rows)
-                        prefetch_l2(a.x + static_cast<int64_t>(pr) * a.xs + slab * 32 * VEC, 32 * VEC * 2);
+                    // (as a difference: rows may be 2^31 - 1)
+                    const int ahead = kFwdPrefetch + lane;
+                    if (lane < U && ahead < rows_i - (t.r0 + base))
+                        prefetch_l2(xp + static_cast<int64_t>(ahead) * a.xs - c0 + slab * 32 * VEC, 32 * VEC * 2);
                 }
                 Raw<NV> cur[U];
                 const uint16_t *lp = xp;
@@ -220,9 +222,9 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
             Raw<NV> fin[H];
 #pragma unroll
             for (int p = 0; p < H; ++p) {
-                const int idx = L + p;
-                if (idx >= H) {
-                    fin[p] = ld_ro<NV>(a.x + static_cast<int64_t>(t.s + idx - H) * a.xs + c0);
+                const int idx = L < H ? L + p : H;  // history index L + p (>= H past the initial values)
+                if (L >= H - p) {
+                    fin[p] = ld_ro<NV>(a.x + (static_cast<int64_t>(t.e) - H + p) * a.xs + c0);
                 } else {
                     fin[p] = init[0];
 #pragma unroll

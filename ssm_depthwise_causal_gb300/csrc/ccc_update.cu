@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(kCtaThreads, kUpdMinBlocks) update_kernel(cons
         uint16_t *orow = a.out + static_cast<int64_t>(cur.s) * a.os + c0;
         const bool pool = len > 0 && q >= 0 && q < a.n_slots;
         const int acc = min(max(cur.acc, 1), a.L - H + 1);
-        const int n_write = min(len + H - 1, a.L);  // positions written
+        const int n_write = len >= a.L ? a.L : min(len + H - 1, a.L);  // positions written
 
         if (len > 0 && q == -1) {  // padded request: zero output, no state access
             if (act) {
@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(kCtaThreads, kUpdMinBlocks) update_kernel(cons
                     if (j >= len) break;
                     st_stream<NV>(orow + static_cast<int64_t>(j) * a.os, update_token<W, ACT, NV>(wt, bb, hw, xr[u]));
                     // token j is history value H + j: position H - 1 + j
-                    if (pool && H - 1 + j < n_write) state_put<NV>(a, q, H - 1 + j, c0, xr[u]);
+                    if (pool && j < n_write - (H - 1)) state_put<NV>(a, q, H - 1 + j, c0, xr[u]);
                 }
             }
         }
@@ -354,7 +354,7 @@ __global__ void __launch_bounds__(kCtaThreads, upd_block_min_blocks(LS)) update_
     // position e % LS): one byte permute gathers both new halves, and a
     // mask per position keeps the old half where nothing is written.
     if (pool) {
-        const int n_write = min(len + H - 1, LS);
+        const int n_write = len >= LS ? LS : min(len + H - 1, LS);
         uint32_t keep_lo[LS], keep_hi[LS];
 #pragma unroll
         for (int p = 0; p < LS; ++p) {
