@@ -15,8 +15,8 @@
  *     z = bias[c] + w[c][0]*h[j] + w[c][1]*h[j+1] + w[c][2]*h[j+2] + w[c][3]*h[j+3]
  *     out[j][c] = BF16_rne( z * sigmoid(z) )
  *
- * (tap 3 multiplies the current token; the bias is added before the four
- * FMAs, which run in the order k = 0, 1, 2, 3).  cache_indices[n] == -1
+ * (tap 3 acts on the current token; the sum starts from the bias and the
+ * four FMAs follow in the order k = 0, 1, 2, 3).  cache_indices[n] == -1
  * produces a zero output and no state access.  A live sequence with at
  * least one token leaves the last three inputs of its history (unactivated)
  * in its slot at positions 0, 1, 2, oldest first; nothing else in the pool
@@ -24,7 +24,8 @@
  * cu_seqlens[N] are never written.
  *
  * The backward (FlashInfer "cake_causal_conv1d_train.cake_causal_conv1d_kcp",
- * Returns: fused dx + deterministic FP32 dweight) recomputes z, forms
+ * Returns: dx from one fused kernel, the weight gradient in FP32 with a
+ * run-to-run identical result) recomputes z, forms
  * dz = dy * s * (1 + z * (1 - s)) with s = sigmoid(z), and gives
  *
  *     dH[i] = carry + w[c][0]*dz[i] + w[c][1]*dz[i-1] + w[c][2]*dz[i-2] + w[c][3]*dz[i-3]

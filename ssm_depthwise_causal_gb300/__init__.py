@@ -12,7 +12,7 @@ Entry points (same names as the C ABI):
 * ``ccc_workspace_size(rows, n_seqs, channels, for_bwd)``
 * ``ccc_fwd(...)``  -- forward + in-place conv_state update
   (FlashInfer ``flashinfer.mamba.causal_conv1d_fn``)
-* ``ccc_bwd(...)``  -- fused dx + deterministic FP32 dweight/dbias
+* ``ccc_bwd(...)``  -- one-pass dx, with FP32 dweight/dbias summed in a fixed order
   (``cake_causal_conv1d_kcp``, Returns)
 * ``ccc_update(...)`` -- speculative / single-token decode step on the pool
 * ``ccc_bwd_noalloc(...)`` -- ``ccc_bwd`` on the library's own scratch

@@ -4,9 +4,9 @@
 // FlashInfer "cake_causal_conv1d_train.cake_causal_conv1d_kcp" (Returns): one
 // kernel produces the input gradient and deterministic FP32 weight-gradient
 // partials; Megatron-Core "core.ssm.causal_conv1d"
-// (assert_causal_conv1d_deterministic): partials go to a per-block workspace
-// and are combined by an ordered reduction instead of atomics, so the result
-// does not depend on scheduling.
+// (assert_causal_conv1d_deterministic): each warp task writes its own
+// partial row to scratch and a second kernel adds the rows in a fixed order
+// (no atomics), so the result does not depend on scheduling.
 //
 // Per token j of a live sequence (history index i = j for the 3 initial
 // values, i = j + 3 for input rows):
