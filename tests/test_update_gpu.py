@@ -264,3 +264,38 @@ def test_btd_helpers(cuda_device):
                    cache, acc, yk2)
     assert torch.equal(yk.view(B * 2, D).view(torch.int16), yk2.view(torch.int16))
     assert torch.equal(pool.view(torch.int16), pool2.view(torch.int16))
+
+
+@pytest.mark.parametrize("layout", ["dense", "channel", "padded"])
+def test_strided_token_rows(cuda_device, layout):
+    """x a column slice of a wider matrix (row stride C + 64) and out with a
+    padded row stride (C + 8), for every pool layout: the outputs equal a
+    contiguous call bit for bit, the padding columns of out are untouched,
+    and the pools end identical."""
+    dev = cuda_device
+    rng = np.random.default_rng(31)
+    g = workloads._gen(31, dev)
+    N, C, L, slots = 21, 264, 7, 30
+    lengths = rng.integers(0, 6, N)
+    rows = int(lengths.sum()) + 2
+    cu = workloads.cu_from_lengths(lengths).to(dev)
+    cache_np = rng.permutation(slots)[:N].astype(np.int32)
+    cache_np[3] = -1
+    cache = torch.from_numpy(cache_np).to(dev)
+    acc = torch.from_numpy(rng.integers(1, L - 2, N).astype(np.int32)).to(dev)
+    weight = workloads.uniform((C, 4), g, dev, -0.5, 0.5, torch.float32)
+    bias = (torch.randn((C,), generator=g, device=dev) * 0.1).to(torch.bfloat16)
+    wide = workloads.normal_bf16((rows, C + 64), g, dev)
+    x_strided = wide[:, 32:32 + C]
+    x = x_strided.contiguous()
+    pool_a = _pool(slots, C, L, layout, g, dev)
+    pool_b = _pool(slots, C, L, layout, workloads._gen(99, dev), dev)  # same layout, then the same values
+    pool_b.copy_(pool_a)
+    out_pad = H.fill_sentinel(torch.empty((rows, C + 8), dtype=torch.bfloat16, device=dev))
+    out = H.fill_sentinel(torch.empty((rows, C), dtype=torch.bfloat16, device=dev))
+    ccc.ccc_update(x_strided, weight, bias, pool_a, cu, cache, acc, out_pad[:, :C])
+    ccc.ccc_update(x, weight, bias, pool_b, cu, cache, acc, out)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(_bits(out_pad[:, :C]), _bits(out))
+    assert np.all(_bits(out_pad[:, C:]) == H.SENTINEL), "padding columns of out were written"
+    np.testing.assert_array_equal(_bits(pool_a), _bits(pool_b))
