@@ -27,9 +27,9 @@
 // of a channel pair, and rebuilding the block after the step, are byte
 // permutes with compile-time selectors, so the block never goes through
 // shared memory.  A warp's only dependent round trips are the sequence's
-// offsets / slot / accepted count, then the block and its new tokens; the
-// grid holds every pair at once, so those trips overlap across warps instead
-// of queueing inside one.  The block is written back (every position; the
+// offsets / slot / accepted count, then the block and its new tokens; with
+// one warp per pair those trips overlap across warps instead of queueing
+// inside one.  The block is written back (every position; the
 // ones not rewritten keep their bits) before the outputs are computed, which
 // frees its registers for the arithmetic.
 //
@@ -39,7 +39,7 @@
 // position for a channel-contiguous pool, single elements otherwise.
 //
 // In both kernels the slab's taps and bias are staged once per CTA in shared
-// memory (coalesced global reads).  Reads of a slot precede every write to
+// memory (one channel per thread).  Reads of a slot precede every write to
 // it in the lane's program order, and no other lane touches the same
 // elements (live slots are unique, lanes' channels disjoint), so the in-place
 // update needs no synchronisation.
