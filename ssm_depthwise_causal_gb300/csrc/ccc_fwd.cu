@@ -38,12 +38,11 @@ namespace ccc {
 
 namespace {
 
-// State positions 0..H-1 of slot q (position 0 = oldest), or the window of
-// positions p0 .. p0+H-1 for the speculative update.
+// State positions 0..H-1 of slot q (position 0 = oldest).
 template <int NV, int H>
 __device__ __forceinline__ void gather_state(const uint16_t *state, int64_t st_slot, int64_t st_c, int64_t st_l,
-                                             bool vec, int q, int p0, int c0, Raw<NV> (&hr)[H]) {
-    const uint16_t *base = state + static_cast<int64_t>(q) * st_slot + static_cast<int64_t>(p0) * st_l;
+                                             bool vec, int q, int c0, Raw<NV> (&hr)[H]) {
+    const uint16_t *base = state + static_cast<int64_t>(q) * st_slot;
     if (vec) {
 #pragma unroll
         for (int p = 0; p < H; ++p) hr[p] = ld_rw<NV>(base + p * st_l + c0);
@@ -155,7 +154,7 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
 #pragma unroll
             for (int p = 0; p < H; ++p) hr[p] = raw_zero<NV>();
             if (o0 == 0) {
-                if (rd && act) gather_state<NV, H>(a.state, a.st_slot, a.st_c, a.st_l, a.state_vec, q, 0, c0, hr);
+                if (rd && act) gather_state<NV, H>(a.state, a.st_slot, a.st_c, a.st_l, a.state_vec, q, c0, hr);
                 if (a.hist && act)
 #pragma unroll
                     for (int p = 0; p < H; ++p)
@@ -218,7 +217,7 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
 #pragma unroll
             for (int p = 0; p < H; ++p) init[p] = raw_zero<NV>();
             if (rd && L < H)  // still unwritten
-                gather_state<NV, H>(a.state, a.st_slot, a.st_c, a.st_l, a.state_vec, q, 0, c0, init);
+                gather_state<NV, H>(a.state, a.st_slot, a.st_c, a.st_l, a.state_vec, q, c0, init);
             Raw<NV> fin[H];
 #pragma unroll
             for (int p = 0; p < H; ++p) {
