@@ -87,8 +87,9 @@ def algorithmic_bytes(wl):
     Forward: x read + out written for valid tokens of live sequences (-1
     sequences write zeros and read nothing), weights, bias, and 3 state rows
     read / written per sequence with a pool.  Backward: x, dy read and dx
-    written per valid token, saved history read, weights, bias, dweight and
-    dbias written."""
+    written per valid token, weights, bias, dweight and dbias written.  The
+    saved history (3 rows per sequence, written by the forward and read by
+    the backward) is not counted, so the figures err low."""
     T, C = wl.valid_tokens, wl.C
     wsz = wl.weight.element_size()
     bsz = 0 if wl.bias is None else wl.bias.element_size()
@@ -346,7 +347,7 @@ def run_ours(args, ws, rank, local):
                          db=torch.empty_like(db)))
     h2d = hx.numel() * 2 + hdy.numel() * 2
     d2h = hout.numel() * 2 + hdx.numel() * 2 + hdw.numel() * 4 + hdb.numel() * 4
-    e2e_steps = max(4, min(K, 10))
+    e2e_steps = max(4, K)  # the same number of steps as the device-timed region
     s_in = torch.cuda.Stream(device=dev)
     s_out = torch.cuda.Stream(device=dev)
     ev = lambda: torch.cuda.Event()  # noqa: E731
@@ -625,6 +626,142 @@ def run_profile(args, local):
     print(json.dumps({"profile_case": wl.name, "valid_tokens": T}), flush=True)
 
 
+CONFIG_WORKLOADS = ("tiny", "dense", "packed", "serving", "long")
+
+
+def time_fragment_chain(ccc, wl, out, dx, flush, stream, args):
+    """The long document as `fragments` consecutive calls chained through a
+    one-slot pool (forward: fragment k reads the state fragment k-1 wrote;
+    backward in reverse, d_init_state of fragment k as d_final_state of
+    fragment k-1): device time of the forward chain and of the backward chain
+    (the host-side sum of the per-fragment dweight is not included)."""
+    dev = wl.x.device
+    T, C, F = wl.rows, wl.C, wl.fragments
+    Lf = T // F
+    pool = torch.zeros((1, C, 4), dtype=torch.bfloat16, device=dev)
+    cache = torch.zeros(1, dtype=torch.int32, device=dev)
+    cu_f = torch.tensor([0, Lf], dtype=torch.int32, device=dev)
+    flags = [torch.tensor([k > 0], device=dev) for k in range(F)]
+    hists = [torch.empty((1, 3, C), dtype=torch.bfloat16, device=dev) for _ in range(F)]
+    d_init = [torch.empty((1, 3, C), dtype=torch.float32, device=dev) for _ in range(F)]
+    dws = [torch.empty((C, 4), dtype=torch.float32, device=dev) for _ in range(F)]
+    ws_f = torch.empty(ccc.ccc_workspace_size(Lf, 1, C, True), dtype=torch.uint8, device=dev)
+    part = lambda t, k: t[k * Lf:(k + 1) * Lf]  # noqa: E731
+
+    def fwd_chain():
+        for k in range(F):
+            ccc.ccc_fwd(part(wl.x, k), wl.weight, wl.bias, pool, cu_f, cache, flags[k], part(out, k), hists[k],
+                        None, stream=stream)
+
+    def bwd_chain():
+        carry = None
+        for k in reversed(range(F)):
+            ccc.ccc_bwd(part(wl.x, k), wl.weight, wl.bias, hists[k], cu_f, cache, flags[k], part(wl.dy, k), carry,
+                        part(dx, k), dws[k], None, d_init[k], ws_f, stream=stream)
+            carry = d_init[k]
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            fwd_chain()
+            bwd_chain()
+        for k in range(K):
+            flush.zero_()
+            ev[k][0].record(stream)
+            fwd_chain()
+            ev[k][1].record(stream)
+            bwd_chain()
+            ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    f_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    b_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    return {"split_fragments": F, "split_fwd_ms": f_ms, "split_bwd_ms": b_ms, "split_step_ms": f_ms + b_ms,
+            "split_step_tokens_per_s": T / ((f_ms + b_ms) / 1e3)}
+
+
+def run_configs(args, local):
+    """Forward and (for training workloads) forward + backward of every
+    workload, device-timed: K steps after W warm-up steps, L2 flushed before
+    each timed step, one JSON line with a row per workload.  A forward with a
+    pool updates it in place every step; the work per step does not depend
+    on the values, so the pool is not restored between steps."""
+    import ssm_depthwise_causal_gb300 as ccc
+    from ssm_depthwise_causal_gb300 import workloads
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    ccc._lib.lib()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    peak, peak_kind = measured_peak()
+    stream = torch.cuda.Stream(device=dev)
+    rows_out = []
+    clocks = ClockSampler(local)
+    clocks.start()
+    for name in CONFIG_WORKLOADS:
+        wl = workloads.WORKLOADS[name](device=dev)
+        T, C, N, rows = wl.valid_tokens, wl.C, wl.n_seqs, wl.rows
+        out = torch.empty_like(wl.x)
+        hist = torch.empty((N, 3, C), dtype=torch.bfloat16, device=dev)
+        state = wl.conv_state
+        dx = dw = db = ws_b = None
+        if wl.training:
+            dx = torch.empty_like(wl.x)
+            dw = torch.empty((C, 4), dtype=torch.float32, device=dev)
+            db = None if wl.bias is None else torch.empty((C,), dtype=torch.float32, device=dev)
+            ws_b = torch.empty(ccc.ccc_workspace_size(rows, N, C, True), dtype=torch.uint8, device=dev)
+
+        def fwd():
+            ccc.ccc_fwd(wl.x, wl.weight, wl.bias, state, wl.cu_seqlens, wl.cache_indices, wl.has_initial_state,
+                        out, hist, None, stream=stream)
+
+        def bwd():
+            ccc.ccc_bwd(wl.x, wl.weight, wl.bias, hist, wl.cu_seqlens, wl.cache_indices, wl.has_initial_state,
+                        wl.dy, None, dx, dw, db, None, ws_b, stream=stream)
+
+        K = args.steps
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                fwd()
+                if wl.training:
+                    bwd()
+            for k in range(K):
+                flush.zero_()
+                ev[k][0].record(stream)
+                fwd()
+                ev[k][1].record(stream)
+                if wl.training:
+                    bwd()
+                ev[k][2].record(stream)
+        torch.cuda.synchronize()
+        fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+        fb, bb = algorithmic_bytes(wl)
+        row = {"workload": wl.name, "valid_tokens": T, "C": C, "n_seqs": N,
+               "fwd_ms": fwd_ms, "fwd_tokens_per_s": T / (fwd_ms / 1e3),
+               "fwd_gbs": fb / (fwd_ms / 1e3) / 1e9, "fwd_frac": fb / (fwd_ms / 1e3) / 1e9 / peak,
+               "fwd_algorithmic_bytes": fb}
+        if wl.training:
+            bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+            step_ms = fwd_ms + bwd_ms
+            row.update({"bwd_ms": bwd_ms, "bwd_gbs": bb / (bwd_ms / 1e3) / 1e9,
+                        "bwd_frac": bb / (bwd_ms / 1e3) / 1e9 / peak, "bwd_algorithmic_bytes": bb,
+                        "step_ms": step_ms, "step_tokens_per_s": T / (step_ms / 1e3),
+                        "step_gbs": (fb + bb) / (step_ms / 1e3) / 1e9,
+                        "step_frac": (fb + bb) / (step_ms / 1e3) / 1e9 / peak})
+        if wl.training and getattr(wl, "fragments", 1) > 1:
+            row.update(time_fragment_chain(ccc, wl, out, dx, flush, stream, args))
+        rows_out.append(row)
+        wl = out = hist = state = dx = dw = db = ws_b = None  # free this workload's tensors
+        torch.cuda.empty_cache()
+    clk = clocks.stop()
+    print(json.dumps({"op": "configs", "steps": args.steps, "warmup": args.warmup, "peak": peak,
+                      "peak_kind": peak_kind, "unit_gbs": "GB/s (algorithmic bytes / CUDA-event time)",
+                      "l2": "flushed before every timed step", "data": "synthetic",
+                      "configs": rows_out, "clocks": clk}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -638,14 +775,17 @@ def main():
                     help="run warm-up + one step of --workload only (for ncu captures)")
     ap.add_argument("--workload", default="packed",
                     choices=["tiny", "dense", "packed", "packed_small", "serving", "long", "decode", "spec_decode"])
-    ap.add_argument("--op", default="fwdbwd", choices=["fwdbwd", "update"],
+    ap.add_argument("--op", default="fwdbwd", choices=["fwdbwd", "update", "configs"],
                     help="fwdbwd: the packed training step (the headline); update: one decode step "
-                         "(ccc_update) of --workload decode / spec_decode")
+                         "(ccc_update) of --workload decode / spec_decode; configs: forward and "
+                         "forward+backward of every workload, device-timed")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     ws, rank, local = dist_env()
     if args.profile:
         run_profile(args, local)
+    elif args.op == "configs":
+        run_configs(args, local)
     elif args.op == "update":
         if args.workload not in ("decode", "spec_decode"):
             args.workload = "decode"

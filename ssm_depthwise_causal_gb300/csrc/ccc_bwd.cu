@@ -403,26 +403,43 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
     }
 }
 
-// dweight[c][k] = sum_{r=0..runs-1} part[r][k][c] (k < W), dbias[c] likewise
-// with row 4: one thread per output, fixed order.
-// The partials are written by the backward grid, which may still be running
-// when this grid becomes resident (programmatic dependent launch): they are
-// read with L2-coherent loads, not through the read-only path.
+// Ordered reduction of the G partial rows part[g][k][c] (k = 0..W-1 taps, 4
+// the bias) into dweight[c][k] and dbias[c].  A CTA owns one k and 32
+// consecutive channels; its warp w (of m = min(8, G)) sums, lane by channel,
+// the contiguous block of rows [w*G/m, (w+1)*G/m) in row order, and warp 0
+// adds the m block sums in block order.  The order of every addition depends
+// only on G and C, so the result is the same bit for bit on every run.  The
+// partials are written by the backward grid, which may still be running when
+// this grid becomes resident (programmatic dependent launch): they are read
+// after griddepcontrol.wait, with L2-coherent loads.
 __global__ void __launch_bounds__(256) reduce_kernel(const float *part, int G, int C, int W, float *dweight,
                                                      float *dbias) {
     grid_dependency_wait();  // the backward's partials
-    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= 5 * C) return;
-    const int k = idx / C, c = idx % C;
-    if (k >= W && k < 4) return;  // tap rows a narrower stencil does not have
-    if (k == 4 && !dbias) return;
-    const float *p = part + static_cast<int64_t>(k) * C + c;
-    float s = __ldcg(p);
-    for (int g = 1; g < G; ++g) s += __ldcg(p + static_cast<int64_t>(g) * 5 * C);
-    if (k < 4) {
-        dweight[W * c + k] = s;
-    } else {
-        dbias[c] = s;
+    __shared__ float blk[kWarpsPerCta][32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int cblocks = (C + 31) / 32;
+    const int k = static_cast<int>(blockIdx.x) / cblocks;
+    const int c = (static_cast<int>(blockIdx.x) % cblocks) * 32 + lane;
+    if ((k >= W && k < 4) || (k == 4 && !dbias)) return;  // whole CTA: no such output
+    const int m = G < kWarpsPerCta ? G : kWarpsPerCta;
+    if (warp < m && c < C) {
+        const int g0 = static_cast<int>(static_cast<int64_t>(warp) * G / m);
+        const int g1 = static_cast<int>(static_cast<int64_t>(warp + 1) * G / m);
+        const int64_t step = static_cast<int64_t>(5) * C;
+        const float *p = part + static_cast<int64_t>(k) * C + c;
+        float s = __ldcg(p + g0 * step);
+        for (int g = g0 + 1; g < g1; ++g) s += __ldcg(p + g * step);
+        blk[warp][lane] = s;
+    }
+    __syncthreads();
+    if (warp == 0 && c < C) {
+        float s = blk[0][lane];
+        for (int w = 1; w < m; ++w) s += blk[w][lane];
+        if (k < 4) {
+            dweight[W * c + k] = s;
+        } else {
+            dbias[c] = s;
+        }
     }
 }
 
@@ -481,7 +498,7 @@ cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t st) {
 cudaError_t launch_reduce(const float *part, int G, int C, int width, float *dweight, float *dbias,
                           cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(5 * static_cast<int64_t>(C), 256)));
+    cfg.gridDim = dim3(static_cast<unsigned>(5 * ceil_div(C, 32)));  // (k, 32-channel block)
     cfg.blockDim = dim3(256);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
