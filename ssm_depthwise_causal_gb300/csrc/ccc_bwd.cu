@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
     // This warp's run: a fixed share of the rows (the same for every slab),
     // so the operand order of every partial sum is fixed.
     RunWalker<kBwdChunk> walk;
-    walk.init(a.cu, a.N, a.rows, run, a.runs, H, true, lane);
+    walk.init(a.cu, a.N, a.rows, run, a.runs, H, true, lane, kBwdWalkRows);
 
     // The rings of history values and dz, carried from one segment to the
     // next along a walk (slot = walk row % RS).

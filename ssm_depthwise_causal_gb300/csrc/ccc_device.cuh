@@ -271,7 +271,9 @@ __device__ __forceinline__ float2 activate2_grad(float2 z, float2 gy) {
 // [cu[n], cu[n+1]) and together they fill [0, T), T = cu[N].  Run r of R
 // takes the rows [r*T/R, (r+1)*T/R) -- equal shares whatever the length mix
 // -- plus the empty sequences positioned in that range (the last run also
-// those at T).  Turning cu_seqlens into these balanced pieces of work
+// those at T).  With a walk cost a > 0 the shares are of cost instead: a
+// sequence costs its rows plus a, and run r takes the rows whose cost lies
+// in [r*K/R, (r+1)*K/R), K = T + a*N.  Turning cu_seqlens into these balanced pieces of work
 // happens at the start of every kernel, on the device, every call (the
 // chunk-map role of FlashInfer "flashinfer.mamba.causal_conv1d_fn",
 // workspace; no scratch and no extra launch here): the warp finds the
@@ -332,9 +334,55 @@ struct RunWalker {
         return cu_at(i);
     }
 
+    // First n in [0, N] with cu[n] + alpha * n > c (cu clamped; true at n = N
+    // whenever c < T + alpha * N): the same 32-way ballot search as in init.
+    __device__ __forceinline__ int first_cost_above(const int32_t *cu, int64_t rows, int64_t c, int alpha,
+                                                    int lane) {
+        int lo = 0, hi = N;
+        while (hi - lo >= 32) {
+            const int step = (hi - lo + 31) / 32;
+            const int idx = min(lo + lane * step, hi);
+            const int64_t key = static_cast<int64_t>(clamp_row(__ldg(cu + idx), rows)) + static_cast<int64_t>(alpha) * idx;
+            const unsigned m = __ballot_sync(kFull, key > c);
+            if (m == 0) {
+                lo = min(lo + 31 * step, hi) + 1;
+            } else {
+                const int j = __ffs(m) - 1;
+                const int new_hi = min(lo + j * step, hi);
+                if (j > 0) lo = min(lo + (j - 1) * step, hi) + 1;
+                hi = new_hi;
+            }
+        }
+        refill(cu, rows, lo, lane);
+        const int64_t key = static_cast<int64_t>(cval) + static_cast<int64_t>(alpha) * (lo + lane);
+        const unsigned m = __ballot_sync(kFull, lane <= hi - lo && key > c);
+        return m ? lo + __ffs(m) - 1 : hi;
+    }
+
+    // The row at cost c of the weighted split, where sequence n costs its
+    // rows plus `alpha` charged at its start: c falls in the last sequence n*
+    // with cu[n*] + alpha * n* <= c, at row cu[n*] + (c - cu[n*] - alpha *
+    // (n* + 1)) clamped to the sequence.  Nondecreasing in c; c >= total
+    // gives T.
+    __device__ __forceinline__ int row_at_cost(const int32_t *cu, int64_t rows, int64_t c, int64_t total, int T,
+                                               int alpha, int lane) {
+        if (c >= total) return T;
+        const int f = first_cost_above(cu, rows, c, alpha, lane);
+        const int ns = f > 0 ? f - 1 : 0;
+        const int s0 = cu_get(cu, rows, ns, lane), e0 = cu_get(cu, rows, ns + 1, lane);
+        const int len = e0 > s0 ? e0 - s0 : 0;
+        int64_t off = c - (static_cast<int64_t>(s0) + static_cast<int64_t>(alpha) * (ns + 1));
+        off = off < 0 ? 0 : (off > len ? len : off);
+        return s0 + static_cast<int>(off);
+    }
+
     // Run `run` of `runs`.  All 32 lanes call with the same arguments.
+    // walk_rows = 0: runs of equal row counts; > 0: runs of equal cost, a
+    // sequence costing its rows plus walk_rows (what a walk's start and end
+    // cost in rows' worth of time), so runs that cross many short sequences
+    // get fewer rows.
     __device__ __forceinline__ void init(const int32_t *cu, int n_seqs, int64_t rows, int run, int runs,
-                                         int hist_rows, bool want_empty, int lane) {
+                                         int hist_rows, bool want_empty, int lane, int walk_rows = 0) {
         N = n_seqs;
         H = hist_rows;
         empties = want_empty;
@@ -348,8 +396,15 @@ struct RunWalker {
             return;
         }
         const int T = cu_get(cu, rows, N, lane);
-        R_lo = static_cast<int>(static_cast<int64_t>(run) * T / runs);
-        R_hi = static_cast<int>(static_cast<int64_t>(run + 1) * T / runs);
+        if (walk_rows > 0) {
+            // Both neighbours of a boundary compute it from the same cost.
+            const int64_t total = static_cast<int64_t>(T) + static_cast<int64_t>(walk_rows) * N;
+            R_lo = row_at_cost(cu, rows, static_cast<int64_t>(run) * total / runs, total, T, walk_rows, lane);
+            R_hi = row_at_cost(cu, rows, static_cast<int64_t>(run + 1) * total / runs, total, T, walk_rows, lane);
+        } else {
+            R_lo = static_cast<int>(static_cast<int64_t>(run) * T / runs);
+            R_hi = static_cast<int>(static_cast<int64_t>(run + 1) * T / runs);
+        }
         // n_a = first n in [0, N) with cu[n+1] >= R_lo (exists: cu[N] = T).
         int lo = 0, hi = N - 1;
         while (hi - lo >= 32) {

@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
     load_taps_w<NV, W>(a.w, a.w_bf16, a.b, a.b_kind, c0, act, wt, bb);
 
     RunWalker<kFwdChunk> walk;
-    walk.init(a.cu, a.N, a.rows, run, a.runs, H, false, lane);
+    walk.init(a.cu, a.N, a.rows, run, a.runs, H, false, lane, kFwdWalkRows);
 
     // The H rows before the current one, oldest first.  (With 3-row batches
     // the window comes back to the same registers every batch; a ring

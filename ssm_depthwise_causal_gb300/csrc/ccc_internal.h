@@ -53,10 +53,16 @@ namespace ccc {
 #ifndef CCC_BWD_PREFETCH
 #define CCC_BWD_PREFETCH 0
 #endif
+#ifndef CCC_FWD_WALK_ROWS
+#define CCC_FWD_WALK_ROWS 0
+#endif
+#ifndef CCC_BWD_WALK_ROWS
+#define CCC_BWD_WALK_ROWS 10
+#endif
 
-// Rows per segment of a walk (RunWalker).  The split into runs is by rows;
-// the segment length only bounds the inner loop (and is a multiple of the
-// backward's batch so a walk's batches stay aligned across segments).
+// Rows per segment of a walk (RunWalker).  The segment length only bounds
+// the inner loop (and is a multiple of the backward's batch so a walk's
+// batches stay aligned across segments).
 constexpr int kFwdChunk = CCC_FWD_CHUNK;
 constexpr int kBwdChunk = CCC_BWD_CHUNK;
 // Channels per lane (8: one 16-byte vector per row).  The backward's
@@ -82,6 +88,15 @@ constexpr int kUpdMinBlocks = CCC_UPD_MIN_BLOCKS;
 // into L2 (cp.async.bulk.prefetch.L2, one row slab per lane); 0 = off.
 constexpr int kFwdPrefetch = CCC_FWD_PREFETCH;
 constexpr int kBwdPrefetch = CCC_BWD_PREFETCH;
+// What a sequence start costs a kernel, in rows' worth of time (the run
+// split balances rows plus this per sequence, RunWalker::init; 0 = rows
+// only).  Measured: a walk of the backward (ring refill, initial history,
+// guarded first and last batches) costs about as much as 8-11 rows, and
+// the weight takes its slowest run on the packed mix from ~3 % above the
+// mean to ~0 (backward 0.5 % faster); a walk of the forward costs 2-3 rows,
+// too little to pay for the two extra searches of a weighted split.
+constexpr int kFwdWalkRows = CCC_FWD_WALK_ROWS;
+constexpr int kBwdWalkRows = CCC_BWD_WALK_ROWS;
 // Backward: stages of the per-lane shared-memory ring (0 = load rows
 // straight into registers).
 constexpr int kBwdRing = CCC_BWD_RING;
