@@ -111,6 +111,7 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
     const bool act = cv < a.C / VEC;
     const bool full = (slab + 1) * 32 * VEC <= a.C;  // warp-uniform: all lanes have channels
     const int c0 = act ? cv * VEC : 0;
+    const int rows_i = static_cast<int>(a.rows);  // host-checked <= 2^31 - 1
 
     float2 wt[W][NV], bb[NV];
     load_taps_w<NV, W>(a.w, a.w_bf16, a.b, a.b_kind, c0, act, wt, bb);
@@ -219,6 +220,24 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
                 px = a.x + static_cast<int64_t>(p_row) * a.xs + c0;
                 pg = a.dy + static_cast<int64_t>(p_row) * a.dys + c0;
                 while (issued < P - 1 && p_row < p_end) issue();
+                if constexpr (kBwdNextWalkPrefetch) {
+                    // Ask L2 for what the next sequence's walk will wait on
+                    // first -- its first P-1 batches of x and dy and its saved
+                    // history -- so that walk starts on L2 hits (lanes 0..2U-1:
+                    // x rows, 2U..4U-1: dy rows, 4U..4U+H-1: history rows).
+                    const int n2 = t.n + 1, s2 = t.e;
+                    if (full && n2 < a.N && s2 < walk.R_hi) {
+                        const int j = lane & (2 * U - 1);
+                        if (lane < 4 * U && j < rows_i - s2) {
+                            const uint16_t *src = lane < 2 * U ? a.x + static_cast<int64_t>(s2 + j) * a.xs
+                                                               : a.dy + static_cast<int64_t>(s2 + j) * a.dys;
+                            prefetch_l2(src + slab * 32 * VEC, 32 * VEC * 2);
+                        } else if (a.hist && lane >= 4 * U && lane < 4 * U + H) {
+                            prefetch_l2(a.hist + (static_cast<int64_t>(n2) * H + (lane - 4 * U)) * a.C + slab * 32 * VEC,
+                                        32 * VEC * 2);
+                        }
+                    }
+                }
             }
         }
         if (!cont) {

@@ -59,6 +59,9 @@ namespace ccc {
 #ifndef CCC_BWD_WALK_ROWS
 #define CCC_BWD_WALK_ROWS 10
 #endif
+#ifndef CCC_BWD_NEXT_WALK_PREFETCH
+#define CCC_BWD_NEXT_WALK_PREFETCH 1
+#endif
 
 // Rows per segment of a walk (RunWalker).  The segment length only bounds
 // the inner loop (and is a multiple of the backward's batch so a walk's
@@ -97,6 +100,9 @@ constexpr int kBwdPrefetch = CCC_BWD_PREFETCH;
 // too little to pay for the two extra searches of a weighted split.
 constexpr int kFwdWalkRows = CCC_FWD_WALK_ROWS;
 constexpr int kBwdWalkRows = CCC_BWD_WALK_ROWS;
+// Backward: at each walk start, ask L2 for the next sequence's first rows
+// and saved history (what its walk start waits on).
+constexpr bool kBwdNextWalkPrefetch = CCC_BWD_NEXT_WALK_PREFETCH != 0;
 // Backward: stages of the per-lane shared-memory ring (0 = load rows
 // straight into registers).
 constexpr int kBwdRing = CCC_BWD_RING;
