@@ -225,8 +225,10 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
                     // first -- its first P-1 batches of x and dy and its saved
                     // history -- so that walk starts on L2 hits (lanes 0..2U-1:
                     // x rows, 2U..4U-1: dy rows, 4U..4U+H-1: history rows).
+                    // (only after a short walk: L2 turns over in about 60 rows'
+                    // time, so rows prefetched before a long walk would be gone)
                     const int n2 = t.n + 1, s2 = t.e;
-                    if (full && n2 < a.N && s2 < walk.R_hi) {
+                    if (full && n2 < a.N && s2 < walk.R_hi && p_end - t.r0 <= kBwdPrefetchWalkMax) {
                         const int j = lane & (2 * U - 1);
                         if (lane < 4 * U && j < rows_i - s2) {
                             const uint16_t *src = lane < 2 * U ? a.x + static_cast<int64_t>(s2 + j) * a.xs

@@ -62,6 +62,9 @@ namespace ccc {
 #ifndef CCC_BWD_NEXT_WALK_PREFETCH
 #define CCC_BWD_NEXT_WALK_PREFETCH 1
 #endif
+#ifndef CCC_BWD_PREFETCH_WALK_MAX
+#define CCC_BWD_PREFETCH_WALK_MAX 96
+#endif
 
 // Rows per segment of a walk (RunWalker).  The segment length only bounds
 // the inner loop (and is a multiple of the backward's batch so a walk's
@@ -103,6 +106,8 @@ constexpr int kBwdWalkRows = CCC_BWD_WALK_ROWS;
 // Backward: at each walk start, ask L2 for the next sequence's first rows
 // and saved history (what its walk start waits on).
 constexpr bool kBwdNextWalkPrefetch = CCC_BWD_NEXT_WALK_PREFETCH != 0;
+// ... only when the current walk loads at most this many rows.
+constexpr int kBwdPrefetchWalkMax = CCC_BWD_PREFETCH_WALK_MAX;
 // Backward: stages of the per-lane shared-memory ring (0 = load rows
 // straight into registers).
 constexpr int kBwdRing = CCC_BWD_RING;
