@@ -34,8 +34,8 @@
  * absent; carry = d_final_state[n][i-len] for the three indices past the end,
  * else 0), dx = dH for the input rows, d_init_state = dH for the three initial
  * values, and dweight[c][k] = sum of dz[j]*h[j+k], dbias[c] = sum of dz[j]
- * over all live tokens.  The weight/bias sums use per-block FP32 partials in
- * workspace combined by an ordered reduction, never atomics (Megatron-Core
+ * over all live tokens.  The weight/bias sums use per-run FP32 partials in
+ * workspace combined by a reduction in a fixed order, never atomics (Megatron-Core
  * "core.ssm.causal_conv1d", assert_causal_conv1d_deterministic), so repeated
  * calls with the same arguments match bit for bit.
  *
@@ -88,9 +88,10 @@ typedef enum {
  * (for_bwd != 0) needs for `rows` packed rows, `n_seqs` sequences and
  * `channels` channels.  Pure host arithmetic; no CUDA call.
  *
- * Forward: always 0.  The kernels split the valid rows into equal runs and
- * find each run's first sequence themselves, on every call (the role of the
- * chunk map of causal_conv1d_fn, workspace), so no scratch is needed.
+ * Forward: always 0.  The kernels split the valid rows into runs (equal rows
+ * in the forward; equal rows plus a fixed cost per sequence in the backward)
+ * and find each run's first sequence themselves, on every call (the role of
+ * the chunk map of causal_conv1d_fn, workspace), so no scratch is needed.
  * Backward: the FP32 partial sums of the ordered weight/bias reduction,
  * R x 5 x C floats with R = 1216 / ceil(C / 256) -- at most about 6.2 MB.
  * The value depends only on `channels` (0 for invalid sizes or an empty
@@ -143,8 +144,8 @@ int ccc_fwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
             void *workspace, size_t workspace_bytes, void *cuda_stream);
 
 /*
- * Backward (cake_causal_conv1d_kcp, Returns: fused dx + deterministic FP32
- * dweight; core.ssm.causal_conv1d, _exchange_initial_states: the state
+ * Backward (cake_causal_conv1d_kcp, Returns: dx from one fused pass and an
+ * FP32 weight gradient that repeats bit for bit; core.ssm.causal_conv1d, _exchange_initial_states: the state
  * gradient is what a preceding fragment receives).
  *
  *  x, rows, C, x_row_stride, weight, w_dtype, width, bias, b_dtype,
