@@ -27,3 +27,22 @@ def test_update_bytes_by_hand():
     assert alg == expect
     assert block == C * (n_live * (3 * 4 + 4 * L) + n_dead * 3 * 2)
     assert n_dead == 2 and np.all(wl.lengths == 3)
+
+
+def test_reference_arm_json_line():
+    """`bench.py --impl reference` (the oracle timed on the host cores) runs
+    without a GPU and prints the contract's JSON line."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "3", "--ref-seconds", "0.2"], capture_output=True, text=True, timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["unit"] == bench.UNIT
+    assert line["value"] > 0 and line["higher_is_better"] is True and line["vs_baseline"] is None
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+    assert line["config"]["C"] == 7168 and line["config"]["rows"] == 65536
