@@ -452,6 +452,42 @@ def check_update_special_cases(orc):
             np.testing.assert_array_equal(st[q, :, n_w:], before[q, :, n_w:])
 
 
+def check_update_impulse(orc):
+    """Closed form of the decode step's read offset and tap order: with the
+    taps one-hot at k (no bias, no activation), token j of a request with
+    accepted count a outputs history value h[j + k] exactly, where h is the
+    slot's positions a-1 .. a+W-3 followed by the request's tokens -- so a
+    wrong read offset, a reversed tap order or a dropped chaining of the
+    step's own tokens changes the output."""
+    L = 8
+    for W in (2, 3, 4):
+        H = W - 1
+        wl = small_case(seed=70 + W, lengths=(1, 3, 4, 2, 0, 5), n_minus_one=0, slots=9, has_init_p=1.0,
+                        width=W)
+        pool = _bf16(np.random.default_rng(70 + W).standard_normal((9, wl.C, L)))
+        cu = wl.cu_seqlens
+        N = len(cu) - 1
+        accepted = torch.tensor([1 + (n % (L - W + 2)) for n in range(N)], dtype=torch.int32)
+        xb = oracle_values(wl.x)
+        pv = oracle_values(pool)
+        for k in range(W):
+            w = torch.zeros((wl.C, W), dtype=torch.float32)
+            w[:, k] = 1.0
+            out, _ = orc.update(wl.x, w, None, cu, pool, wl.cache_indices, accepted, activation=None)
+            for n, q in enumerate(wl.cache_indices.tolist()):
+                s, e = int(cu[n]), int(cu[n + 1])
+                a = int(accepted[n])
+                h = np.concatenate([pv[q, :, a - 1:a - 1 + H].T, xb[s:e]], 0)
+                for j in range(e - s):
+                    np.testing.assert_array_equal(out[s + j], h[j + k], err_msg=f"W={W} k={k} seq {n} token {j}")
+
+
+def oracle_values(t: torch.Tensor) -> np.ndarray:
+    """Exact float64 values of a BF16 tensor (the top 16 bits of an FP32)."""
+    u = _u16(t).astype(np.uint32) << 16
+    return u.view(np.float32).astype(np.float64)
+
+
 def check_update_variants(orc):
     """The decode and speculative chains at widths 2 and 3 and without
     activation."""
@@ -472,5 +508,6 @@ ALL_CHECKS = [
     check_update_decode_chain,
     check_update_speculative_chain,
     check_update_special_cases,
+    check_update_impulse,
     check_update_variants,
 ]
