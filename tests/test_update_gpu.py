@@ -299,3 +299,47 @@ def test_strided_token_rows(cuda_device, layout):
     np.testing.assert_array_equal(_bits(out_pad[:, :C]), _bits(out))
     assert np.all(_bits(out_pad[:, C:]) == H.SENTINEL), "padding columns of out were written"
     np.testing.assert_array_equal(_bits(pool_a), _bits(pool_b))
+
+
+@pytest.mark.parametrize("width", [2, 3, 4])
+def test_one_hot_taps_read_offsets(cuda_device, width):
+    """With the taps one-hot at k, no bias and no activation, token j of a
+    request with accepted count a must output the history value h[j + k]
+    (the slot's positions a-1 .. a+W-3, then the request's tokens) bit for
+    bit: an exact check of the kernels' offset selection and tap order, for
+    every dense pool length the register-block kernel is compiled for, every
+    accepted count, and the channel-contiguous pool."""
+    dev = cuda_device
+    rng = np.random.default_rng(80 + width)
+    H = width - 1
+    for L in list(range(H, 9)) + ["channel"]:
+        layout = "channel" if L == "channel" else "dense"
+        Lr = 7 if L == "channel" else L
+        N, C, slots = 13, 264, 16
+        g = workloads._gen(80 + width, dev)
+        pool = _pool(slots, C, Lr, layout, g, dev)
+        lengths = rng.integers(0, 6, N)
+        x, cu, lengths, rows = _step_inputs(rng, N, C, lengths, dev, g)
+        cache = torch.from_numpy(rng.permutation(slots)[:N].astype(np.int32)).to(dev)
+        acc = torch.from_numpy((1 + np.arange(N) % (Lr - width + 2)).astype(np.int32)).to(dev)
+        before = _bits(pool).astype(np.uint16)
+        xb = _bits(x)
+        cu_np = np.concatenate([[0], np.cumsum(lengths)])
+        for k in range(width):
+            w = torch.zeros((C, width), dtype=torch.float32, device=dev)
+            w[:, k] = 1.0
+            p = pool.clone() if layout == "dense" else _pool(slots, C, Lr, layout, g, dev)
+            p.copy_(pool)
+            out = H_fill(rows, C, dev)
+            ccc.ccc_update(x, w, None, p, cu, cache, acc, out, activation=None)
+            torch.cuda.synchronize()
+            o = _bits(out)
+            for n, q in enumerate(cache.tolist()):
+                s, e = cu_np[n], cu_np[n + 1]
+                a = int(acc[n])
+                h = np.concatenate([before[q, :, a - 1:a - 1 + H].T, xb[s:e]], 0)
+                np.testing.assert_array_equal(o[s:e], h[k:k + (e - s)], err_msg=f"L={L} k={k} seq {n}")
+
+
+def H_fill(rows, C, dev):
+    return H.fill_sentinel(torch.empty((rows, C), dtype=torch.bfloat16, device=dev))
