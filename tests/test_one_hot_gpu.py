@@ -25,10 +25,16 @@ def _eq(a, b):
     return torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
-def test_packed_fwd_bwd_one_hot(cuda_device):
+@pytest.fixture(scope="module")
+def packed(cuda_device):
+    return workloads.packed(device=cuda_device)
+
+
+@pytest.mark.parametrize("W", [4, 3, 2])
+def test_packed_fwd_bwd_one_hot(cuda_device, packed, W):
     dev = cuda_device
-    wl = workloads.packed(device=dev)
-    C, N, rows, W = wl.C, wl.n_seqs, wl.rows, 4
+    wl = packed
+    C, N, rows = wl.C, wl.n_seqs, wl.rows
     Hh = W - 1
     cu = wl.cu_seqlens.cpu().numpy()
     T = int(cu[-1])
