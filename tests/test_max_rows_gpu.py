@@ -51,6 +51,7 @@ def test_rows_at_the_int32_limit(cuda_device):
     dev = cuda_device
     if torch.cuda.get_device_properties(dev).total_memory < 200 * 10 ** 9:
         pytest.skip("needs ~140 GB of device memory")
+    torch.cuda.empty_cache()  # blocks cached by earlier tests in this process
     g = workloads._gen(2024, dev)
     x = dy = out = dx = None
     try:
