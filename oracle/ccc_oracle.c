@@ -110,12 +110,14 @@ static int width_ok(int W) { return W >= 2 && W <= MAX_W; }
 
 /*
  * Forward.  w: [C][W] taps.  state: contiguous [n_slots][C][L] BF16 pool or
- * NULL (zero history, no write-back).  cache: [N] or NULL (only allowed
- * without a pool: all sequences live).  has_init: [N] bytes or NULL (all
- * false).  out: [rows][C] doubles, only rows of sequences written.  hist
- * (optional): [N][W-1][C] BF16, the initial history each nonempty sequence
- * used (zeros for -1 requests).  act: 1 = SiLU, 0 = none.  Returns 0, or -1
- * on an invalid argument.
+ * NULL (zero history, no write-back).  cache: [N] slot IDs, required with a
+ * pool; optional without one (NULL: all sequences live), where only its -1
+ * entries matter: a -1 request outputs zeros with or without a pool.
+ * has_init: [N] bytes or NULL (all false; ignored without a pool).  out:
+ * [rows][C] doubles, only rows of sequences written.  hist (optional):
+ * [N][W-1][C] BF16, the initial history each nonempty sequence used (zeros
+ * for -1 requests).  act: 1 = SiLU, 0 = none.  Returns 0, or -1 on an
+ * invalid argument.
  */
 int oracle_fwd(const uint16_t *x, int64_t rows, int32_t C, int64_t x_stride,
                const double *w, int32_t W, const double *bias, int32_t act,
@@ -135,8 +137,8 @@ int oracle_fwd(const uint16_t *x, int64_t rows, int32_t C, int64_t x_stride,
         const double *wk = w + (int64_t)W * c;
         for (int32_t n = 0; n < N; ++n) {
             const int64_t s = cu[n], e = cu[n + 1], len = e - s;
-            const int32_t q = state ? cache[n] : 0;
-            if (state && q == -1) {
+            const int32_t q = cache ? cache[n] : 0;
+            if (cache && q == -1) {
                 /* -1: zero output, no state access. */
                 for (int64_t j = 0; j < len; ++j) out[(s + j) * out_stride + c] = 0.0;
                 if (hist && len > 0)

@@ -496,6 +496,220 @@ def check_update_variants(orc):
         check_update_speculative_chain(orc, width=W, activation=act)
 
 
+
+# ------------------------------------------------ -1 without a pool --
+
+def check_minus_one_without_pool(orc):
+    """cache_indices given without a pool (FlashInfer causal_conv1d_fn,
+    cache_indices: the -1 sentinel gives a zero output and touches no state):
+    the -1 requests output +0 and contribute nothing to dx, dweight or dbias;
+    every other request is conv1d from zero history (no pool to read)."""
+    for W, act in ((4, "silu"), (3, None), (2, "silu")):
+        wl = small_case(seed=60 + W, lengths=(6, 4, 0, 9, 3, 2), n_minus_one=2, width=W, activation=act)
+        wl = dataclasses.replace(wl, conv_state=None, has_initial_state=None)
+        assert (wl.cache_indices == -1).sum() == 2
+        check_forward_matches_conv1d(orc, wl)
+        check_backward_matches_autograd(orc, wl)
+
+
+# ------------------------------------------------------- brute force --
+
+def _silu(z):
+    """SiLU(z) = z * sigma(z), sigma(z) = 1 / (1 + e^-z)."""
+    return z * (1.0 / (1.0 + math.exp(-z)))
+
+
+def _silu_grad(z):
+    """d/dz [z * sigma(z)] = sigma(z) * (1 + z * (1 - sigma(z)))."""
+    sg = 1.0 / (1.0 + math.exp(-z))
+    return sg * (1.0 + z * (1.0 - sg))
+
+
+def brute_force(x, w, b, cu, pool=None, cache=None, has_init=None, dy=None, d_final=None,
+                activation="silu"):
+    """The method written out as Python float loops (no numpy or torch
+    arithmetic), one sequence and one channel at a time, straight from the
+    definition (FlashInfer causal_conv1d_fn, Parameters; cake_causal_conv1d_kcp,
+    Returns):
+
+    * the history is a Python list: W-1 initial values (pool positions
+      0..W-2 of the request's slot when has_init, zeros otherwise), then the
+      sequence's inputs;
+    * z_j = b + w_0 h[j] + ... + w_{W-1} h[j+W-1] (bias first), y_j = SiLU(z_j);
+    * the pool slot receives the history list's last W-1 entries;
+    * dH = dL/dh by the chain rule, scattered from every token: z_j adds
+      w_k dz_j to dH[j+k], and the final-state gradient d_final[p] lands on
+      h[len+p] (the value written to position p);
+    * dx = dH[W-1:], d_init = dH[:W-1] when the state was read (else 0),
+      dweight[c][k] = sum dz_j h[j+k], dbias[c] = sum dz_j.
+
+    Inputs are nested Python lists of floats (x [rows][C], w [C][W], b [C] or
+    None, pool [slots][C][L], dy [rows][C], d_final [N][W-1][C]).  Returns a
+    dict of nested lists, plus for every floating output the sum of the
+    absolute values of the terms that formed it ("*_mag"), the scale of its
+    rounding error."""
+    rows, C = len(x), len(x[0])
+    W = len(w[0])
+    H = W - 1
+    N = len(cu) - 1
+    act = activation is not None
+    out = [[None] * C for _ in range(rows)]
+    out_mag = [[None] * C for _ in range(rows)]
+    new_pool = None if pool is None else [[list(p) for p in slot] for slot in pool]
+    hist = [[[None] * C for _ in range(H)] for _ in range(N)]
+    res = dict(out=out, out_mag=out_mag, pool=new_pool, hist=hist)
+    if dy is not None:
+        dx = [[None] * C for _ in range(rows)]
+        dx_mag = [[None] * C for _ in range(rows)]
+        d_init = [[[0.0] * C for _ in range(H)] for _ in range(N)]
+        d_init_mag = [[[0.0] * C for _ in range(H)] for _ in range(N)]
+        dweight = [[0.0] * W for _ in range(C)]
+        dweight_mag = [[0.0] * W for _ in range(C)]
+        dbias = [0.0] * C
+        dbias_mag = [0.0] * C
+        res.update(dx=dx, dx_mag=dx_mag, d_init=d_init, d_init_mag=d_init_mag, dweight=dweight,
+                   dweight_mag=dweight_mag, dbias=dbias, dbias_mag=dbias_mag)
+    for n in range(N):
+        s, e = cu[n], cu[n + 1]
+        L = e - s
+        q = None if cache is None else cache[n]
+        if q == -1:                      # zero output, no state access, zero gradient
+            for j in range(L):
+                for c in range(C):
+                    out[s + j][c] = 0.0
+                    out_mag[s + j][c] = 0.0
+                    if dy is not None:
+                        dx[s + j][c] = 0.0
+                        dx_mag[s + j][c] = 0.0
+            if L > 0:
+                for i in range(H):
+                    hist[n][i] = [0.0] * C
+            continue
+        read = pool is not None and has_init is not None and bool(has_init[n])
+        for c in range(C):
+            init = [pool[q][c][i] for i in range(H)] if read else [0.0] * H
+            h = init + [x[s + j][c] for j in range(L)]
+            if L > 0:
+                for i in range(H):
+                    hist[n][i][c] = h[i]
+            bias = 0.0 if b is None else b[c]
+            z = []
+            for j in range(L):
+                acc, mag = bias, abs(bias)
+                for k in range(W):
+                    acc += w[c][k] * h[j + k]
+                    mag += abs(w[c][k] * h[j + k])
+                z.append(acc)
+                out[s + j][c] = _silu(acc) if act else acc
+                out_mag[s + j][c] = mag
+            if new_pool is not None and L > 0:
+                new_pool[q][c][0:H] = h[L:L + H]
+            if dy is None:
+                continue
+            dz = [(_silu_grad(z[j]) if act else 1.0) * dy[s + j][c] for j in range(L)]
+            dH = [0.0] * (L + H)
+            dH_mag = [0.0] * (L + H)
+            if d_final is not None:
+                for p in range(H):
+                    dH[L + p] += d_final[n][p][c]
+                    dH_mag[L + p] += abs(d_final[n][p][c])
+            for j in range(L):
+                for k in range(W):
+                    dH[j + k] += w[c][k] * dz[j]
+                    dH_mag[j + k] += abs(w[c][k] * dz[j])
+            for i in range(L + H):
+                if i >= H:
+                    dx[s + i - H][c] = dH[i]
+                    dx_mag[s + i - H][c] = dH_mag[i]
+                elif read and L > 0:
+                    d_init[n][i][c] = dH[i]
+                    d_init_mag[n][i][c] = dH_mag[i]
+            for j in range(L):
+                for k in range(W):
+                    dweight[c][k] += dz[j] * h[j + k]
+                    dweight_mag[c][k] += abs(dz[j] * h[j + k])
+                dbias[c] += dz[j]
+                dbias_mag[c] += abs(dz[j])
+    return res
+
+
+def _close_to_brute(got, want, mag, what, rel=1e-15):
+    """|oracle - brute force| <= rel * (sum of |terms|), element by element,
+    over the elements the brute force defines (None = not written)."""
+    got = np.asarray(got, dtype=np.float64)
+    for idx in np.ndindex(*got.shape):
+        wv = want
+        mv = mag
+        for i in idx:
+            wv = wv[i]
+            mv = mv[i]
+        if wv is None:
+            assert np.isnan(got[idx]), f"{what}{idx}: written, but the method leaves it alone"
+            continue
+        assert abs(got[idx] - wv) <= rel * mv, f"{what}{idx}: oracle {got[idx]!r} brute force {wv!r}"
+        if wv == 0.0 and mv == 0.0:
+            assert not math.copysign(1.0, got[idx]) < 0, f"{what}{idx}: -0 where +0 is due"
+
+
+def check_brute_force_direct_summation(orc):
+    """The oracle against the brute force above on tiny batches (up to 4
+    sequences of 0 to 6 tokens, C = 8) at every width, with and without
+    SiLU, with a pool, a -1 request, has_initial_state flags and a
+    final-state gradient, and without a pool (-1 requests still zero):
+    values within 1e-15 of the scale of their terms, the pool and the
+    saved history bit for bit."""
+    cases = [
+        # lengths, width, activation, with pool, -1 requests
+        ((5, 0, 6, 2), 4, "silu", True, 1),
+        ((1, 3, 6, 4), 4, None, True, 1),
+        ((6, 2, 0, 5), 3, "silu", True, 1),
+        ((4, 6, 1), 3, None, True, 0),
+        ((2, 5, 6, 0), 2, "silu", True, 1),
+        ((6, 1, 3), 2, None, True, 1),
+        ((3, 6, 0, 4), 4, "silu", False, 1),
+        ((6, 5), 3, "silu", False, 0),
+    ]
+    for t, (lengths, W, act, with_pool, m1) in enumerate(cases):
+        wl = small_case(seed=90 + t, C=8, lengths=lengths, n_minus_one=m1, has_init_p=0.6, width=W,
+                        activation=act, slots=6)
+        if not with_pool:
+            wl = dataclasses.replace(wl, conv_state=None, has_initial_state=None)
+        H = W - 1
+        gen = torch.Generator().manual_seed(100 + t)
+        d_final = torch.randn(wl.n_seqs, H, wl.C, generator=gen, dtype=F64)
+        vals = lambda a: None if a is None else oracle_values(a).tolist()  # noqa: E731
+        ci = None if wl.cache_indices is None else [int(v) for v in wl.cache_indices]
+        hi = None if wl.has_initial_state is None else [bool(v) for v in wl.has_initial_state]
+        bf = brute_force(vals(wl.x), wl.weight.double().tolist(),
+                         None if wl.bias is None else wl.bias.double().tolist(),
+                         [int(v) for v in wl.cu_seqlens], vals(wl.conv_state), ci, hi,
+                         vals(wl.dy), d_final.tolist(), act)
+        out, st, hist = orc.fwd(wl.x, wl.weight, wl.bias, wl.cu_seqlens, wl.conv_state,
+                                wl.cache_indices, wl.has_initial_state, activation=act)
+        tag = f"case {t} (W={W}, {act}, pool={with_pool}): "
+        _close_to_brute(out, bf["out"], bf["out_mag"], tag + "out")
+        if with_pool:
+            np.testing.assert_array_equal(oracle_values_bits(st), np.asarray(bf["pool"]), err_msg=tag + "pool")
+        lens = np.diff(wl.cu_seqlens.numpy())
+        for n in range(wl.n_seqs):
+            if lens[n] > 0:
+                np.testing.assert_array_equal(oracle_values_bits(hist[n]), np.asarray(bf["hist"][n]),
+                                              err_msg=tag + f"saved history {n}")
+        g = orc.bwd(wl.x, wl.weight, wl.bias, wl.cu_seqlens, wl.dy, hist if with_pool else None,
+                    wl.cache_indices, wl.has_initial_state, d_final, activation=act)
+        _close_to_brute(g["dx"], bf["dx"], bf["dx_mag"], tag + "dx")
+        _close_to_brute(g["d_init"], bf["d_init"], bf["d_init_mag"], tag + "d_init")
+        _close_to_brute(g["dweight"], bf["dweight"], bf["dweight_mag"], tag + "dweight")
+        if wl.bias is not None:
+            _close_to_brute(g["dbias"], bf["dbias"], bf["dbias_mag"], tag + "dbias")
+
+
+def oracle_values_bits(bits: np.ndarray) -> np.ndarray:
+    """Exact float64 values of BF16 bit patterns (uint16 arrays)."""
+    u = np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return u.view(np.float32).astype(np.float64)
+
+
 ALL_CHECKS = [
     check_forward_matches_conv1d,
     check_backward_matches_autograd,
@@ -510,4 +724,6 @@ ALL_CHECKS = [
     check_update_special_cases,
     check_update_impulse,
     check_update_variants,
+    check_minus_one_without_pool,
+    check_brute_force_direct_summation,
 ]

@@ -45,6 +45,9 @@ MUTANTS = {
     "update_empty_writes_state": [("if (len == 0) continue;", "if (len < 0) continue;")],
     "update_minus_one_negative_zero": [("out[(s + j) * out_stride + c] = 0.0;\n                    continue;",
                                         "out[(s + j) * out_stride + c] = -0.0;\n                    continue;")],
+    "minus_one_needs_a_pool": [("const int32_t q = cache ? cache[n] : 0;\n            if (cache && q == -1) {",
+                                "const int32_t q = state ? cache[n] : 0;\n            if (state && q == -1) {")],
+    "bwd_dfinal_dropped": [("if (i >= len && d_final) acc = d_final", "if (0) acc = d_final")],
     "update_taps_reversed": [("for (int k = 0; k < W; ++k) z += wk[k] * bf16_to_f64(h[j + k]);",
                               "for (int k = 0; k < W; ++k) z += wk[k] * bf16_to_f64(h[j + W - 1 - k]);")],
 }
