@@ -93,10 +93,12 @@ typedef enum {
  * and find each run's first sequence themselves, on every call (the role of
  * the chunk map of causal_conv1d_fn, workspace), so no scratch is needed.
  * Backward: the FP32 partial sums of the ordered weight/bias reduction,
- * R x 5 x C floats with R = 1216 / ceil(C / 256) -- at most about 6.2 MB.
- * The value depends only on `channels` (0 for invalid sizes or an empty
- * batch), so a workspace sized once can be reused (and captured in a CUDA
- * graph).
+ * R x 5 x C floats (rounded up to 256 bytes) with R = min(1216 / ceil(C /
+ * 256), ceil(rows / 16)), at least 1 -- so at most max(6,225,920, 20 x C)
+ * bytes, and less for small batches.  The value depends only on `rows` and
+ * `channels` (0 for invalid sizes or an empty batch), never on device values,
+ * so a workspace sized once for a shape can be reused (and captured in a CUDA
+ * graph); one sized for more rows also serves fewer.
  */
 size_t ccc_workspace_size(int64_t rows, int32_t n_seqs, int32_t channels, int32_t for_bwd);
 
@@ -195,13 +197,16 @@ int ccc_bwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
  * CCC_NOALLOC_SCRATCH_BYTES compiled into the library, held by every GPU the
  * library is loaded on until the process exits; a shape whose
  * ccc_workspace_size(rows, N, C, 1) exceeds it returns CCC_ERR_WORKSPACE with
- * nothing enqueued (with the current kernels that size never exceeds about
- * 6.2 MB, so every shape fits).  The first call on a device looks up the array's device
- * address (cudaGetSymbolAddress) and caches it; make that first call before
- * any stream capture on the device.  All calls share the array, so calls
- * whose GPU work overlaps (other streams, other host threads on the same
- * device) race and must be serialized by the caller.  Nothing is allocated
- * and no allocating routine is called.
+ * nothing enqueued (that size is at most max(6,225,920, 20 x C) bytes, so
+ * every C up to 838,856 fits).  The first call in a CUDA context (normally
+ * the device's primary context: once per device, and again after a device
+ * reset) looks up the array's device address (cudaGetSymbolAddress) and
+ * caches it under the context; make that first call before any stream
+ * capture in the context.  All calls share the array and it keeps the last
+ * call's contents (nothing in it needs to start at zero), so calls whose GPU
+ * work overlaps (other streams, other host threads on the same device) race
+ * and must be serialized by the caller.  Nothing is allocated and no
+ * allocating routine is called.
  */
 #define CCC_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 

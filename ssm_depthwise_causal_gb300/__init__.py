@@ -92,6 +92,23 @@ def _width(weight: torch.Tensor) -> int:
     return int(weight.shape[1])
 
 
+def _on_current_device(*tensors) -> None:
+    """Every given tensor must be a CUDA tensor on the current device: the
+    library launches on the current device, so a tensor elsewhere would be
+    read through a peer mapping or fault."""
+    cur = None
+    for t in tensors:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"expected CUDA tensors, got one on {t.device}")
+        if cur is None:
+            cur = torch.cuda.current_device()
+        if t.device.index != cur:
+            raise ValueError(f"a tensor is on cuda:{t.device.index} but the current device is cuda:{cur}; "
+                             f"call inside torch.cuda.device({t.device.index})")
+
+
 def _stream(stream) -> ctypes.c_void_p:
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -130,6 +147,8 @@ def ccc_fwd(x, weight, bias, conv_state, cu_seqlens, cache_indices, has_initial_
         raise ValueError("out must match x")
     N = cu_seqlens.numel() - 1
     n_slots, L, st = _pool_args(conv_state, C)
+    _on_current_device(x2, weight, bias, conv_state, cu_seqlens, cache_indices, has_initial_state, o2,
+                       saved_hist, workspace)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = _lib.lib().ccc_fwd(
         _ptr(x2), rows, C, xs, _ptr(weight), _dtype_code(weight), _width(weight),
@@ -151,6 +170,8 @@ def ccc_bwd(x, weight, bias, saved_hist, cu_seqlens, cache_indices, has_initial_
     if (grows, gC) != (rows, C) or (drows, dC) != (rows, C):
         raise ValueError("dy and dx must match x")
     N = cu_seqlens.numel() - 1
+    _on_current_device(x2, weight, bias, saved_hist, cu_seqlens, cache_indices, has_initial_state, g2,
+                       d_final_state, d2, dweight, dbias, d_init_state, workspace)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = _lib.lib().ccc_bwd(
         _ptr(x2), rows, C, xs, _ptr(weight), _dtype_code(weight), _width(weight),
@@ -176,6 +197,8 @@ def ccc_bwd_noalloc(x, weight, bias, saved_hist, cu_seqlens, cache_indices, has_
     if (grows, gC) != (rows, C) or (drows, dC) != (rows, C):
         raise ValueError("dy and dx must match x")
     N = cu_seqlens.numel() - 1
+    _on_current_device(x2, weight, bias, saved_hist, cu_seqlens, cache_indices, has_initial_state, g2,
+                       d_final_state, d2, dweight, dbias, d_init_state)
     rc = _lib.lib().ccc_bwd_noalloc(
         _ptr(x2), rows, C, xs, _ptr(weight), _dtype_code(weight), _width(weight),
         _ptr(bias), _dtype_code(bias), _act_code(activation),
@@ -198,6 +221,7 @@ def ccc_update(x, weight, bias, conv_state, cu_seqlens, cache_indices, num_accep
         raise ValueError("out must match x")
     N = cu_seqlens.numel() - 1
     n_slots, L, st = _pool_args(conv_state, C)
+    _on_current_device(x2, weight, bias, conv_state, cu_seqlens, cache_indices, num_accepted, o2)
     rc = _lib.lib().ccc_update(
         _ptr(x2), rows, C, xs, _ptr(weight), _dtype_code(weight), _width(weight),
         _ptr(bias), _dtype_code(bias), _act_code(activation),
@@ -219,6 +243,7 @@ def ccc_check(rows, cu_seqlens, cache_indices=None, n_slots=0, num_accepted=None
         status = torch.empty(words, dtype=torch.int32, device=cu_seqlens.device)
     if status.dtype != torch.int32 or not status.is_contiguous():
         raise ValueError("status must be a contiguous int32 tensor")
+    _on_current_device(cu_seqlens, cache_indices, num_accepted, status)
     rc = _lib.lib().ccc_check(int(rows), _ptr(cu_seqlens), N, _ptr(cache_indices), int(n_slots),
                               _ptr(num_accepted), int(max_accepted), _ptr(status), status.numel(),
                               _stream(stream))

@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -71,16 +72,20 @@ bool state_layout_ok(int n_slots, int C, int L, int64_t s_slot, int64_t s_c, int
 }
 
 // Per-device launch facts, queried once per device (host calls, no sync).
+// They are properties of the hardware and the compiled kernel, so they stay
+// valid across device resets and contexts.
 struct DeviceFacts {
     int sms = 0;
     int fwd_ctas = 0;
 };
 
-const DeviceFacts &device_facts() {
+DeviceFacts device_facts() {
+    static std::mutex mu;
     static DeviceFacts cached[64];
     static const DeviceFacts fallback{152, ccc::kFwdMinBlocks};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fallback;
+    std::lock_guard<std::mutex> lock(mu);
     DeviceFacts &f = cached[dev];
     if (f.sms == 0) {
         int n = 0;
@@ -91,9 +96,6 @@ const DeviceFacts &device_facts() {
     return f;
 }
 
-int sm_count() { return device_facts().sms; }
-int fwd_ctas() { return device_facts().fwd_ctas; }
-
 }  // namespace
 
 extern "C" {
@@ -102,7 +104,7 @@ size_t ccc_workspace_size(int64_t rows, int32_t n_seqs, int32_t channels, int32_
     if (rows < 0 || n_seqs < 0 || channels <= 0 || channels % 8) return 0;
     if (rows == 0 || n_seqs == 0) return 0;
     if (!for_bwd) return 0;  // the forward splits its work in-kernel: no scratch
-    const int R = ccc::bwd_runs(channels);
+    const int R = ccc::bwd_runs(rows, channels);
     return round_up(static_cast<size_t>(R) * 5 * channels * sizeof(float), kAlignWs);
 }
 
@@ -206,7 +208,10 @@ int ccc_fwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
     a.os = static_cast<int>(out_row_stride);
     a.hist = static_cast<uint16_t *>(saved_hist);
     a.slabs = ccc::slabs_of(C, ccc::kFwdVec);
-    a.runs = ccc::runs_per_slab(static_cast<int64_t>(sm_count()) * fwd_ctas() * ccc::kWarpsPerCta, a.slabs);
+    a.taps_vec = ccc::kFwdVec == 8 && aligned(weight, 16) && (!bias || aligned(bias, 16));
+    const DeviceFacts facts = device_facts();
+    a.runs = ccc::runs_per_slab(static_cast<int64_t>(facts.sms) * facts.fwd_ctas * ccc::kWarpsPerCta * ccc::kFwdWaves,
+                                a.slabs);
     if (ccc::launch_fwd(a, st) != cudaSuccess) return CCC_ERR_CUDA;
     g_last_launches = 1;
     return CCC_OK;
@@ -299,7 +304,8 @@ int ccc_bwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
     a.d_init = d_init_state;
     a.part = static_cast<float *>(workspace);
     a.slabs = ccc::bwd_slabs(C);
-    a.runs = ccc::bwd_runs(C);
+    a.taps_vec = ccc::kBwdVec == 8 && ccc::kBwdRing > 0 && aligned(weight, 16) && (!bias || aligned(bias, 16));
+    a.runs = ccc::bwd_runs(rows, C);
     if (ccc::launch_bwd(a, st) != cudaSuccess) return CCC_ERR_CUDA;
     if (ccc::launch_reduce(a.part, a.runs, C, width, dweight, dbias, st) != cudaSuccess) return CCC_ERR_CUDA;
     g_last_launches = 2;
@@ -372,7 +378,7 @@ int ccc_update(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
     a.out = static_cast<uint16_t *>(out);
     a.os = static_cast<int>(out_row_stride);
     a.slabs = ccc::update_slabs(C);
-    a.groups = ccc::update_groups(N, a.slabs, sm_count());
+    a.groups = ccc::update_groups(N, a.slabs, device_facts().sms);
     if (ccc::launch_update(a, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return CCC_ERR_CUDA;
     g_last_launches = 1;
     return CCC_OK;

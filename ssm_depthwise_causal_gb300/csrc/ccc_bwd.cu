@@ -36,7 +36,8 @@
 // causal_conv1d_cp, weight [D, W]) and the activation (SiLU, or none: then
 // dz = dy); W = 4 with SiLU is the contract above, and "3" reads W-1.
 //
-// Determinism.  The number of runs per slab R is fixed by C only; the warp
+// Determinism.  The number of runs per slab R is fixed by the host
+// arguments rows and C only (never by the device or by device values); the warp
 // with task (slab, run r) walks rows [r*T/R, (r+1)*T/R) (T = cu_seqlens[N])
 // in order and writes partial[r][k][c] for its channels, so every partial sum
 // has a fixed operand order; the reduce kernel then sums the R partials of
@@ -103,6 +104,8 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
     constexpr int RING_WARP = P * U * 2 * 32 * VB;      // ring bytes per warp
     static_assert(P == 0 || kBwdChunk % U == 0, "segments must be whole batches");
     extern __shared__ __align__(16) unsigned char dyn_smem[];
+    __shared__ SeqMeta<kBwdStageSeqs> meta;  // (before any exit: the whole CTA stages it)
+    const bool staged = stage_meta(meta, a.cu, a.N, a.rows, a.cache, a.has_init);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int gw = blockIdx.x * kWarpsPerCta + warp;  // this warp's task
     if (gw >= a.slabs * a.runs) return;               // (whole warp) no task in the last CTA
@@ -114,7 +117,12 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
     const int rows_i = static_cast<int>(a.rows);  // host-checked <= 2^31 - 1
 
     float2 wt[W][NV], bb[NV];
-    load_taps_w<NV, W>(a.w, a.w_bf16, a.b, a.b_kind, c0, act, wt, bb);
+    if (a.taps_vec) {  // through this warp's ring slice (not in use yet)
+        load_taps_staged<NV, W>(a.w, a.w_bf16, a.b, a.b_kind, slab * 32 * VEC, a.C, c0, act, lane,
+                                dyn_smem + warp * RING_WARP, wt, bb);
+    } else {
+        load_taps_w<NV, W>(a.w, a.w_bf16, a.b, a.b_kind, c0, act, wt, bb);
+    }
 
     float2 g[W][NV], gb[NV];  // sum dz*h[j+k], sum dz
 #pragma unroll
@@ -127,7 +135,7 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
     // This warp's run: a fixed share of the rows (the same for every slab),
     // so the operand order of every partial sum is fixed.
     RunWalker<kBwdChunk> walk;
-    walk.init(a.cu, a.N, a.rows, run, a.runs, H, true, lane, kBwdWalkRows);
+    walk.init(a.cu, a.N, a.rows, run, a.runs, H, true, lane, kBwdWalkRows, staged ? meta.cu : nullptr);
 
     // The rings of history values and dz, carried from one segment to the
     // next along a walk (slot = walk row % RS).
@@ -186,8 +194,13 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
     bool cont, next_cont;
     while (walk.next(a.cu, a.rows, lane, t, cont, next_cont)) {
         if (!cont) {  // a new walk: the sequence's flags
-            live = !(a.cache && __ldg(a.cache + t.n) == -1);
-            read_state = a.has_init != nullptr && __ldg(a.has_init + t.n) != 0;
+            if (staged) {
+                live = meta.cache[t.n] != -1;
+                read_state = meta.flag[t.n] != 0;
+            } else {
+                live = !(a.cache && __ldg(a.cache + t.n) == -1);
+                read_state = a.has_init != nullptr && __ldg(a.has_init + t.n) != 0;
+            }
         }
         const int nr = t.nr;
         const int o0 = t.r0 - t.s, L = t.e - t.s;
@@ -496,18 +509,13 @@ cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t st) {
     constexpr int P = kBwdRing;
     constexpr size_t ring_bytes = static_cast<size_t>(P) * kBwdUnroll * 2 * 32 * kBwdVec * 2 * kWarpsPerCta;
     if (ring_bytes > 48 * 1024) {
-        // Opt in to more than 48 KB of dynamic shared memory, once per device
-        // and instantiation.
-        static bool attr_set[64][6] = {};
-        const int slot = (a.width - 2) * 2 + (a.act ? 1 : 0);
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
+        // Opt in to more than 48 KB of dynamic shared memory.  Set on every
+        // launch (a host-side attribute, no device work): no flag shared
+        // between host threads, and nothing stale after a device reset or in
+        // another context.
+        const cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ring_bytes));
         if (e != cudaSuccess) return e;
-        if (dev < 0 || dev >= 64 || !attr_set[dev][slot]) {
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ring_bytes));
-            if (e != cudaSuccess) return e;
-            if (dev >= 0 && dev < 64) attr_set[dev][slot] = true;
-        }
     }
     cfg.dynamicSmemBytes = ring_bytes;
     return cudaLaunchKernelEx(&cfg, kern, a);

@@ -221,6 +221,100 @@ __device__ __forceinline__ void load_taps_w(const void *w, int w_bf16, const voi
     }
 }
 
+// The same taps and bias, read through shared memory when the taps and the
+// bias are 16-byte aligned (VEC = 8).  A lane's taps are VEC*W consecutive
+// values, so a warp's are one contiguous block of its slab: the warp copies
+// that block into `buf` (this warp's own shared memory, >= 32 * VEC * W * 4
+// bytes) with 16-byte loads, consecutive lanes on consecutive chunks (a few
+// fully used 512-byte requests), then each lane reads its own chunks back.
+// Per-lane global loads of the taps touch a different 128-byte line per lane
+// and instruction; with some 40 of them per warp and 16 warps per SM they
+// kept every warp waiting ~10 us at the start of each kernel.  Chunk j of
+// lane l is stored at NC*l + (j ^ swz(l)) so that the read-back is free of
+// bank conflicts (NC = chunks per lane: 2W for FP32 taps, W for BF16).
+template <int NC>
+__device__ __forceinline__ int tap_swizzle(int l) {
+    if constexpr (NC == 8) return l & 7;
+    if constexpr (NC == 4) return (l >> 1) & 3;
+    if constexpr (NC == 2) return (l >> 2) & 1;
+    return 0;
+}
+
+template <int NV, int W, int ESZ>
+__device__ __forceinline__ void stage_taps(const void *w, int slab_c0, int C, int lane, bool act,
+                                           unsigned char *buf, float2 (&wt)[W][NV]) {
+    constexpr int VEC = 2 * NV;
+    constexpr int NC = VEC * W * ESZ / 16;  // 16-byte chunks per lane
+    static_assert(VEC * W * ESZ % 16 == 0, "a lane's taps must be whole 16-byte chunks");
+    const int nch = C - slab_c0 < 32 * VEC ? C - slab_c0 : 32 * VEC;
+    const int bytes = nch * W * ESZ;  // a multiple of 16 (C % 8 == 0)
+    const unsigned char *src = static_cast<const unsigned char *>(w) + static_cast<int64_t>(slab_c0) * W * ESZ;
+    for (int off = lane * 16; off < bytes; off += 32 * 16) {
+        const int g = off >> 4, l = g / NC, j = g % NC;
+        *reinterpret_cast<uint4 *>(buf + 16 * (NC * l + (j ^ tap_swizzle<NC>(l)))) =
+            __ldg(reinterpret_cast<const uint4 *>(src + off));
+    }
+    __syncwarp();
+    uint32_t words[4 * NC];
+#pragma unroll
+    for (int j = 0; j < NC; ++j) {
+        uint4 q = make_uint4(0u, 0u, 0u, 0u);
+        if (act) q = *reinterpret_cast<const uint4 *>(buf + 16 * (NC * lane + (j ^ tap_swizzle<NC>(lane))));
+        words[4 * j] = q.x;
+        words[4 * j + 1] = q.y;
+        words[4 * j + 2] = q.z;
+        words[4 * j + 3] = q.w;
+    }
+    __syncwarp();  // every lane has read before the buffer is reused
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+            float t[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int idx = (2 * v + h) * W + k;  // value index: [channel][tap]
+                if constexpr (ESZ == 4) {
+                    t[h] = __uint_as_float(words[idx]);
+                } else {
+                    const uint32_t u = words[idx >> 1];
+                    t[h] = __uint_as_float((idx & 1) ? (u & 0xffff0000u) : (u << 16));
+                }
+            }
+            wt[k][v] = make_float2(t[0], t[1]);
+        }
+    }
+}
+
+template <int NV, int W>
+__device__ __forceinline__ void load_taps_staged(const void *w, int w_bf16, const void *b, int b_kind, int slab_c0,
+                                                 int C, int c0, bool act, int lane, unsigned char *buf,
+                                                 float2 (&wt)[W][NV], float2 (&bb)[NV]) {
+    static_assert(NV == 4, "staged taps need 8 channels per lane");
+    if (w_bf16) {
+        stage_taps<NV, W, 2>(w, slab_c0, C, lane, act, buf, wt);
+    } else {
+        stage_taps<NV, W, 4>(w, slab_c0, C, lane, act, buf, wt);
+    }
+    // bias: 32 (FP32) or 16 (BF16) contiguous bytes per lane
+#pragma unroll
+    for (int v = 0; v < NV; ++v) bb[v] = f2_zero();
+    if (act && b_kind == 1) {
+        const uint4 lo = __ldg(reinterpret_cast<const uint4 *>(static_cast<const float *>(b) + c0));
+        const uint4 hi = __ldg(reinterpret_cast<const uint4 *>(static_cast<const float *>(b) + c0 + 4));
+        bb[0] = make_float2(__uint_as_float(lo.x), __uint_as_float(lo.y));
+        bb[1] = make_float2(__uint_as_float(lo.z), __uint_as_float(lo.w));
+        bb[2] = make_float2(__uint_as_float(hi.x), __uint_as_float(hi.y));
+        bb[3] = make_float2(__uint_as_float(hi.z), __uint_as_float(hi.w));
+    } else if (act && b_kind == 2) {
+        const uint4 q = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(b) + c0));
+        bb[0] = bf2_to_f2(q.x);
+        bb[1] = bf2_to_f2(q.y);
+        bb[2] = bf2_to_f2(q.z);
+        bb[3] = bf2_to_f2(q.w);
+    }
+}
+
 // Pre-activation of one channel pair for a width-W stencil: the bias, then
 // tap k on history row k (k < W-1, oldest first), then tap W-1 on the
 // current row -- the FMA order of FlashInfer causal_conv1d_fn (bias added
@@ -295,6 +389,42 @@ __device__ __forceinline__ float2 activate2_grad(float2 z, float2 gy) {
 
 // Row indices fit in 32 bits (the host rejects rows > INT32_MAX: cu_seqlens
 // is int32); every address is formed in 64 bits from them.
+//
+// Batches of up to kStageSeqs sequences have their metadata staged in
+// shared memory by the whole CTA at the kernel's start -- the clamped
+// offsets, the slots and the flags, one coalesced load -- so the walker's
+// searches and every per-sequence lookup cost shared-memory latency instead
+// of a chain of dependent global loads before the first row is read.
+// Larger batches read them from global memory as they go.  CAP is a
+// multiple of 128; every member is a multiple of 128 bytes long.
+template <int CAP>
+struct SeqMeta {
+    static_assert(CAP % 128 == 0, "CAP must be a multiple of 128");
+    int cu[CAP + 32];           // clamped to [0, rows]
+    int cache[CAP];             // slot, or -2 without cache_indices
+    unsigned char flag[CAP];    // has_initial_state (0 without it)
+};
+
+// All threads of the CTA call this (it ends with __syncthreads); returns
+// whether the batch's metadata now sits in `m`.
+template <int CAP>
+__device__ __forceinline__ bool stage_meta(SeqMeta<CAP> &m, const int32_t *cu, int N, int64_t rows,
+                                           const int32_t *cache, const uint8_t *has_init) {
+    const bool staged = N > 0 && N <= CAP;
+    if (staged) {
+        for (int i = threadIdx.x; i <= N; i += blockDim.x) {
+            const int v = __ldg(cu + i);
+            m.cu[i] = v < 0 ? 0 : (v > rows ? static_cast<int>(rows) : v);
+            if (i < N) {
+                m.cache[i] = cache ? __ldg(cache + i) : -2;
+                m.flag[i] = has_init ? (__ldg(has_init + i) != 0) : 0;
+            }
+        }
+    }
+    __syncthreads();
+    return staged;
+}
+
 struct Item {
     int n;
     int s, e, r0;
@@ -314,15 +444,21 @@ struct RunWalker {
     bool fresh;      // nothing of sequence n handed out yet
     int cbase;       // lane j caches the clamped cu[cbase + j]
     int cval;
+    const int *scu;  // the clamped offsets in shared memory, or nullptr
 
     __device__ __forceinline__ static int clamp_row(int v, int64_t rows) {
         return v < 0 ? 0 : (v > rows ? static_cast<int>(rows) : v);
     }
 
+    // Clamped cu[i], 0 <= i <= N: from shared memory when staged.
+    __device__ __forceinline__ int cu_val(const int32_t *cu, int64_t rows, int i) const {
+        return scu ? scu[i] : clamp_row(__ldg(cu + i), rows);
+    }
+
     __device__ __forceinline__ void refill(const int32_t *cu, int64_t rows, int base, int lane) {
         cbase = base;
         const int idx = base + lane;
-        cval = idx <= N ? clamp_row(__ldg(cu + idx), rows) : static_cast<int>(rows);
+        cval = idx <= N ? cu_val(cu, rows, idx) : static_cast<int>(rows);
     }
 
     // Clamped cu[i] for cbase <= i < cbase + 32 (all lanes, same i).
@@ -342,7 +478,7 @@ struct RunWalker {
         while (hi - lo >= 32) {
             const int step = (hi - lo + 31) / 32;
             const int idx = min(lo + lane * step, hi);
-            const int64_t key = static_cast<int64_t>(clamp_row(__ldg(cu + idx), rows)) + static_cast<int64_t>(alpha) * idx;
+            const int64_t key = static_cast<int64_t>(cu_val(cu, rows, idx)) + static_cast<int64_t>(alpha) * idx;
             const unsigned m = __ballot_sync(kFull, key > c);
             if (m == 0) {
                 lo = min(lo + 31 * step, hi) + 1;
@@ -380,9 +516,12 @@ struct RunWalker {
     // walk_rows = 0: runs of equal row counts; > 0: runs of equal cost, a
     // sequence costing its rows plus walk_rows (what a walk's start and end
     // cost in rows' worth of time), so runs that cross many short sequences
-    // get fewer rows.
+    // get fewer rows.  `staged`: the clamped offsets (stage_meta), or
+    // nullptr to read cu_seqlens from global memory.
     __device__ __forceinline__ void init(const int32_t *cu, int n_seqs, int64_t rows, int run, int runs,
-                                         int hist_rows, bool want_empty, int lane, int walk_rows = 0) {
+                                         int hist_rows, bool want_empty, int lane, int walk_rows = 0,
+                                         const int *staged = nullptr) {
+        scu = staged;
         N = n_seqs;
         H = hist_rows;
         empties = want_empty;
@@ -410,7 +549,7 @@ struct RunWalker {
         while (hi - lo >= 32) {
             const int step = (hi - lo + 31) / 32;
             const int idx = min(lo + lane * step, hi);
-            const int v = clamp_row(__ldg(cu + idx + 1), rows);
+            const int v = cu_val(cu, rows, idx + 1);
             const unsigned m = __ballot_sync(kFull, v >= R_lo);
             if (m == 0) {
                 lo = min(lo + 31 * step, hi) + 1;

@@ -97,6 +97,9 @@ template <int VEC, int U, int W, bool ACT>
 __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const FwdArgs a) {
     constexpr int NV = VEC / 2;
     constexpr int H = W - 1;  // history rows
+    __shared__ SeqMeta<kFwdStageSeqs> meta;  // (before any exit: the whole CTA stages it)
+    __shared__ __align__(16) unsigned char taps_buf[kWarpsPerCta][32 * VEC * W * 4];
+    const bool staged = stage_meta(meta, a.cu, a.N, a.rows, a.cache, a.has_init);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int gw = blockIdx.x * kWarpsPerCta + warp;  // this warp's task
     if (gw >= a.slabs * a.runs) return;               // (whole warp) no task in the last CTA
@@ -108,10 +111,15 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
     const int rows_i = static_cast<int>(a.rows);  // host-checked <= 2^31 - 1
 
     float2 wt[W][NV], bb[NV];
-    load_taps_w<NV, W>(a.w, a.w_bf16, a.b, a.b_kind, c0, act, wt, bb);
+    if (a.taps_vec) {
+        load_taps_staged<NV, W>(a.w, a.w_bf16, a.b, a.b_kind, slab * 32 * VEC, a.C, c0, act, lane, taps_buf[warp],
+                                wt, bb);
+    } else {
+        load_taps_w<NV, W>(a.w, a.w_bf16, a.b, a.b_kind, c0, act, wt, bb);
+    }
 
     RunWalker<kFwdChunk> walk;
-    walk.init(a.cu, a.N, a.rows, run, a.runs, H, false, lane, kFwdWalkRows);
+    walk.init(a.cu, a.N, a.rows, run, a.runs, H, false, lane, kFwdWalkRows, staged ? meta.cu : nullptr);
 
     // The H rows before the current one, oldest first.  (With 3-row batches
     // the window comes back to the same registers every batch; a ring
@@ -124,8 +132,13 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
     bool has_init_n = false;
     while (walk.next(a.cu, a.rows, lane, t, cont, more)) {
         if (!cont) {  // a new sequence (or the run's first rows): its slot and flag
-            q = a.cache ? __ldg(a.cache + t.n) : -2;
-            has_init_n = a.has_init != nullptr && __ldg(a.has_init + t.n) != 0;
+            if (staged) {
+                q = meta.cache[t.n];
+                has_init_n = meta.flag[t.n] != 0;
+            } else {
+                q = a.cache ? __ldg(a.cache + t.n) : -2;
+                has_init_n = a.has_init != nullptr && __ldg(a.has_init + t.n) != 0;
+            }
         }
         const int nr = t.nr;
         if (nr <= 0) continue;

@@ -44,6 +44,9 @@ namespace ccc {
 #ifndef CCC_BWD_TARGET_WARPS
 #define CCC_BWD_TARGET_WARPS 1216
 #endif
+#ifndef CCC_BWD_MIN_RUN_ROWS
+#define CCC_BWD_MIN_RUN_ROWS 16
+#endif
 #ifndef CCC_BWD_RING
 #define CCC_BWD_RING 3
 #endif
@@ -64,6 +67,15 @@ namespace ccc {
 #endif
 #ifndef CCC_BWD_PREFETCH_WALK_MAX
 #define CCC_BWD_PREFETCH_WALK_MAX 96
+#endif
+#ifndef CCC_FWD_WAVES
+#define CCC_FWD_WAVES 1
+#endif
+#ifndef CCC_FWD_STAGE_SEQS
+#define CCC_FWD_STAGE_SEQS 1024
+#endif
+#ifndef CCC_BWD_STAGE_SEQS
+#define CCC_BWD_STAGE_SEQS 256
 #endif
 
 // Rows per segment of a walk (RunWalker).  The segment length only bounds
@@ -113,12 +125,24 @@ constexpr int kBwdPrefetchWalkMax = CCC_BWD_PREFETCH_WALK_MAX;
 constexpr int kBwdRing = CCC_BWD_RING;
 // Backward warps the work split is sized for: 152 SMs x 1 resident CTA x 8
 // warps, i.e. one full wave on GB300.  Fixed, not queried, so the reduction
-// order -- and with it every bit of dweight / dbias -- depends only on
-// (rows, N, C).
+// order -- and with it every bit of dweight / dbias -- depends only on the
+// host arguments (rows, C), never on the device or on device values.
 constexpr int kBwdTargetWarps = CCC_BWD_TARGET_WARPS;
+// ... but never more runs per slab than one per this many rows of the
+// batch: a small batch then writes (and the reduce re-reads) a few partial
+// rows instead of ~1216 / slabs of them.
+constexpr int kBwdMinRunRows = CCC_BWD_MIN_RUN_ROWS;
 
 // Warps per CTA of the forward and backward kernels.
 constexpr int kWarpsPerCta = 8;
+// Forward: resident waves of warps the rows are split over (1: every warp
+// has one run and the grid is one wave).
+constexpr int kFwdWaves = CCC_FWD_WAVES;
+// Sequences whose offsets, slots and flags a CTA stages in shared memory
+// (multiples of 128).  The backward's is small so that its copy ring plus
+// this stays within the 100 KB shared-memory carveout.
+constexpr int kFwdStageSeqs = CCC_FWD_STAGE_SEQS;
+constexpr int kBwdStageSeqs = CCC_BWD_STAGE_SEQS;
 
 struct FwdArgs {
     const uint16_t *x;
@@ -143,6 +167,7 @@ struct FwdArgs {
     int os;
     uint16_t *hist;
     int slabs, runs;     // work split (see runs_per_slab)
+    int taps_vec;        // weight and bias 16-byte aligned: taps read through shared memory
 };
 
 struct BwdArgs {
@@ -169,6 +194,7 @@ struct BwdArgs {
     float *d_init;
     float *part;  // [runs][5][C]: rows 0..W-1 taps, row 4 bias
     int slabs, runs;
+    int taps_vec;  // weight and bias 16-byte aligned: taps read through shared memory
 };
 
 // The speculative / single-token decode update (ccc_update.cu).
@@ -217,10 +243,15 @@ inline int runs_per_slab(int64_t target_warps, int slabs) {
 
 // Backward task split: slabs of 32*VEC channels times `runs` runs per slab;
 // runs is also the number of FP32 partial rows per channel.  Both depend
-// only on C.
+// only on the host arguments rows and C: runs = min(1216 / slabs,
+// ceil(rows / kBwdMinRunRows)), at least 1.
 inline int bwd_slabs(int C) { return slabs_of(C, kBwdVec); }
 
-inline int bwd_runs(int C) { return runs_per_slab(kBwdTargetWarps, bwd_slabs(C)); }
+inline int bwd_runs(int64_t rows, int C) {
+    const int by_width = runs_per_slab(kBwdTargetWarps, bwd_slabs(C));
+    const int64_t by_rows = ceil_div(rows < 1 ? 1 : rows, kBwdMinRunRows);
+    return by_rows < by_width ? static_cast<int>(by_rows) : by_width;
+}
 
 cudaError_t launch_fwd(const FwdArgs &a, cudaStream_t st);
 cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t st);

@@ -11,20 +11,26 @@
 // The scratch is one file-scope __device__ array of kScratchBytes.  Every GPU
 // on which the library's module is loaded holds it until the process exits.
 // The name `g_scratch` in host code is only a host-side stand-in for the
-// device symbol, never a device address: the address is fetched once per
-// device with cudaGetSymbolAddress (with that device current) on the first
-// call made on that device, and cached.  That first call on a device should
-// therefore come before any stream capture on it.
+// device symbol, never a device address.  The device address is looked up
+// with cudaGetSymbolAddress, with the caller's device current, at set-up:
+// the first call made in a CUDA context (normally the device's primary
+// context, so once per device; again after a device reset, which replaces
+// that context, or in any other context the caller makes current), and
+// cached under the context's unique ID, which the driver never reuses within
+// a process.  That first call in a context should come before any stream
+// capture in it.
 //
 // Every call uses the same array and leaves its contents behind for the next
 // call.  Nothing in it has to start at zero: the backward writes every
 // partial sum before the reduction reads it.  The backward's scratch is
-// R x 5 x C floats with R x ceil(C / 256) <= 1216, at most about 6.2 MB, so
-// every shape fits; the size check stays as a guard.  Two calls whose work
-// overlaps on the GPU (different streams, or different host threads on the
-// same device) race on the array; callers must serialize them.
+// R x 5 x C floats (R partial rows, R x ceil(C / 256) <= 1216 and R >= 1), at
+// most max(6,225,920, 20 x C) bytes, so every C up to 838,856 fits; larger C
+// is refused before any CUDA call.  Two calls whose work overlaps on the GPU
+// (different streams, or different host threads on the same device) race on
+// the array; callers must serialize them.
 #include <mutex>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "ccc.h"
@@ -32,24 +38,79 @@
 namespace {
 
 constexpr size_t kScratchBytes = CCC_NOALLOC_SCRATCH_BYTES;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
-std::mutex g_setup_mu;
-void *g_scratch_addr[kMaxDevices] = {};
+// Driver entry points, fetched through the runtime so the library needs no
+// link against the driver library.
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
 
-// Device address of g_scratch on the current device (set up on first use).
+std::once_flag g_entry_once;
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+void load_entry_points() {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f);
+}
+
+// Unique ID of the context current on this thread; 0 when there is none yet
+// (or it cannot be read).
+unsigned long long current_context_id() {
+    std::call_once(g_entry_once, load_entry_points);
+    if (!g_ctx_get_current || !g_ctx_get_id) return 0;
+    CUcontext ctx = nullptr;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    unsigned long long id = 0;
+    if (g_ctx_get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Cache of looked-up addresses: context ID -> device address of g_scratch.
+struct Entry {
+    unsigned long long ctx_id;
+    void *addr;
+};
+constexpr int kCacheEntries = 64;
+std::mutex g_cache_mu;
+Entry g_cache[kCacheEntries] = {};
+int g_cache_next = 0;
+
+// Device address of g_scratch in the current context (looked up on the
+// first call in each context).
 int scratch_address(void **out) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CCC_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_setup_mu);
-    if (g_scratch_addr[dev] == nullptr) {
+    unsigned long long id = current_context_id();
+    if (id == 0) {
+        // No context on this thread yet: the lookup below makes the current
+        // device's primary context current (as any runtime call would).
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || p == nullptr) return CCC_ERR_CUDA;
-        g_scratch_addr[dev] = p;
+        id = current_context_id();
+        if (id == 0) {  // cannot key it: use the fresh lookup uncached
+            *out = p;
+            return CCC_OK;
+        }
     }
-    *out = g_scratch_addr[dev];
+    std::lock_guard<std::mutex> lock(g_cache_mu);
+    for (const Entry &e : g_cache) {
+        if (e.ctx_id == id) {
+            *out = e.addr;
+            return CCC_OK;
+        }
+    }
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || p == nullptr) return CCC_ERR_CUDA;
+    g_cache[g_cache_next] = Entry{id, p};
+    g_cache_next = (g_cache_next + 1) % kCacheEntries;
+    *out = p;
     return CCC_OK;
 }
 

@@ -165,18 +165,32 @@ def assert_bf16_close(gpu_bits: np.ndarray, ref64: np.ndarray, what: str, rows=N
             f"(bits {int(gpu_bits[i]):#06x}) ref {r32[i]!r}")
 
 
-def assert_reduction_close(gpu: np.ndarray, ref: np.ndarray, abs_terms: np.ndarray, what: str):
+def assert_reduction_close(gpu: np.ndarray, ref: np.ndarray, abs_terms: np.ndarray, what: str) -> dict:
+    """The FP32 reduction tolerance.  Returns how the elements passed:
+    ``n`` elements, ``floor_only`` of them within 1e-6 sum|terms| but not
+    within 1e-4 |ref| (sums that cancel to near zero), ``max_rel`` the
+    largest |err| / |ref| and ``max_err_terms`` the largest
+    |err| / sum|terms|."""
     err = np.abs(gpu.astype(np.float64) - ref)
-    ok = (err <= 1e-4 * np.abs(ref)) | (err <= 1e-6 * abs_terms)
+    rel_ok = err <= 1e-4 * np.abs(ref)
+    floor_ok = err <= 1e-6 * abs_terms
+    ok = rel_ok | floor_ok
     if not ok.all():
         i = np.argwhere(~ok)[0]
         raise AssertionError(f"{what}: {int((~ok).sum())} elements out of tolerance; first at "
                              f"{tuple(i)}: gpu {gpu[tuple(i)]!r} ref {ref[tuple(i)]!r} "
                              f"sum|terms| {abs_terms[tuple(i)]!r}")
+    with np.errstate(divide="ignore", invalid="ignore"):
+        rel = np.where(ref != 0, err / np.abs(ref), np.where(err == 0, 0.0, np.inf))
+        per_terms = np.where(abs_terms > 0, err / abs_terms, 0.0)
+    return dict(n=int(err.size), floor_only=int((~rel_ok).sum()), max_rel=float(rel.max(initial=0.0)),
+                max_err_terms=float(per_terms.max(initial=0.0)))
 
 
-def compare(wl_cpu, ref, gpu: dict, *, backward=True, rows_checked=None, chans=None):
-    """Compare GPU results (numpy, same channel subset) against the oracle."""
+def compare(wl_cpu, ref, gpu: dict, *, backward=True, rows_checked=None, chans=None) -> dict:
+    """Compare GPU results (numpy, same channel subset) against the oracle.
+    Returns the reduction statistics of dweight (and dbias) for the
+    backward (see assert_reduction_close)."""
     T = int(wl_cpu.cu_seqlens[-1])
     live = live_rows(wl_cpu)
     m1 = minus_one_rows(wl_cpu)
@@ -194,17 +208,18 @@ def compare(wl_cpu, ref, gpu: dict, *, backward=True, rows_checked=None, chans=N
     np.testing.assert_array_equal(gpu["hist"][ne], ref["hist"][ne], err_msg="saved_hist")
     assert np.all(gpu["hist"][~ne] == SENTINEL), "saved_hist rows of empty sequences were written"
     if not backward:
-        return
+        return {}
     assert_bf16_close(gpu["dx"][lv], ref["dx"][lv], "dx", lv, chans)
     assert np.all(gpu["dx"][mo] == 0), "-1 rows of dx must be +0"
     assert np.all(gpu["dx"][pad] == SENTINEL), "padding rows of dx were written"
-    assert_reduction_close(gpu["dweight"], ref["dweight"], ref["abs_dweight"], "dweight")
+    stats = {"dweight": assert_reduction_close(gpu["dweight"], ref["dweight"], ref["abs_dweight"], "dweight")}
     if gpu.get("dbias") is not None:
-        assert_reduction_close(gpu["dbias"], ref["dbias"], ref["abs_dbias"], "dbias")
+        stats["dbias"] = assert_reduction_close(gpu["dbias"], ref["dbias"], ref["abs_dbias"], "dbias")
     if gpu.get("d_init") is not None:
         di, rdi = gpu["d_init"].astype(np.float64), ref["d_init"]
         ok = np.abs(di - rdi) <= 1e-4 * np.abs(rdi) + 1e-5
         assert ok.all(), f"d_init_state: {int((~ok).sum())} elements out of tolerance"
+    return stats
 
 
 def gpu_numpy(res: GpuResult, chans=None) -> dict:

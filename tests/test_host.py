@@ -51,12 +51,16 @@ def test_workspace_size_rules(lib):
     assert ws(16384, 4, 4096, False) == 0
     assert ws(65536, 200, 7168, False) == 0
     assert ws(1 << 24, 100000, 8192, False) == 0
-    # backward: the FP32 partial sums, R = 1216 // ceil(C / 256) rows of
-    # [5][C] floats, rounded up to 256 bytes; independent of rows and N
-    for C in (8, 256, 264, 4096, 7168, 8192):
-        R = max(1, 1216 // ((C + 255) // 256))
-        assert ws(65536, 200, C, True) == (R * 5 * C * 4 + 255) // 256 * 256, C
-        assert ws(16, 1, C, True) == ws(1 << 24, 9999, C, True)
+    # backward: the FP32 partial sums, R = min(1216 // ceil(C / 256),
+    # ceil(rows / 16)) (at least 1) rows of [5][C] floats, rounded up to 256
+    # bytes; a function of rows and C, not of N
+    for C in (8, 256, 264, 4096, 7168, 8192, 400000):
+        for rows in (1, 15, 16, 17, 1040, 16384, 65536, 1 << 24):
+            R = min(max(1, 1216 // ((C + 255) // 256)), (rows + 15) // 16)
+            assert ws(rows, 200, C, True) == (R * 5 * C * 4 + 255) // 256 * 256, (C, rows)
+            assert ws(rows, 1, C, True) == ws(rows, 9999, C, True)
+    # the tiny training batch (1040 rows, C 256): 65 partial rows, not 1216
+    assert ws(1040, 4, 256, True) == 65 * 5 * 256 * 4
     # degenerate / invalid
     assert ws(0, 4, 4096, True) == 0
     assert ws(100, 0, 4096, False) == 0
@@ -64,12 +68,26 @@ def test_workspace_size_rules(lib):
     assert ws(-1, 4, 4096, False) == 0
 
 
-def test_noalloc_scratch_holds_every_shape(lib):
-    """The backward's scratch is R * 5 * C floats with R * ceil(C/256) <= 1216,
-    at most ~6.2 MB: every shape fits the fixed array behind
-    ccc_bwd_noalloc."""
-    worst = max(ccc.ccc_workspace_size(1 << 20, 1000, C, True) for C in range(8, 70000, 8))
-    assert worst <= _lib.NOALLOC_SCRATCH_BYTES
+def test_noalloc_scratch_bound(lib):
+    """The backward's scratch is R * 5 * C floats with R * ceil(C/256) <= 1216
+    and R >= 1: at most max(6,225,920, 20 * C) bytes, so the fixed array
+    behind ccc_bwd_noalloc holds every C up to 838,856."""
+    for C in list(range(8, 70000, 8)) + [311288, 311296, 311304, 500000, 838856]:
+        need = ccc.ccc_workspace_size(1 << 20, 1000, C, True)
+        assert need <= max(6225920, (20 * C + 255) // 256 * 256), C
+        assert need <= _lib.NOALLOC_SCRATCH_BYTES, C
+    assert ccc.ccc_workspace_size(1 << 20, 1000, 838864, True) > _lib.NOALLOC_SCRATCH_BYTES
+
+
+def test_noalloc_refuses_wider_than_its_array(lib):
+    """C = 838,864 needs 16,777,280 bytes of partials, more than the array:
+    refused with CCC_ERR_WORKSPACE by the size check, which runs before any
+    CUDA call or pointer check (the fake addresses are never used)."""
+    C = 838864
+    f = lib.ccc_bwd_noalloc
+    rc = f(P(A), 64, C, C, P(A * 2), 0, 4, None, -1, 1, None, P(A * 3), 1, None, None,
+           P(A * 4), C, None, P(A * 5), C, P(A * 6), None, None, None)
+    assert rc == E_WS
 
 
 P = ctypes.c_void_p
@@ -219,3 +237,18 @@ def test_check_host_errors(lib):
     assert chk(10, cu, 2, None, 0, None, 0, st, 0, None) == E_WS
     assert chk(10, cu, 2, None, 0, None, 0, P(0x10008), 1, None) == E_ALIAS  # status inside cu_seqlens
     assert chk(10, cu, 2, cache, 64, None, 0, P(0x1fffc), 3, None) == E_ALIAS  # bitmap runs into cache
+
+
+def test_binding_rejects_tensors_off_the_current_device(lib):
+    """The binding hands raw pointers to kernels launched on the current CUDA
+    device, so it refuses CPU tensors (and tensors on another GPU) before
+    calling the library."""
+    import torch
+    x = torch.zeros((16, 8), dtype=torch.bfloat16)
+    w = torch.zeros((8, 4))
+    cu = torch.tensor([0, 16], dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        ccc.ccc_fwd(x, w, None, None, cu, None, None, torch.empty_like(x))
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        ccc.ccc_bwd_noalloc(x, w, None, None, cu, None, None, x, None, torch.empty_like(x),
+                            torch.empty((8, 4)), None, None)
