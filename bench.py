@@ -7,11 +7,14 @@ lognormal-length sequences, weight BF16, bias FP32), through the C ABI.
 Prints one JSON line (rank 0).  ``value`` is valid tokens per second of the
 whole job (all ranks; each rank is an independent replica on its own GPU),
 timed with CUDA events on the launch stream over K steps after W warm-up
-steps, inputs resident in HBM.  ``e2e`` is the same metric with the inputs
+steps, inputs resident in HBM; each step replays the ccc_fwd and ccc_bwd
+calls, each captured once as a CUDA graph.  ``e2e`` is the same metric with the inputs
 copied from pinned host memory and the results copied back inside every
 step.  ``roofline`` is for the backward call (the dominant kernel),
 ``cpu_baseline`` times the float64 oracle on a bounded sample of the same
-workload on this host's cores.
+workload on this host's cores.  ``configs`` (one GPU) holds the forward and
+forward + backward throughput of every workload (tiny, dense, packed,
+serving, long, and long as chained fragments), device-timed the same way.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -161,15 +164,19 @@ class ClockSampler:
 # ---------------------------------------------------------------- traffic --
 
 # The sources that decide what the backward launch does (kernel, helpers,
-# launch configuration): a change to any of them makes recorded counters stale.
-BWD_SOURCES = ("ccc_bwd.cu", "ccc_device.cuh", "ccc_internal.h", "ccc_api.cu")
+# launch configuration) and the build script (compiler flags): a change to
+# any of them, or extra compiler flags in the environment, makes recorded
+# counters stale.
+BWD_SOURCES = ("ssm_depthwise_causal_gb300/csrc/ccc_bwd.cu", "ssm_depthwise_causal_gb300/csrc/ccc_device.cuh",
+               "ssm_depthwise_causal_gb300/csrc/ccc_internal.h", "ssm_depthwise_causal_gb300/csrc/ccc_api.cu",
+               "ssm_depthwise_causal_gb300/_build.py")
 
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "ssm_depthwise_causal_gb300", "csrc")
     for f in BWD_SOURCES:
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    h.update(os.environ.get("CCC_EXTRA_NVCC_FLAGS", "").strip().encode())
     return h.hexdigest()
 
 
@@ -228,6 +235,52 @@ def time_oracle(wl, target_s=12.0):
 
 # ------------------------------------------------------------------ runs --
 
+def headline_config(wl, ws):
+    """The `config` object of the headline line (the same for both arms)."""
+    return {"workload": "packed C=7168 rows=65536 N=200 lognormal lengths, fwd+bwd",
+            "rows": wl.rows, "C": wl.C, "n_seqs": wl.n_seqs, "valid_tokens": wl.valid_tokens,
+            "weight": "bf16", "bias": "f32", "state": "none",
+            "l2": "inputs larger than L2 (x, dy, out, dx 939 MB each)",
+            "parallelism": f"replicas x{ws}"}
+
+
+def capture(call, stream, reps=1):
+    """`reps` back-to-back calls of `call` (which enqueues library calls on
+    `stream` and returns how many kernels they launched) captured as one
+    CUDA graph, after one eager call outside the capture; returns the graph
+    and the kernel launches one replay makes."""
+    with torch.cuda.stream(stream):
+        call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        launches = sum(call() for _ in range(reps))
+    torch.cuda.synchronize()
+    return g, launches
+
+
+def time_graph(g, stream):
+    """Milliseconds of one replay of graph `g` on `stream`, between two CUDA
+    events."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def time_calls(call, stream, K, W):
+    """Milliseconds per call of K back-to-back calls of `call`, captured as
+    one CUDA graph and replayed once, after W warm-up calls (their own
+    graph); returns (ms per call, kernel launches in the timed region)."""
+    g_w, _ = capture(call, stream, reps=W)
+    g_k, n = capture(call, stream, reps=K)
+    time_graph(g_w, stream)
+    return time_graph(g_k, stream) / K, n
+
+
 def run_reference(args, ws, rank):
     from ssm_depthwise_causal_gb300 import workloads
     if rank != 0:
@@ -246,8 +299,7 @@ def run_reference(args, ws, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wl.valid_tokens / v,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": "packed C=7168 rows=65536 N=200 lognormal lengths, fwd+bwd",
-                   "rows": wl.rows, "C": wl.C, "n_seqs": wl.n_seqs, "valid_tokens": wl.valid_tokens},
+        "config": headline_config(wl, args.gpus),
         "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -265,6 +317,7 @@ def run_ours(args, ws, rank, local):
 
     wl = workloads.packed(device=dev)
     T, C, N, rows = wl.valid_tokens, wl.C, wl.n_seqs, wl.rows
+    config = headline_config(wl, ws)
     out = torch.empty_like(wl.x)
     dx = torch.empty_like(wl.x)
     hist = torch.empty((N, 3, C), dtype=torch.bfloat16, device=dev)
@@ -273,53 +326,41 @@ def run_ours(args, ws, rank, local):
     ws_f = torch.empty(max(1, ccc.ccc_workspace_size(rows, N, C, False)), dtype=torch.uint8, device=dev)
     ws_b = torch.empty(ccc.ccc_workspace_size(rows, N, C, True), dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
-    launches = {"n": 0}
 
-    def step(x, dy, s):
-        ccc.ccc_fwd(x, wl.weight, wl.bias, None, wl.cu_seqlens, None, None, out, hist, ws_f, stream=s)
-        launches["n"] += ccc.last_launch_count()
-        ccc.ccc_bwd(x, wl.weight, wl.bias, hist, wl.cu_seqlens, None, None, dy, None, dx, dw, db, None,
-                    ws_b, stream=s)
-        launches["n"] += ccc.last_launch_count()
+    def fwd_call():
+        ccc.ccc_fwd(wl.x, wl.weight, wl.bias, None, wl.cu_seqlens, None, None, out, hist, ws_f, stream=stream)
+        return ccc.last_launch_count()
 
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            step(wl.x, wl.dy, stream)
-    torch.cuda.synchronize()
+    def bwd_call():
+        ccc.ccc_bwd(wl.x, wl.weight, wl.bias, hist, wl.cu_seqlens, None, None, wl.dy, None, dx, dw, db, None,
+                    ws_b, stream=stream)
+        return ccc.last_launch_count()
 
-    # ---- device-resident timing
+    def step_call():
+        return fwd_call() + bwd_call()
+
+    # K steps (ccc_fwd then ccc_bwd) captured as one CUDA graph -- the
+    # library neither allocates nor synchronizes, so its calls capture -- and
+    # replayed once between two events, after W warm-up steps (their own
+    # graph); then K of each call alone (forward / backward split and the
+    # backward's roofline).
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    g_warm, _ = capture(step_call, stream, reps=args.warmup)
+    g_step, gpu_launches = capture(step_call, stream, reps=K)
+    time_graph(g_warm, stream)
     clocks = ClockSampler(local)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
-    launches["n"] = 0
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        t_start.record(stream)
-        for k in range(K):
-            ev[k][0].record(stream)
-            ccc.ccc_fwd(wl.x, wl.weight, wl.bias, None, wl.cu_seqlens, None, None, out, hist, ws_f, stream=stream)
-            launches["n"] += ccc.last_launch_count()
-            ev[k][1].record(stream)
-            ccc.ccc_bwd(wl.x, wl.weight, wl.bias, hist, wl.cu_seqlens, None, None, wl.dy, None, dx, dw, db,
-                        None, ws_b, stream=stream)
-            launches["n"] += ccc.last_launch_count()
-            ev[k][2].record(stream)
-        t_end.record(stream)
-    torch.cuda.synchronize()
+    elapsed_ms = time_graph(g_step, stream)
+    fwd_ms, _ = time_calls(fwd_call, stream, K, args.warmup)
+    bwd_ms, _ = time_calls(bwd_call, stream, K, args.warmup)
     clk = clocks.stop()
     if dist:
         dist.barrier()
-    elapsed_ms = job_max(t_start.elapsed_time(t_end), dist, dev)
-    gpu_launches = launches["n"]
-    fwd_ms = statistics.mean(ev[k][0].elapsed_time(ev[k][1]) for k in range(K))
-    bwd_ms = statistics.mean(ev[k][1].elapsed_time(ev[k][2]) for k in range(K))
+    elapsed_ms = job_max(elapsed_ms, dist, dev)
     ms_step = elapsed_ms / K
     value = job_throughput(ws, T, ms_step)
     fb, bb = algorithmic_bytes(wl)
@@ -417,17 +458,25 @@ def run_ours(args, ws, rank, local):
         tok_s, threads, sample, _ = time_oracle(wl, target_s=args.ref_seconds)
         cpu = {"value": tok_s, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample}
 
+    # ---- every workload's forward and forward + backward (one GPU)
+    configs = None
+    if ws == 1 and not args.no_configs:
+        wl = out = dx = hist = sets = hx = hdy = hout = hdx = None  # the headline's buffers are done
+        torch.cuda.empty_cache()
+        cclk = ClockSampler(local)
+        cclk.start()
+        rows_c, launches_c = time_configs(dev, K, args.warmup)
+        configs = {"unit_gbs": "GB/s (algorithmic bytes / CUDA-event time)", "peak": peak,
+                   "peak_kind": peak_kind, "steps": K, "warmup": args.warmup, "workloads": rows_c,
+                   "gpu_launches": launches_c, "clocks": cclk.stop()}
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "storage_dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": "packed C=7168 rows=65536 N=200 lognormal lengths, fwd+bwd",
-                       "rows": rows, "C": C, "n_seqs": N, "valid_tokens": T,
-                       "weight": "bf16", "bias": "f32", "state": "none",
-                       "l2": "inputs larger than L2 (x, dy, out, dx 939 MB each)",
-                       "parallelism": f"replicas x{ws}"},
+            "config": config,
             "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
             "fwd_tokens_per_s": ws * T / (fwd_ms / 1e3),
             "effective_gbs": eff_gbs, "frac_of_nominal_8tbs": eff_gbs / NOMINAL_HBM_GBS,
@@ -444,6 +493,7 @@ def run_ours(args, ws, rank, local):
                     "link": link},
             "gpu_launches": gpu_launches,
             "clocks": clk,
+            "configs": configs,
         }
         print(json.dumps(line), flush=True)
     if dist:
@@ -523,10 +573,12 @@ def run_update(args, ws, rank, local):
     def call(x, s):
         ccc.ccc_update(x, wl.weight, wl.bias, pool, wl.cu_seqlens, wl.cache_indices, acc, out, stream=s)
 
+    # the step captured once as a CUDA graph and replayed
+    g_upd, n_upd = capture(lambda: (call(wl.x, stream), ccc.last_launch_count())[1], stream)
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             flush.zero_()
-            call(wl.x, stream)
+            g_upd.replay()
     torch.cuda.synchronize()
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
@@ -535,13 +587,12 @@ def run_update(args, ws, rank, local):
         dist.barrier()
     clocks.start()
     time.sleep(0.3)
-    launches = 0
+    launches = K * n_upd
     with torch.cuda.stream(stream):
         for k in range(K):
             flush.zero_()
             ev[k][0].record(stream)
-            call(wl.x, stream)
-            launches += ccc.last_launch_count()
+            g_upd.replay()
             ev[k][1].record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -629,12 +680,22 @@ def run_profile(args, local):
 CONFIG_WORKLOADS = ("tiny", "dense", "packed", "serving", "long")
 
 
-def time_fragment_chain(ccc, wl, out, dx, flush, stream, args):
+def working_set_bytes(wl):
+    """Device bytes one step touches: x and out (and dy, dx when training),
+    plus the pool."""
+    n = wl.x.numel() * 2 * (4 if wl.training else 2)
+    if wl.conv_state is not None:
+        n += wl.conv_state.numel() * 2
+    return n
+
+
+def time_fragment_chain(ccc, wl, out, dx, stream, steps, warmup):
     """The long document as `fragments` consecutive calls chained through a
     one-slot pool (forward: fragment k reads the state fragment k-1 wrote;
     backward in reverse, d_init_state of fragment k as d_final_state of
     fragment k-1): device time of the forward chain and of the backward chain
-    (the host-side sum of the per-fragment dweight is not included)."""
+    (the host-side sum of the per-fragment dweight is not included).  Steps
+    run back to back: every tensor is far larger than L2."""
     dev = wl.x.device
     T, C, F = wl.rows, wl.C, wl.fragments
     Lf = T // F
@@ -649,59 +710,54 @@ def time_fragment_chain(ccc, wl, out, dx, flush, stream, args):
     part = lambda t, k: t[k * Lf:(k + 1) * Lf]  # noqa: E731
 
     def fwd_chain():
+        n = 0
         for k in range(F):
             ccc.ccc_fwd(part(wl.x, k), wl.weight, wl.bias, pool, cu_f, cache, flags[k], part(out, k), hists[k],
                         None, stream=stream)
+            n += ccc.last_launch_count()
+        return n
 
     def bwd_chain():
-        carry = None
+        n, carry = 0, None
         for k in reversed(range(F)):
             ccc.ccc_bwd(part(wl.x, k), wl.weight, wl.bias, hists[k], cu_f, cache, flags[k], part(wl.dy, k), carry,
                         part(dx, k), dws[k], None, d_init[k], ws_f, stream=stream)
+            n += ccc.last_launch_count()
             carry = d_init[k]
+        return n
 
-    K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            fwd_chain()
-            bwd_chain()
-        for k in range(K):
-            flush.zero_()
-            ev[k][0].record(stream)
-            fwd_chain()
-            ev[k][1].record(stream)
-            bwd_chain()
-            ev[k][2].record(stream)
-    torch.cuda.synchronize()
-    f_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
-    b_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
-    return {"split_fragments": F, "split_fwd_ms": f_ms, "split_bwd_ms": b_ms, "split_step_ms": f_ms + b_ms,
-            "split_step_tokens_per_s": T / ((f_ms + b_ms) / 1e3)}
+    s_ms, n = time_calls(lambda: fwd_chain() + bwd_chain(), stream, steps, warmup)
+    f_ms, _ = time_calls(fwd_chain, stream, steps, warmup)
+    b_ms, _ = time_calls(bwd_chain, stream, steps, warmup)
+    return {"split_fragments": F, "split_fwd_ms": f_ms, "split_bwd_ms": b_ms, "split_step_ms": s_ms,
+            "split_step_tokens_per_s": T / (s_ms / 1e3)}, n
 
 
-def run_configs(args, local):
+def time_configs(dev, steps, warmup):
     """Forward and (for training workloads) forward + backward of every
-    workload, device-timed: K steps after W warm-up steps, L2 flushed before
-    each timed step, one JSON line with a row per workload.  A forward with a
-    pool updates it in place every step; the work per step does not depend
-    on the values, so the pool is not restored between steps."""
+    workload through the C ABI, each call captured once as a CUDA graph and
+    replayed, device-timed with CUDA events on the launch stream: `steps`
+    steps after `warmup` warm-up steps.  A workload whose
+    step touches more than twice the L2 size runs its steps back to back
+    (as the headline does); a smaller one (the tiny batch) is preceded by an
+    L2 flush (a write of twice the L2 size) every step.  A forward with a
+    pool updates it in place every step; the work per step does not depend on
+    the values, so the pool is not restored between steps.  Returns (rows,
+    kernel launches in the timed regions)."""
     import ssm_depthwise_causal_gb300 as ccc
     from ssm_depthwise_causal_gb300 import workloads
 
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    ccc._lib.lib()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
-    peak, peak_kind = measured_peak()
+    flush = None
+    peak, _ = measured_peak()
     stream = torch.cuda.Stream(device=dev)
     rows_out = []
-    clocks = ClockSampler(local)
-    clocks.start()
     for name in CONFIG_WORKLOADS:
         wl = workloads.WORKLOADS[name](device=dev)
         T, C, N, rows = wl.valid_tokens, wl.C, wl.n_seqs, wl.rows
+        flushed = working_set_bytes(wl) < 2 * l2
+        if flushed and flush is None:
+            flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
         out = torch.empty_like(wl.x)
         hist = torch.empty((N, 3, C), dtype=torch.bfloat16, device=dev)
         state = wl.conv_state
@@ -715,51 +771,84 @@ def run_configs(args, local):
         def fwd():
             ccc.ccc_fwd(wl.x, wl.weight, wl.bias, state, wl.cu_seqlens, wl.cache_indices, wl.has_initial_state,
                         out, hist, None, stream=stream)
+            return ccc.last_launch_count()
 
         def bwd():
             ccc.ccc_bwd(wl.x, wl.weight, wl.bias, hist, wl.cu_seqlens, wl.cache_indices, wl.has_initial_state,
                         wl.dy, None, dx, dw, db, None, ws_b, stream=stream)
+            return ccc.last_launch_count()
 
-        K = args.steps
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-        with torch.cuda.stream(stream):
-            for _ in range(args.warmup):
-                fwd()
-                if wl.training:
-                    bwd()
-            for k in range(K):
-                flush.zero_()
-                ev[k][0].record(stream)
-                fwd()
-                ev[k][1].record(stream)
-                if wl.training:
-                    bwd()
-                ev[k][2].record(stream)
-        torch.cuda.synchronize()
-        fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+        K = steps
+        if flushed:  # L2 flushed before each call, each call (a one-call graph) between its own two events
+            g_f, n_f = capture(fwd, stream)
+            g_b, n_b = capture(bwd, stream) if wl.training else (None, 0)
+            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+            with torch.cuda.stream(stream):
+                for _ in range(warmup):
+                    g_f.replay()
+                    if g_b is not None:
+                        g_b.replay()
+                for k in range(K):
+                    flush.zero_()
+                    ev[k][0].record(stream)
+                    g_f.replay()
+                    ev[k][1].record(stream)
+                    if g_b is not None:
+                        flush.zero_()
+                        ev[k][2].record(stream)
+                        g_b.replay()
+                        ev[k][3].record(stream)
+            torch.cuda.synchronize()
+            fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+            bwd_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev) if g_b is not None else None
+            step_ms = fwd_ms + bwd_ms if g_b is not None else None
+            timed_launches = K * (n_f + n_b)
+        else:  # back to back: K calls in one graph between two events (as the headline)
+            fwd_ms, timed_launches = time_calls(fwd, stream, K, warmup)
+            bwd_ms = step_ms = None
+            if wl.training:
+                bwd_ms, _ = time_calls(bwd, stream, K, warmup)
+                step_ms, timed_launches = time_calls(lambda: fwd() + bwd(), stream, K, warmup)
         fb, bb = algorithmic_bytes(wl)
         row = {"workload": wl.name, "valid_tokens": T, "C": C, "n_seqs": N,
+               "l2": ("flushed before every timed call, each call between its own events" if flushed
+                      else "inputs larger than L2, K calls back to back in one CUDA graph between two events"),
                "fwd_ms": fwd_ms, "fwd_tokens_per_s": T / (fwd_ms / 1e3),
                "fwd_gbs": fb / (fwd_ms / 1e3) / 1e9, "fwd_frac": fb / (fwd_ms / 1e3) / 1e9 / peak,
                "fwd_algorithmic_bytes": fb}
         if wl.training:
-            bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
-            step_ms = fwd_ms + bwd_ms
             row.update({"bwd_ms": bwd_ms, "bwd_gbs": bb / (bwd_ms / 1e3) / 1e9,
                         "bwd_frac": bb / (bwd_ms / 1e3) / 1e9 / peak, "bwd_algorithmic_bytes": bb,
                         "step_ms": step_ms, "step_tokens_per_s": T / (step_ms / 1e3),
                         "step_gbs": (fb + bb) / (step_ms / 1e3) / 1e9,
                         "step_frac": (fb + bb) / (step_ms / 1e3) / 1e9 / peak})
+        rows_out.append((row, timed_launches))
         if wl.training and getattr(wl, "fragments", 1) > 1:
-            row.update(time_fragment_chain(ccc, wl, out, dx, flush, stream, args))
-        rows_out.append(row)
+            chain, n_chain = time_fragment_chain(ccc, wl, out, dx, stream, steps, warmup)
+            row.update(chain)
+            rows_out[-1] = (row, timed_launches + n_chain)
         wl = out = hist = state = dx = dw = db = ws_b = None  # free this workload's tensors
         torch.cuda.empty_cache()
+    flush = None
+    torch.cuda.empty_cache()
+    return [r for r, _ in rows_out], sum(n for _, n in rows_out)
+
+
+def run_configs(args, local):
+    """--op configs: the per-workload table alone, one JSON line."""
+    import ssm_depthwise_causal_gb300 as ccc
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    ccc._lib.lib()
+    peak, peak_kind = measured_peak()
+    clocks = ClockSampler(local)
+    clocks.start()
+    rows, launches = time_configs(dev, args.steps, args.warmup)
     clk = clocks.stop()
     print(json.dumps({"op": "configs", "steps": args.steps, "warmup": args.warmup, "peak": peak,
                       "peak_kind": peak_kind, "unit_gbs": "GB/s (algorithmic bytes / CUDA-event time)",
-                      "l2": "flushed before every timed step", "data": "synthetic",
-                      "configs": rows_out, "clocks": clk}), flush=True)
+                      "data": "synthetic", "configs": rows, "gpu_launches": launches, "clocks": clk}), flush=True)
 
 
 def main():
@@ -771,6 +860,8 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=12.0,
                     help="approximate CPU seconds of one oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload table (forward and forward+backward of every workload)")
     ap.add_argument("--profile", action="store_true",
                     help="run warm-up + one step of --workload only (for ncu captures)")
     ap.add_argument("--workload", default="packed",

@@ -438,41 +438,64 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
 }
 
 // Ordered reduction of the G partial rows part[g][k][c] (k = 0..W-1 taps, 4
-// the bias) into dweight[c][k] and dbias[c].  A CTA owns one k and 32
-// consecutive channels; its warp w (of m = min(8, G)) sums, lane by channel,
-// the contiguous block of rows [w*G/m, (w+1)*G/m) in row order, and warp 0
-// adds the m block sums in block order.  The order of every addition depends
+// the bias) into dweight[c][k] and dbias[c].  A CTA owns one k and 128
+// consecutive channels, 4 per lane (16-byte loads); its warp w (of
+// m = min(8, G)) sums the contiguous block of rows [w*G/m, (w+1)*G/m) in row
+// order -- the rows are loaded kRedBatch at a time before they are added, so
+// a warp waits for one round trip per batch, not per row -- and warp 0 adds
+// the m block sums in block order.  The order of every addition depends
 // only on G and C, so the result is the same bit for bit on every run.  The
 // partials are written by the backward grid, which may still be running when
 // this grid becomes resident (programmatic dependent launch): they are read
 // after griddepcontrol.wait, with L2-coherent loads.
+constexpr int kRedChannels = 128;  // channels per CTA (4 per lane)
+constexpr int kRedBatch = 8;       // rows loaded before they are added
+
+__device__ __forceinline__ float4 f4_add(float4 a, float4 b) {
+    return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+
 __global__ void __launch_bounds__(256) reduce_kernel(const float *part, int G, int C, int W, float *dweight,
                                                      float *dbias) {
     grid_dependency_wait();  // the backward's partials
-    __shared__ float blk[kWarpsPerCta][32];
+    __shared__ float4 blk[kWarpsPerCta][32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int cblocks = (C + 31) / 32;
+    const int cblocks = (C + kRedChannels - 1) / kRedChannels;
     const int k = static_cast<int>(blockIdx.x) / cblocks;
-    const int c = (static_cast<int>(blockIdx.x) % cblocks) * 32 + lane;
+    const int c = (static_cast<int>(blockIdx.x) % cblocks) * kRedChannels + 4 * lane;  // C % 8 == 0: c..c+3 < C
     if ((k >= W && k < 4) || (k == 4 && !dbias)) return;  // whole CTA: no such output
     const int m = G < kWarpsPerCta ? G : kWarpsPerCta;
     if (warp < m && c < C) {
         const int g0 = static_cast<int>(static_cast<int64_t>(warp) * G / m);
         const int g1 = static_cast<int>(static_cast<int64_t>(warp + 1) * G / m);
-        const int64_t step = static_cast<int64_t>(5) * C;
-        const float *p = part + static_cast<int64_t>(k) * C + c;
-        float s = __ldcg(p + g0 * step);
-        for (int g = g0 + 1; g < g1; ++g) s += __ldcg(p + g * step);
+        const int64_t step = static_cast<int64_t>(5) * C / 4;  // one partial row, in float4
+        const float4 *p = reinterpret_cast<const float4 *>(part + static_cast<int64_t>(k) * C + c);
+        float4 s = __ldcg(p + g0 * step);
+        for (int g = g0 + 1; g < g1; g += kRedBatch) {
+            float4 v[kRedBatch];
+#pragma unroll
+            for (int u = 0; u < kRedBatch; ++u)
+                v[u] = g + u < g1 ? __ldcg(p + (g + u) * step) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int u = 0; u < kRedBatch; ++u)
+                if (g + u < g1) s = f4_add(s, v[u]);
+        }
         blk[warp][lane] = s;
     }
     __syncthreads();
     if (warp == 0 && c < C) {
-        float s = blk[0][lane];
-        for (int w = 1; w < m; ++w) s += blk[w][lane];
+        float4 s = blk[0][lane];
+        for (int w = 1; w < m; ++w) s = f4_add(s, blk[w][lane]);
         if (k < 4) {
-            dweight[W * c + k] = s;
-        } else {
-            dbias[c] = s;
+            dweight[W * c + k] = s.x;
+            dweight[W * (c + 1) + k] = s.y;
+            dweight[W * (c + 2) + k] = s.z;
+            dweight[W * (c + 3) + k] = s.w;
+        } else {  // (dbias is only 4-byte aligned)
+            dbias[c] = s.x;
+            dbias[c + 1] = s.y;
+            dbias[c + 2] = s.z;
+            dbias[c + 3] = s.w;
         }
     }
 }
@@ -527,7 +550,7 @@ cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t st) {
 cudaError_t launch_reduce(const float *part, int G, int C, int width, float *dweight, float *dbias,
                           cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(5 * ceil_div(C, 32)));  // (k, 32-channel block)
+    cfg.gridDim = dim3(static_cast<unsigned>(5 * ceil_div(C, kRedChannels)));  // (k, 128-channel block)
     cfg.blockDim = dim3(256);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
