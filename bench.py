@@ -271,6 +271,39 @@ def time_graph(g, stream):
     return e0.elapsed_time(e1)
 
 
+def time_flushed(call, flush, stream, K, W):
+    """Per-call time of `call` (a one-launch-per-call L2-resident step) with
+    L2 flushed before every call: K (flush, call) pairs captured as one CUDA
+    graph, minus K flushes alone (also one graph), divided by K -- no event or
+    launch gap between calls.  Also returns the per-call time with each call
+    between its own two events after a flush (that includes the launch
+    latency), and the kernel launches of the K calls."""
+    def pair():
+        flush.zero_()
+        return call()
+
+    def flush_only():
+        flush.zero_()
+        return 0
+
+    g_w, _ = capture(pair, stream, reps=W)
+    g_pair, n = capture(pair, stream, reps=K)
+    g_flush, _ = capture(flush_only, stream, reps=K)
+    time_graph(g_w, stream)
+    time_graph(g_flush, stream)
+    ms = (time_graph(g_pair, stream) - time_graph(g_flush, stream)) / K
+    g_one, _ = capture(call, stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    with torch.cuda.stream(stream):
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            g_one.replay()
+            b.record(stream)
+    torch.cuda.synchronize()
+    return ms, statistics.mean(a.elapsed_time(b) for a, b in ev), n
+
+
 def time_calls(call, stream, K, W):
     """Milliseconds per call of K back-to-back calls of `call`, captured as
     one CUDA graph and replayed once, after W warm-up calls (their own
@@ -573,30 +606,16 @@ def run_update(args, ws, rank, local):
     def call(x, s):
         ccc.ccc_update(x, wl.weight, wl.bias, pool, wl.cu_seqlens, wl.cache_indices, acc, out, stream=s)
 
-    # the step captured once as a CUDA graph and replayed
-    g_upd, n_upd = capture(lambda: (call(wl.x, stream), ccc.last_launch_count())[1], stream)
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            flush.zero_()
-            g_upd.replay()
-    torch.cuda.synchronize()
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    step = lambda: (call(wl.x, stream), ccc.last_launch_count())[1]  # noqa: E731
     clocks = ClockSampler(local)
     if dist:
         dist.barrier()
     clocks.start()
     time.sleep(0.3)
-    launches = K * n_upd
-    with torch.cuda.stream(stream):
-        for k in range(K):
-            flush.zero_()
-            ev[k][0].record(stream)
-            g_upd.replay()
-            ev[k][1].record(stream)
-    torch.cuda.synchronize()
+    ms, ms_events, launches = time_flushed(step, flush, stream, K, args.warmup)
     clk = clocks.stop()
-    ms = job_max(statistics.mean(a.elapsed_time(b) for a, b in ev), dist, dev)
+    ms = job_max(ms, dist, dev)
     value = job_throughput(ws, T, ms)
     alg, block = update_algorithmic_bytes(wl)
     peak, peak_kind = measured_peak()
@@ -626,7 +645,10 @@ def run_update(args, ws, rank, local):
                        "pool": list(pool.shape), "l2": "flushed before every timed step (working set < L2)",
                        "parallelism": f"replicas x{ws}"},
             "effective_gbs": gbs,
-            "roofline": {"kernel": "update_kernel (one launch per step)", "bound": "hbm", "achieved": gbs,
+            "timing": "K (L2 flush, step) pairs in one CUDA graph minus K flushes alone, per step; "
+                      "ms_per_step_events: each step between its own events after a flush",
+            "ms_per_step_events": ms_events,
+            "roofline": {"kernel": "update_block_kernel (one launch per step)", "bound": "hbm", "achieved": gbs,
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": gbs / peak,
                          "traffic": None, "algorithmic_bytes_per_launch": alg,
                          "state_block_bytes_per_launch": block},
@@ -779,30 +801,14 @@ def time_configs(dev, steps, warmup):
             return ccc.last_launch_count()
 
         K = steps
-        if flushed:  # L2 flushed before each call, each call (a one-call graph) between its own two events
-            g_f, n_f = capture(fwd, stream)
-            g_b, n_b = capture(bwd, stream) if wl.training else (None, 0)
-            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
-            with torch.cuda.stream(stream):
-                for _ in range(warmup):
-                    g_f.replay()
-                    if g_b is not None:
-                        g_b.replay()
-                for k in range(K):
-                    flush.zero_()
-                    ev[k][0].record(stream)
-                    g_f.replay()
-                    ev[k][1].record(stream)
-                    if g_b is not None:
-                        flush.zero_()
-                        ev[k][2].record(stream)
-                        g_b.replay()
-                        ev[k][3].record(stream)
-            torch.cuda.synchronize()
-            fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
-            bwd_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev) if g_b is not None else None
-            step_ms = fwd_ms + bwd_ms if g_b is not None else None
-            timed_launches = K * (n_f + n_b)
+        if flushed:  # L2 flushed before every call (see time_flushed)
+            fwd_ms, _, n_f = time_flushed(fwd, flush, stream, K, warmup)
+            bwd_ms = step_ms = None
+            timed_launches = n_f
+            if wl.training:
+                bwd_ms, _, n_b = time_flushed(bwd, flush, stream, K, warmup)
+                step_ms = fwd_ms + bwd_ms
+                timed_launches += n_b
         else:  # back to back: K calls in one graph between two events (as the headline)
             fwd_ms, timed_launches = time_calls(fwd, stream, K, warmup)
             bwd_ms = step_ms = None
@@ -811,8 +817,8 @@ def time_configs(dev, steps, warmup):
                 step_ms, timed_launches = time_calls(lambda: fwd() + bwd(), stream, K, warmup)
         fb, bb = algorithmic_bytes(wl)
         row = {"workload": wl.name, "valid_tokens": T, "C": C, "n_seqs": N,
-               "l2": ("flushed before every timed call, each call between its own events" if flushed
-                      else "inputs larger than L2, K calls back to back in one CUDA graph between two events"),
+               "l2": ("flushed before every call: K (flush, call) pairs in one CUDA graph minus K flushes"
+                      if flushed else "inputs larger than L2, K calls back to back in one CUDA graph between two events"),
                "fwd_ms": fwd_ms, "fwd_tokens_per_s": T / (fwd_ms / 1e3),
                "fwd_gbs": fb / (fwd_ms / 1e3) / 1e9, "fwd_frac": fb / (fwd_ms / 1e3) / 1e9 / peak,
                "fwd_algorithmic_bytes": fb}

@@ -225,8 +225,9 @@ __device__ __forceinline__ void load_taps_w(const void *w, int w_bf16, const voi
 // bias are 16-byte aligned (VEC = 8).  A lane's taps are VEC*W consecutive
 // values, so a warp's are one contiguous block of its slab: the warp copies
 // that block into `buf` (this warp's own shared memory, >= 32 * VEC * W * 4
-// bytes) with 16-byte loads, consecutive lanes on consecutive chunks (a few
-// fully used 512-byte requests), then each lane reads its own chunks back.
+// bytes) with 16-byte cp.async copies, consecutive lanes on consecutive
+// chunks (a few fully used 512-byte requests), then each lane reads its own
+// chunks back; the bias is read directly (whole 16-byte vectors).
 // Per-lane global loads of the taps touch a different 128-byte line per lane
 // and instruction; with some 40 of them per warp and 16 warps per SM they
 // kept every warp waiting ~10 us at the start of each kernel.  Chunk j of
@@ -240,9 +241,12 @@ __device__ __forceinline__ int tap_swizzle(int l) {
     return 0;
 }
 
+// The copy itself, as one cp.async commit group per lane (global -> shared
+// without registers), so it can be issued early and overlap other work;
+// read_staged_taps reads the block back once every lane has waited for its
+// group (cp.async.wait_group) and the warp has synchronized.
 template <int NV, int W, int ESZ>
-__device__ __forceinline__ void stage_taps(const void *w, int slab_c0, int C, int lane, bool act,
-                                           unsigned char *buf, float2 (&wt)[W][NV]) {
+__device__ __forceinline__ void issue_taps_copy(const void *w, int slab_c0, int C, int lane, uint32_t buf) {
     constexpr int VEC = 2 * NV;
     constexpr int NC = VEC * W * ESZ / 16;  // 16-byte chunks per lane
     static_assert(VEC * W * ESZ % 16 == 0, "a lane's taps must be whole 16-byte chunks");
@@ -251,10 +255,15 @@ __device__ __forceinline__ void stage_taps(const void *w, int slab_c0, int C, in
     const unsigned char *src = static_cast<const unsigned char *>(w) + static_cast<int64_t>(slab_c0) * W * ESZ;
     for (int off = lane * 16; off < bytes; off += 32 * 16) {
         const int g = off >> 4, l = g / NC, j = g % NC;
-        *reinterpret_cast<uint4 *>(buf + 16 * (NC * l + (j ^ tap_swizzle<NC>(l)))) =
-            __ldg(reinterpret_cast<const uint4 *>(src + off));
+        cp_async<16>(buf + static_cast<uint32_t>(16 * (NC * l + (j ^ tap_swizzle<NC>(l)))), src + off, true);
     }
-    __syncwarp();
+    cp_async_commit();
+}
+
+template <int NV, int W, int ESZ>
+__device__ __forceinline__ void read_staged_taps(const unsigned char *buf, int lane, bool act, float2 (&wt)[W][NV]) {
+    constexpr int VEC = 2 * NV;
+    constexpr int NC = VEC * W * ESZ / 16;
     uint32_t words[4 * NC];
 #pragma unroll
     for (int j = 0; j < NC; ++j) {
@@ -265,7 +274,6 @@ __device__ __forceinline__ void stage_taps(const void *w, int slab_c0, int C, in
         words[4 * j + 2] = q.z;
         words[4 * j + 3] = q.w;
     }
-    __syncwarp();  // every lane has read before the buffer is reused
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
 #pragma unroll
@@ -286,6 +294,57 @@ __device__ __forceinline__ void stage_taps(const void *w, int slab_c0, int C, in
     }
 }
 
+// The synchronous form: the warp's block copied with plain 16-byte loads
+// and stores, then read back.
+template <int NV, int W, int ESZ>
+__device__ __forceinline__ void stage_taps(const void *w, int slab_c0, int C, int lane, bool act,
+                                           unsigned char *buf, float2 (&wt)[W][NV]) {
+    constexpr int VEC = 2 * NV;
+    constexpr int NC = VEC * W * ESZ / 16;
+    const int nch = C - slab_c0 < 32 * VEC ? C - slab_c0 : 32 * VEC;
+    const int bytes = nch * W * ESZ;
+    const unsigned char *src = static_cast<const unsigned char *>(w) + static_cast<int64_t>(slab_c0) * W * ESZ;
+    for (int off = lane * 16; off < bytes; off += 32 * 16) {
+        const int g = off >> 4, l = g / NC, j = g % NC;
+        *reinterpret_cast<uint4 *>(buf + 16 * (NC * l + (j ^ tap_swizzle<NC>(l)))) =
+            __ldg(reinterpret_cast<const uint4 *>(src + off));
+    }
+    __syncwarp();
+    read_staged_taps<NV, W, ESZ>(buf, lane, act, wt);
+    __syncwarp();  // every lane has read before the buffer is reused
+}
+
+// Issue the copy of this warp's taps into `buf` (see issue_taps_copy).
+template <int NV, int W>
+__device__ __forceinline__ void issue_taps(const void *w, int w_bf16, int slab_c0, int C, int lane, uint32_t buf) {
+    static_assert(NV == 4, "staged taps need 8 channels per lane");
+    if (w_bf16) {
+        issue_taps_copy<NV, W, 2>(w, slab_c0, C, lane, buf);
+    } else {
+        issue_taps_copy<NV, W, 4>(w, slab_c0, C, lane, buf);
+    }
+}
+
+// Read them back: every lane has waited for its copy group; the warp
+// synchronizes here (before and after, so `buf` may be reused afterwards).
+template <int NV, int W>
+__device__ __forceinline__ void take_taps(int w_bf16, int lane, bool act, const unsigned char *buf,
+                                          float2 (&wt)[W][NV]) {
+    __syncwarp();
+    if (w_bf16) {
+        read_staged_taps<NV, W, 2>(buf, lane, act, wt);
+    } else {
+        read_staged_taps<NV, W, 4>(buf, lane, act, wt);
+    }
+    __syncwarp();
+}
+
+// Bias of this lane's channels: 32 (FP32) or 16 (BF16) contiguous,
+// 16-byte aligned bytes.
+template <int NV>
+__device__ __forceinline__ void load_bias_vec(const void *b, int b_kind, int c0, bool act, float2 (&bb)[NV]);
+
+// Taps (staged, synchronously) and bias in one call.
 template <int NV, int W>
 __device__ __forceinline__ void load_taps_staged(const void *w, int w_bf16, const void *b, int b_kind, int slab_c0,
                                                  int C, int c0, bool act, int lane, unsigned char *buf,
@@ -296,7 +355,11 @@ __device__ __forceinline__ void load_taps_staged(const void *w, int w_bf16, cons
     } else {
         stage_taps<NV, W, 4>(w, slab_c0, C, lane, act, buf, wt);
     }
-    // bias: 32 (FP32) or 16 (BF16) contiguous bytes per lane
+    load_bias_vec<NV>(b, b_kind, c0, act, bb);
+}
+template <int NV>
+__device__ __forceinline__ void load_bias_vec(const void *b, int b_kind, int c0, bool act, float2 (&bb)[NV]) {
+    static_assert(NV == 4, "vector bias loads need 8 channels per lane");
 #pragma unroll
     for (int v = 0; v < NV; ++v) bb[v] = f2_zero();
     if (act && b_kind == 1) {

@@ -110,16 +110,22 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
     const int c0 = act ? cv * VEC : 0;
     const int rows_i = static_cast<int>(a.rows);  // host-checked <= 2^31 - 1
 
+    // Taps: with aligned taps the warp's block is copied (cp.async) into its
+    // shared buffer while the run search below runs, then read back.
     float2 wt[W][NV], bb[NV];
     if (a.taps_vec) {
-        load_taps_staged<NV, W>(a.w, a.w_bf16, a.b, a.b_kind, slab * 32 * VEC, a.C, c0, act, lane, taps_buf[warp],
-                                wt, bb);
+        issue_taps<NV, W>(a.w, a.w_bf16, slab * 32 * VEC, a.C, lane, smem_addr(taps_buf[warp]));
+        load_bias_vec<NV>(a.b, a.b_kind, c0, act, bb);
     } else {
         load_taps_w<NV, W>(a.w, a.w_bf16, a.b, a.b_kind, c0, act, wt, bb);
     }
 
     RunWalker<kFwdChunk> walk;
     walk.init(a.cu, a.N, a.rows, run, a.runs, H, false, lane, kFwdWalkRows, staged ? meta.cu : nullptr);
+    if (a.taps_vec) {
+        cp_async_wait(0);
+        take_taps<NV, W>(a.w_bf16, lane, act, taps_buf[warp], wt);
+    }
 
     // The H rows before the current one, oldest first.  (With 3-row batches
     // the window comes back to the same registers every batch; a ring
