@@ -341,3 +341,23 @@ def test_all_row_strides(cuda_device, width, act):
     wl = workloads.make_custom(lengths, 264, rows=sum(lengths) + 3, seed=31, device=cuda_device,
                                n_minus_one=3, width=width, activation=act)
     check(wl, H.run_gpu(wl, x_pad_cols=24, out_pad_cols=40))
+
+
+# ------------------------------------------- metadata staging boundaries --
+# The kernels stage a batch's offsets, slots and flags in shared memory for up
+# to 1024 sequences (forward) and 256 (backward) and read them from global
+# memory beyond that: both sides of both limits, with -1 requests, empty
+# sequences, a pool and d_final_state, on every channel.
+
+@pytest.mark.parametrize("N,width,act", [(256, 4, "silu"), (257, 4, "silu"), (1024, 4, "silu"),
+                                         (1025, 4, "silu"), (2000, 4, "silu"), (300, 2, "silu"),
+                                         (1100, 3, None)])
+def test_many_sequences_staged_and_global_metadata(cuda_device, N, width, act):
+    rng = np.random.default_rng(N)
+    lengths = tuple(int(v) for v in rng.integers(0, 12, N))
+    wl = workloads.make_custom(lengths, 264, rows=sum(lengths) + 7, seed=N, device=cuda_device,
+                               n_minus_one=N // 20, has_init_p=0.5, slots=2 * N + 3, width=width,
+                               activation=act)
+    g = torch.Generator(device=cuda_device).manual_seed(N)
+    d_final = torch.randn((wl.n_seqs, width - 1, wl.C), generator=g, device=cuda_device)
+    check(wl, H.run_gpu(wl, d_final=d_final), d_final=d_final)
