@@ -361,3 +361,33 @@ def test_many_sequences_staged_and_global_metadata(cuda_device, N, width, act):
     g = torch.Generator(device=cuda_device).manual_seed(N)
     d_final = torch.randn((wl.n_seqs, width - 1, wl.C), generator=g, device=cuda_device)
     check(wl, H.run_gpu(wl, d_final=d_final), d_final=d_final)
+
+
+# --------------------------------------------- taps not 16-byte aligned --
+# Aligned taps and bias go through shared memory; taps or a bias that are
+# only element-aligned (a view one element into a buffer) take the per-lane
+# path.  Both must give the oracle's results.
+
+def _offset_view(t: torch.Tensor) -> torch.Tensor:
+    """The same values one element into a larger buffer (not 16-byte aligned)."""
+    flat = torch.empty(t.numel() + 1, dtype=t.dtype, device=t.device)
+    v = flat[1:].view(t.shape)
+    v.copy_(t)
+    assert v.data_ptr() % 16 != 0
+    return v
+
+
+UNALIGNED = [(W, wd, bd, which) for W, wd, bd in ((4, torch.float32, torch.float32), (4, torch.bfloat16, torch.float32),
+                                                  (3, torch.float32, torch.bfloat16))
+             for which in ("weight", "bias", "both")] + [(2, torch.bfloat16, None, "weight")]
+
+
+@pytest.mark.parametrize("width,w_dtype,b_dtype,which", UNALIGNED)
+def test_unaligned_taps(cuda_device, width, w_dtype, b_dtype, which):
+    import dataclasses
+    wl = workloads.make_custom((40, 0, 7, 130, 2, 64), 264, rows=250, seed=41, device=cuda_device,
+                               n_minus_one=1, width=width, w_dtype=w_dtype, b_dtype=b_dtype)
+    w = _offset_view(wl.weight) if which in ("weight", "both") else wl.weight
+    b = _offset_view(wl.bias) if which in ("bias", "both") and wl.bias is not None else wl.bias
+    wl = dataclasses.replace(wl, weight=w, bias=b)
+    check(wl, H.run_gpu(wl))
