@@ -225,9 +225,10 @@ __device__ __forceinline__ void load_taps_w(const void *w, int w_bf16, const voi
 // bias are 16-byte aligned (VEC = 8).  A lane's taps are VEC*W consecutive
 // values, so a warp's are one contiguous block of its slab: the warp copies
 // that block into `buf` (this warp's own shared memory, >= 32 * VEC * W * 4
-// bytes) with 16-byte cp.async copies, consecutive lanes on consecutive
-// chunks (a few fully used 512-byte requests), then each lane reads its own
-// chunks back; the bias is read directly (whole 16-byte vectors).
+// bytes) with 16-byte copies (cp.async, or loads and stores), consecutive
+// lanes on consecutive chunks (a few fully used 512-byte requests), then
+// each lane reads its own chunks back; the bias is read directly (whole
+// 16-byte vectors).
 // Per-lane global loads of the taps touch a different 128-byte line per lane
 // and instruction; with some 40 of them per warp and 16 warps per SM they
 // kept every warp waiting ~10 us at the start of each kernel.  Chunk j of
@@ -342,22 +343,6 @@ __device__ __forceinline__ void take_taps(int w_bf16, int lane, bool act, const 
 // Bias of this lane's channels: 32 (FP32) or 16 (BF16) contiguous,
 // 16-byte aligned bytes.
 template <int NV>
-__device__ __forceinline__ void load_bias_vec(const void *b, int b_kind, int c0, bool act, float2 (&bb)[NV]);
-
-// Taps (staged, synchronously) and bias in one call.
-template <int NV, int W>
-__device__ __forceinline__ void load_taps_staged(const void *w, int w_bf16, const void *b, int b_kind, int slab_c0,
-                                                 int C, int c0, bool act, int lane, unsigned char *buf,
-                                                 float2 (&wt)[W][NV], float2 (&bb)[NV]) {
-    static_assert(NV == 4, "staged taps need 8 channels per lane");
-    if (w_bf16) {
-        stage_taps<NV, W, 2>(w, slab_c0, C, lane, act, buf, wt);
-    } else {
-        stage_taps<NV, W, 4>(w, slab_c0, C, lane, act, buf, wt);
-    }
-    load_bias_vec<NV>(b, b_kind, c0, act, bb);
-}
-template <int NV>
 __device__ __forceinline__ void load_bias_vec(const void *b, int b_kind, int c0, bool act, float2 (&bb)[NV]) {
     static_assert(NV == 4, "vector bias loads need 8 channels per lane");
 #pragma unroll
@@ -378,6 +363,20 @@ __device__ __forceinline__ void load_bias_vec(const void *b, int b_kind, int c0,
     }
 }
 
+
+// Taps (staged, synchronously) and bias in one call.
+template <int NV, int W>
+__device__ __forceinline__ void load_taps_staged(const void *w, int w_bf16, const void *b, int b_kind, int slab_c0,
+                                                 int C, int c0, bool act, int lane, unsigned char *buf,
+                                                 float2 (&wt)[W][NV], float2 (&bb)[NV]) {
+    static_assert(NV == 4, "staged taps need 8 channels per lane");
+    if (w_bf16) {
+        stage_taps<NV, W, 2>(w, slab_c0, C, lane, act, buf, wt);
+    } else {
+        stage_taps<NV, W, 4>(w, slab_c0, C, lane, act, buf, wt);
+    }
+    load_bias_vec<NV>(b, b_kind, c0, act, bb);
+}
 // Pre-activation of one channel pair for a width-W stencil: the bias, then
 // tap k on history row k (k < W-1, oldest first), then tap W-1 on the
 // current row -- the FMA order of FlashInfer causal_conv1d_fn (bias added
@@ -453,8 +452,9 @@ __device__ __forceinline__ float2 activate2_grad(float2 z, float2 gy) {
 // Row indices fit in 32 bits (the host rejects rows > INT32_MAX: cu_seqlens
 // is int32); every address is formed in 64 bits from them.
 //
-// Batches of up to kStageSeqs sequences have their metadata staged in
-// shared memory by the whole CTA at the kernel's start -- the clamped
+// Batches of up to CAP sequences (1024 in the forward, 256 in the
+// backward) have their metadata staged in shared memory by the whole CTA
+// at the kernel's start -- the clamped
 // offsets, the slots and the flags, one coalesced load -- so the walker's
 // searches and every per-sequence lookup cost shared-memory latency instead
 // of a chain of dependent global loads before the first row is read.
