@@ -185,6 +185,53 @@ int ccc_bwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
             void *workspace, size_t workspace_bytes, void *cuda_stream);
 
 /*
+ * Launch options of ccc_fwd_ex / ccc_bwd_ex (ccc_fwd and ccc_bwd are these
+ * with options = 0).  Library behaviour, not part of the method.
+ *
+ * CCC_OPT_OVERLAP_PROLOGUE: launch the call's main kernel as a programmatic
+ * dependent of the kernel enqueued just before it on the stream, so that
+ * the kernel's prologue -- reading cu_seqlens, cache_indices,
+ * has_initial_state, the weight and the bias, and splitting the rows into
+ * runs -- can run while that previous kernel finishes.  The kernel then
+ * waits for the previous kernel to complete (and its writes to be visible)
+ * before it reads x, dy, conv_state, saved_hist or d_final_state, and before
+ * it writes anything.  Contract: the kernel enqueued immediately before the
+ * call on `cuda_stream` (in stream order, also inside a CUDA graph) must not
+ * write cu_seqlens, cache_indices, has_initial_state, weight or bias.  This
+ * holds in the usual step order -- the forward after the projection that
+ * produces x, the backward after the kernel that produces dy or after this
+ * library's forward, a forward after this library's backward -- but not,
+ * e.g., right after a kernel that builds cu_seqlens on the device or an
+ * optimizer step that updates these taps; leave the option off there.
+ * Results are identical with and without it.  Unknown option bits return
+ * CCC_ERR_SHAPE.
+ */
+enum { CCC_OPT_OVERLAP_PROLOGUE = 1 << 0 };
+
+int ccc_fwd_ex(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
+               const void *weight, int32_t w_dtype, int32_t width,
+               const void *bias, int32_t b_dtype, int32_t activation,
+               void *conv_state, int32_t n_slots, int32_t state_len,
+               int64_t st_slot, int64_t st_c, int64_t st_l,
+               const int32_t *cu_seqlens, int32_t N,
+               const int32_t *cache_indices, const uint8_t *has_initial_state,
+               void *out, int64_t out_row_stride,
+               void *saved_hist,
+               void *workspace, size_t workspace_bytes, uint32_t options, void *cuda_stream);
+
+int ccc_bwd_ex(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
+               const void *weight, int32_t w_dtype, int32_t width,
+               const void *bias, int32_t b_dtype, int32_t activation,
+               const void *saved_hist,
+               const int32_t *cu_seqlens, int32_t N,
+               const int32_t *cache_indices, const uint8_t *has_initial_state,
+               const void *dy, int64_t dy_row_stride,
+               const float *d_final_state,
+               void *dx, int64_t dx_row_stride,
+               float *dweight, float *dbias, float *d_init_state,
+               void *workspace, size_t workspace_bytes, uint32_t options, void *cuda_stream);
+
+/*
  * Backward without a workspace argument, for callers that cannot allocate
  * device memory (a host framework whose memory pool they cannot reach, a
  * plugin host that forbids device allocation after start-up, a latency-

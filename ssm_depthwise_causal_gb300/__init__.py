@@ -138,9 +138,12 @@ def ccc_workspace_size(rows: int, n_seqs: int, channels: int, for_bwd: bool) -> 
 
 
 def ccc_fwd(x, weight, bias, conv_state, cu_seqlens, cache_indices, has_initial_state, out,
-            saved_hist=None, workspace=None, stream=None, activation="silu") -> None:
+            saved_hist=None, workspace=None, stream=None, activation="silu", overlap=False) -> None:
     """Forward through the C ABI.  Tensors are CUDA tensors laid out as in
-    include/ccc.h; ``conv_state`` is updated in place."""
+    include/ccc.h; ``conv_state`` is updated in place.  ``overlap=True``
+    sets CCC_OPT_OVERLAP_PROLOGUE (ccc_fwd_ex): only when the kernel enqueued
+    just before on the stream writes none of cu_seqlens, cache_indices,
+    has_initial_state, weight and bias."""
     x2, rows, C, xs = _rows_view(x, "x")
     o2, orows, oC, os_ = _rows_view(out, "out")
     if (orows, oC) != (rows, C):
@@ -150,20 +153,22 @@ def ccc_fwd(x, weight, bias, conv_state, cu_seqlens, cache_indices, has_initial_
     _on_current_device(x2, weight, bias, conv_state, cu_seqlens, cache_indices, has_initial_state, o2,
                        saved_hist, workspace)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = _lib.lib().ccc_fwd(
+    rc = _lib.lib().ccc_fwd_ex(
         _ptr(x2), rows, C, xs, _ptr(weight), _dtype_code(weight), _width(weight),
         _ptr(bias), _dtype_code(bias), _act_code(activation),
         _ptr(conv_state), n_slots, L, st[0], st[1], st[2],
         _ptr(cu_seqlens), N, _ptr(cache_indices), _ptr(has_initial_state),
-        _ptr(o2), os_, _ptr(saved_hist), _ptr(workspace), ws_bytes, _stream(stream))
+        _ptr(o2), os_, _ptr(saved_hist), _ptr(workspace), ws_bytes,
+        _lib.OPT_OVERLAP_PROLOGUE if overlap else 0, _stream(stream))
     if rc != 0:
         raise CCCError(rc, "ccc_fwd")
 
 
 def ccc_bwd(x, weight, bias, saved_hist, cu_seqlens, cache_indices, has_initial_state, dy,
             d_final_state, dx, dweight, dbias, d_init_state, workspace=None, stream=None,
-            activation="silu") -> None:
-    """Backward through the C ABI (see include/ccc.h for every argument)."""
+            activation="silu", overlap=False) -> None:
+    """Backward through the C ABI (see include/ccc.h for every argument);
+    ``overlap`` as in ccc_fwd (ccc_bwd_ex)."""
     x2, rows, C, xs = _rows_view(x, "x")
     g2, grows, gC, gs = _rows_view(dy, "dy")
     d2, drows, dC, ds = _rows_view(dx, "dx")
@@ -173,12 +178,13 @@ def ccc_bwd(x, weight, bias, saved_hist, cu_seqlens, cache_indices, has_initial_
     _on_current_device(x2, weight, bias, saved_hist, cu_seqlens, cache_indices, has_initial_state, g2,
                        d_final_state, d2, dweight, dbias, d_init_state, workspace)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = _lib.lib().ccc_bwd(
+    rc = _lib.lib().ccc_bwd_ex(
         _ptr(x2), rows, C, xs, _ptr(weight), _dtype_code(weight), _width(weight),
         _ptr(bias), _dtype_code(bias), _act_code(activation),
         _ptr(saved_hist), _ptr(cu_seqlens), N, _ptr(cache_indices), _ptr(has_initial_state),
         _ptr(g2), gs, _ptr(d_final_state), _ptr(d2), ds, _ptr(dweight), _ptr(dbias),
-        _ptr(d_init_state), _ptr(workspace), ws_bytes, _stream(stream))
+        _ptr(d_init_state), _ptr(workspace), ws_bytes, _lib.OPT_OVERLAP_PROLOGUE if overlap else 0,
+        _stream(stream))
     if rc != 0:
         raise CCCError(rc, "ccc_bwd")
 

@@ -14,8 +14,11 @@ _PATH = os.path.join(_PKG, "libccc.so")
 _lock = threading.Lock()
 _handle = None
 
-EXPORTS = ("ccc_workspace_size", "ccc_fwd", "ccc_bwd", "ccc_bwd_noalloc", "ccc_update",
-           "ccc_check_status_words", "ccc_check", "ccc_status_string", "ccc_last_launch_count")
+EXPORTS = ("ccc_workspace_size", "ccc_fwd", "ccc_bwd", "ccc_fwd_ex", "ccc_bwd_ex", "ccc_bwd_noalloc",
+           "ccc_update", "ccc_check_status_words", "ccc_check", "ccc_status_string", "ccc_last_launch_count")
+
+# Launch option bits of ccc_fwd_ex / ccc_bwd_ex (include/ccc.h).
+OPT_OVERLAP_PROLOGUE = 1 << 0
 
 # Size of the fixed scratch array behind ccc_bwd_noalloc (CCC_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -45,6 +48,11 @@ def lib() -> ctypes.CDLL:
             h.ccc_bwd.argtypes = [P, i64, i32, i64, P, i32, i32, P, i32, i32, P, P, i32, P, P, P, i64, P,
                                   P, i64, P, P, P, P, sz, P]
             h.ccc_bwd.restype = ctypes.c_int
+            u32 = ctypes.c_uint32
+            h.ccc_fwd_ex.argtypes = h.ccc_fwd.argtypes[:-1] + [u32, P]
+            h.ccc_fwd_ex.restype = ctypes.c_int
+            h.ccc_bwd_ex.argtypes = h.ccc_bwd.argtypes[:-1] + [u32, P]
+            h.ccc_bwd_ex.restype = ctypes.c_int
             h.ccc_bwd_noalloc.argtypes = [P, i64, i32, i64, P, i32, i32, P, i32, i32, P, P, i32, P, P, P,
                                           i64, P, P, i64, P, P, P, P]
             h.ccc_bwd_noalloc.restype = ctypes.c_int

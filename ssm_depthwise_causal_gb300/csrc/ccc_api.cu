@@ -134,6 +134,22 @@ int ccc_fwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
             void *out, int64_t out_row_stride,
             void *saved_hist,
             void *workspace, size_t workspace_bytes, void *cuda_stream) {
+    return ccc_fwd_ex(x, rows, C, x_row_stride, weight, w_dtype, width, bias, b_dtype, activation, conv_state,
+                      n_slots, state_len, st_slot, st_c, st_l, cu_seqlens, N, cache_indices, has_initial_state, out,
+                      out_row_stride, saved_hist, workspace, workspace_bytes, 0u, cuda_stream);
+}
+
+int ccc_fwd_ex(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
+               const void *weight, int32_t w_dtype, int32_t width,
+               const void *bias, int32_t b_dtype, int32_t activation,
+               void *conv_state, int32_t n_slots, int32_t state_len,
+               int64_t st_slot, int64_t st_c, int64_t st_l,
+               const int32_t *cu_seqlens, int32_t N,
+               const int32_t *cache_indices, const uint8_t *has_initial_state,
+               void *out, int64_t out_row_stride,
+               void *saved_hist,
+               void *workspace, size_t workspace_bytes, uint32_t options, void *cuda_stream) {
+    if (options & ~static_cast<uint32_t>(CCC_OPT_OVERLAP_PROLOGUE)) return CCC_ERR_SHAPE;
     // ---- shapes and dtypes
     if (rows < 0 || N < 0 || C <= 0 || C % 8 != 0) return CCC_ERR_SHAPE;
     if (rows > INT32_MAX) return CCC_ERR_SHAPE;  // cu_seqlens is int32
@@ -212,7 +228,7 @@ int ccc_fwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
     const DeviceFacts facts = device_facts();
     a.runs = ccc::runs_per_slab(static_cast<int64_t>(facts.sms) * facts.fwd_ctas * ccc::kWarpsPerCta * ccc::kFwdWaves,
                                 a.slabs);
-    if (ccc::launch_fwd(a, st) != cudaSuccess) return CCC_ERR_CUDA;
+    if (ccc::launch_fwd(a, st, (options & CCC_OPT_OVERLAP_PROLOGUE) != 0) != cudaSuccess) return CCC_ERR_CUDA;
     g_last_launches = 1;
     return CCC_OK;
 }
@@ -228,6 +244,23 @@ int ccc_bwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
             void *dx, int64_t dx_row_stride,
             float *dweight, float *dbias, float *d_init_state,
             void *workspace, size_t workspace_bytes, void *cuda_stream) {
+    return ccc_bwd_ex(x, rows, C, x_row_stride, weight, w_dtype, width, bias, b_dtype, activation, saved_hist,
+                      cu_seqlens, N, cache_indices, has_initial_state, dy, dy_row_stride, d_final_state, dx,
+                      dx_row_stride, dweight, dbias, d_init_state, workspace, workspace_bytes, 0u, cuda_stream);
+}
+
+int ccc_bwd_ex(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
+               const void *weight, int32_t w_dtype, int32_t width,
+               const void *bias, int32_t b_dtype, int32_t activation,
+               const void *saved_hist,
+               const int32_t *cu_seqlens, int32_t N,
+               const int32_t *cache_indices, const uint8_t *has_initial_state,
+               const void *dy, int64_t dy_row_stride,
+               const float *d_final_state,
+               void *dx, int64_t dx_row_stride,
+               float *dweight, float *dbias, float *d_init_state,
+               void *workspace, size_t workspace_bytes, uint32_t options, void *cuda_stream) {
+    if (options & ~static_cast<uint32_t>(CCC_OPT_OVERLAP_PROLOGUE)) return CCC_ERR_SHAPE;
     if (rows < 0 || N < 0 || C <= 0 || C % 8 != 0) return CCC_ERR_SHAPE;
     if (rows > INT32_MAX) return CCC_ERR_SHAPE;
     if (x_row_stride < C || dy_row_stride < C || dx_row_stride < C || x_row_stride % 8 || dy_row_stride % 8 ||
@@ -306,7 +339,7 @@ int ccc_bwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
     a.slabs = ccc::bwd_slabs(C);
     a.taps_vec = ccc::kBwdVec == 8 && ccc::kBwdRing > 0 && aligned(weight, 16) && (!bias || aligned(bias, 16));
     a.runs = ccc::bwd_runs(rows, C);
-    if (ccc::launch_bwd(a, st) != cudaSuccess) return CCC_ERR_CUDA;
+    if (ccc::launch_bwd(a, st, (options & CCC_OPT_OVERLAP_PROLOGUE) != 0) != cudaSuccess) return CCC_ERR_CUDA;
     if (ccc::launch_reduce(a.part, a.runs, C, width, dweight, dbias, st) != cudaSuccess) return CCC_ERR_CUDA;
     g_last_launches = 2;
     return CCC_OK;

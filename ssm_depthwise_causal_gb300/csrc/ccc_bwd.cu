@@ -137,6 +137,13 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
     RunWalker<kBwdChunk> walk;
     walk.init(a.cu, a.N, a.rows, run, a.runs, H, true, lane, kBwdWalkRows, staged ? meta.cu : nullptr);
 
+    // Everything above reads only the offsets, slots, flags, taps and bias.
+    // Launched as a programmatic dependent (CCC_OPT_OVERLAP_PROLOGUE) it may
+    // have run while the previous kernel finished; wait for that kernel
+    // before reading x, dy, the saved history or the final-state gradient,
+    // or writing anything.  (A no-op for an ordinary launch.)
+    grid_dependency_wait();
+
     // The rings of history values and dz, carried from one segment to the
     // next along a walk (slot = walk row % RS).
     constexpr int RS = U;
@@ -458,6 +465,7 @@ __device__ __forceinline__ float4 f4_add(float4 a, float4 b) {
 __global__ void __launch_bounds__(256) reduce_kernel(const float *part, int G, int C, int W, float *dweight,
                                                      float *dbias) {
     grid_dependency_wait();  // the backward's partials
+    grid_dependents_launch();  // (a dependent's prologue may overlap this kernel)
     __shared__ float4 blk[kWarpsPerCta][32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int cblocks = (C + kRedChannels - 1) / kRedChannels;
@@ -522,7 +530,7 @@ BwdKernel bwd_kernel_for(int width, int act) {
 
 }  // namespace
 
-cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t st) {
+cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t st, bool overlap) {
     const BwdKernel kern = bwd_kernel_for(a.width, a.act);
     if (!kern) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
@@ -541,6 +549,13 @@ cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t st) {
         if (e != cudaSuccess) return e;
     }
     cfg.dynamicSmemBytes = ring_bytes;
+    cudaLaunchAttribute attr[1];
+    if (overlap) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 

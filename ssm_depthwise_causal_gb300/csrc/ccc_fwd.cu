@@ -127,6 +127,13 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
         take_taps<NV, W>(a.w_bf16, lane, act, taps_buf[warp], wt);
     }
 
+    // Everything above reads only the offsets, slots, flags, taps and bias.
+    // Launched as a programmatic dependent (CCC_OPT_OVERLAP_PROLOGUE) it may
+    // have run while the previous kernel finished; wait for that kernel
+    // before reading x, the pool or the saved history, or writing anything.
+    // (A no-op for an ordinary launch.)
+    grid_dependency_wait();
+
     // The H rows before the current one, oldest first.  (With 3-row batches
     // the window comes back to the same registers every batch; a ring
     // indexed by walk row, as in the backward, measured no faster here.)
@@ -254,6 +261,9 @@ __global__ void __launch_bounds__(kCtaThreads, kFwdMinBlocks) fwd_kernel(const F
             for (int p = 0; p < H; ++p) put_state<NV>(a.state, a.st_slot, a.st_c, a.st_l, a.state_vec, q, p, c0, fin[p]);
         }
     }
+    // Let a kernel launched as this one's programmatic dependent start its
+    // prologue (it waits for this grid's writes before reading them).
+    grid_dependents_launch();
 }
 
 }  // namespace
@@ -290,12 +300,21 @@ int fwd_ctas_per_sm() {
     return n;
 }
 
-cudaError_t launch_fwd(const FwdArgs &a, cudaStream_t st) {
+cudaError_t launch_fwd(const FwdArgs &a, cudaStream_t st, bool overlap) {
     const FwdKernel kern = fwd_kernel_for(a.width, a.act);
     if (!kern) return cudaErrorInvalidValue;
-    const dim3 grid(static_cast<unsigned>(ceil_div(static_cast<int64_t>(a.slabs) * a.runs, kWarpsPerCta)));
-    kern<<<grid, kCtaThreads, 0, st>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(static_cast<int64_t>(a.slabs) * a.runs, kWarpsPerCta)));
+    cfg.blockDim = dim3(kCtaThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    if (overlap) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 }  // namespace ccc

@@ -253,8 +253,11 @@ inline int bwd_runs(int64_t rows, int C) {
     return by_rows < by_width ? static_cast<int>(by_rows) : by_width;
 }
 
-cudaError_t launch_fwd(const FwdArgs &a, cudaStream_t st);
-cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t st);
+// `overlap`: launch as a programmatic dependent of the previous kernel in
+// the stream (the prologue may run while that kernel finishes; the kernel
+// waits for it before touching activations, history, state or outputs).
+cudaError_t launch_fwd(const FwdArgs &a, cudaStream_t st, bool overlap);
+cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t st, bool overlap);
 // Resident forward CTAs per SM on the current device (occupancy query).
 int fwd_ctas_per_sm();
 cudaError_t launch_reduce(const float *part, int G, int C, int width, float *dweight, float *dbias,

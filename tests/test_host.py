@@ -252,3 +252,21 @@ def test_binding_rejects_tensors_off_the_current_device(lib):
     with pytest.raises(ValueError, match="CUDA tensors"):
         ccc.ccc_bwd_noalloc(x, w, None, None, cu, None, None, x, None, torch.empty_like(x),
                             torch.empty((8, 4)), None, None)
+
+
+def test_launch_options(lib):
+    """ccc_fwd_ex / ccc_bwd_ex take CCC_OPT_OVERLAP_PROLOGUE (bit 0) and
+    refuse any other bit before touching CUDA."""
+    a = fwd_args()
+    args = [P(a["x"]), a["rows"], a["C"], a["xs"], P(a["w"]), a["wd"], a["W"], P(a["b"]), a["bd"], a["act"],
+            P(a["state"]), a["slots"], a["L"], a["s0"], a["s1"], a["s2"], P(a["cu"]), a["N"], P(a["ci"]),
+            P(a["hi"]), P(a["out"]), a["os"], P(a["hist"]), P(a["ws"]), a["wsb"]]
+    for bad in (2, 4, 1 << 31, 3):
+        assert lib.ccc_fwd_ex(*args, bad, None) == E_SHAPE
+    zero = list(args)
+    zero[1] = 0  # rows == 0: checks pass, nothing launched
+    assert lib.ccc_fwd_ex(*zero, _lib.OPT_OVERLAP_PROLOGUE, None) == OK
+    b = [P(A), 64, 256, 256, P(A * 2), 0, 4, None, -1, 1, None, P(A * 3), 4, None, None, P(A * 4), 256, None,
+         P(A * 5), 256, P(A * 6), None, None, P(A * 9), 1 << 30]
+    assert lib.ccc_bwd_ex(*b, 2, None) == E_SHAPE
+    assert lib.ccc_bwd_ex(*b, 4, None) == E_SHAPE
