@@ -185,8 +185,9 @@ int ccc_bwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
             void *workspace, size_t workspace_bytes, void *cuda_stream);
 
 /*
- * Launch options of ccc_fwd_ex / ccc_bwd_ex (ccc_fwd and ccc_bwd are these
- * with options = 0).  Library behaviour, not part of the method.
+ * Launch options of ccc_fwd_ex / ccc_bwd_ex / ccc_update_ex (ccc_fwd,
+ * ccc_bwd and ccc_update are these with options = 0).  Library behaviour,
+ * not part of the method.
  *
  * CCC_OPT_OVERLAP_PROLOGUE: launch the call's main kernel as a programmatic
  * dependent of the kernel enqueued just before it on the stream, so that
@@ -197,7 +198,8 @@ int ccc_bwd(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
  * before it reads x, dy, conv_state, saved_hist or d_final_state, and before
  * it writes anything.  Contract: the kernel enqueued immediately before the
  * call on `cuda_stream` (in stream order, also inside a CUDA graph) must not
- * write cu_seqlens, cache_indices, has_initial_state, weight or bias.  This
+ * write cu_seqlens, cache_indices, has_initial_state (num_accepted for
+ * ccc_update_ex), weight or bias.  This
  * holds in the usual step order -- the forward after the projection that
  * produces x, the backward after the kernel that produces dy or after this
  * library's forward, a forward after this library's backward -- but not,
@@ -310,6 +312,16 @@ int ccc_update(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
                const int32_t *cu_seqlens, int32_t N,
                const int32_t *cache_indices, const int32_t *num_accepted,
                void *out, int64_t out_row_stride, void *cuda_stream);
+
+/* ccc_update with launch options (CCC_OPT_OVERLAP_PROLOGUE, above). */
+int ccc_update_ex(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
+                  const void *weight, int32_t w_dtype, int32_t width,
+                  const void *bias, int32_t b_dtype, int32_t activation,
+                  void *conv_state, int32_t n_slots, int32_t state_len,
+                  int64_t st_slot, int64_t st_c, int64_t st_l,
+                  const int32_t *cu_seqlens, int32_t N,
+                  const int32_t *cache_indices, const int32_t *num_accepted,
+                  void *out, int64_t out_row_stride, uint32_t options, void *cuda_stream);
 
 /*
  * Device-side check of the caller-owned metadata.  The pages leave the

@@ -216,7 +216,7 @@ def ccc_bwd_noalloc(x, weight, bias, saved_hist, cu_seqlens, cache_indices, has_
 
 
 def ccc_update(x, weight, bias, conv_state, cu_seqlens, cache_indices, num_accepted, out,
-               stream=None, activation="silu") -> None:
+               stream=None, activation="silu", overlap=False) -> None:
     """Speculative / single-token decode step through the C ABI: the new
     tokens' outputs from the history in ``conv_state`` (read at positions
     num_accepted-1 ..), and the pool update for the next step (include/ccc.h,
@@ -228,12 +228,12 @@ def ccc_update(x, weight, bias, conv_state, cu_seqlens, cache_indices, num_accep
     N = cu_seqlens.numel() - 1
     n_slots, L, st = _pool_args(conv_state, C)
     _on_current_device(x2, weight, bias, conv_state, cu_seqlens, cache_indices, num_accepted, o2)
-    rc = _lib.lib().ccc_update(
+    rc = _lib.lib().ccc_update_ex(
         _ptr(x2), rows, C, xs, _ptr(weight), _dtype_code(weight), _width(weight),
         _ptr(bias), _dtype_code(bias), _act_code(activation),
         _ptr(conv_state), n_slots, L, st[0], st[1], st[2],
         _ptr(cu_seqlens), N, _ptr(cache_indices), _ptr(num_accepted),
-        _ptr(o2), os_, _stream(stream))
+        _ptr(o2), os_, _lib.OPT_OVERLAP_PROLOGUE if overlap else 0, _stream(stream))
     if rc != 0:
         raise CCCError(rc, "ccc_update")
 

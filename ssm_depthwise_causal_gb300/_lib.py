@@ -15,7 +15,8 @@ _lock = threading.Lock()
 _handle = None
 
 EXPORTS = ("ccc_workspace_size", "ccc_fwd", "ccc_bwd", "ccc_fwd_ex", "ccc_bwd_ex", "ccc_bwd_noalloc",
-           "ccc_update", "ccc_check_status_words", "ccc_check", "ccc_status_string", "ccc_last_launch_count")
+           "ccc_update", "ccc_update_ex", "ccc_check_status_words", "ccc_check", "ccc_status_string",
+           "ccc_last_launch_count")
 
 # Launch option bits of ccc_fwd_ex / ccc_bwd_ex (include/ccc.h).
 OPT_OVERLAP_PROLOGUE = 1 << 0
@@ -59,6 +60,8 @@ def lib() -> ctypes.CDLL:
             h.ccc_update.argtypes = [P, i64, i32, i64, P, i32, i32, P, i32, i32, P, i32, i32, i64, i64, i64,
                                      P, i32, P, P, P, i64, P]
             h.ccc_update.restype = ctypes.c_int
+            h.ccc_update_ex.argtypes = h.ccc_update.argtypes[:-1] + [ctypes.c_uint32, P]
+            h.ccc_update_ex.restype = ctypes.c_int
             h.ccc_check_status_words.argtypes = [i32]
             h.ccc_check_status_words.restype = sz
             h.ccc_check.argtypes = [i64, P, i32, P, i32, P, i32, P, sz, P]

@@ -353,6 +353,20 @@ int ccc_update(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
                const int32_t *cu_seqlens, int32_t N,
                const int32_t *cache_indices, const int32_t *num_accepted,
                void *out, int64_t out_row_stride, void *cuda_stream) {
+    return ccc_update_ex(x, rows, C, x_row_stride, weight, w_dtype, width, bias, b_dtype, activation, conv_state,
+                         n_slots, state_len, st_slot, st_c, st_l, cu_seqlens, N, cache_indices, num_accepted, out,
+                         out_row_stride, 0u, cuda_stream);
+}
+
+int ccc_update_ex(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
+                  const void *weight, int32_t w_dtype, int32_t width,
+                  const void *bias, int32_t b_dtype, int32_t activation,
+                  void *conv_state, int32_t n_slots, int32_t state_len,
+                  int64_t st_slot, int64_t st_c, int64_t st_l,
+                  const int32_t *cu_seqlens, int32_t N,
+                  const int32_t *cache_indices, const int32_t *num_accepted,
+                  void *out, int64_t out_row_stride, uint32_t options, void *cuda_stream) {
+    if (options & ~static_cast<uint32_t>(CCC_OPT_OVERLAP_PROLOGUE)) return CCC_ERR_SHAPE;
     if (rows < 0 || N < 0 || C <= 0 || C % 8 != 0) return CCC_ERR_SHAPE;
     if (rows > INT32_MAX) return CCC_ERR_SHAPE;
     if (x_row_stride < C || out_row_stride < C || x_row_stride % 8 || out_row_stride % 8) return CCC_ERR_SHAPE;
@@ -412,7 +426,9 @@ int ccc_update(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
     a.os = static_cast<int>(out_row_stride);
     a.slabs = ccc::update_slabs(C);
     a.groups = ccc::update_groups(N, a.slabs, device_facts().sms);
-    if (ccc::launch_update(a, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return CCC_ERR_CUDA;
+    if (ccc::launch_update(a, static_cast<cudaStream_t>(cuda_stream), (options & CCC_OPT_OVERLAP_PROLOGUE) != 0) !=
+        cudaSuccess)
+        return CCC_ERR_CUDA;
     g_last_launches = 1;
     return CCC_OK;
 }

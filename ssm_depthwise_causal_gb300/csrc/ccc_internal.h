@@ -265,6 +265,6 @@ cudaError_t launch_reduce(const float *part, int G, int C, int width, float *dwe
 int update_slabs(int C);
 int update_stage_max_len();
 int update_groups(int N, int slabs, int sms);
-cudaError_t launch_update(const UpdArgs &a, cudaStream_t st);
+cudaError_t launch_update(const UpdArgs &a, cudaStream_t st, bool overlap);
 
 }  // namespace ccc

@@ -188,6 +188,10 @@ __global__ void __launch_bounds__(kCtaThreads, kUpdMinBlocks) update_kernel(cons
         ts.store(s_tap);
     }
     __syncthreads();
+    // Only offsets, slots, accepted counts, taps and bias read above; launched
+    // as a programmatic dependent (CCC_OPT_OVERLAP_PROLOGUE) wait here for the
+    // previous kernel before touching the pool, x or out.  (A no-op otherwise.)
+    grid_dependency_wait();
     if (cur.n < 0) return;  // whole warp, after the CTA barrier
 
     const int cv = slab * 32 + lane;
@@ -291,6 +295,11 @@ __global__ void __launch_bounds__(kCtaThreads, upd_block_min_blocks(LS)) update_
     const Req r = load_req(a, grp * kWarpsPerCta + warp, a.N);
     TapStage<W> ts;
     ts.load(a, slab);
+    // Only offsets, slots, accepted counts, taps and bias read so far;
+    // launched as a programmatic dependent (CCC_OPT_OVERLAP_PROLOGUE) wait
+    // here for the previous kernel before touching the pool, x or out.  (A
+    // no-op otherwise.)
+    grid_dependency_wait();
 
     // The block and the first T0 new tokens, loaded before the CTA barrier.
     const int cv = slab * 32 + lane;
@@ -475,7 +484,7 @@ int update_groups(int N, int slabs, int sms) {
     return static_cast<int>(g < 1 ? 1 : g);
 }
 
-cudaError_t launch_update(const UpdArgs &a, cudaStream_t st) {
+cudaError_t launch_update(const UpdArgs &a, cudaStream_t st, bool overlap) {
     const int ls = a.state_stage ? a.L : 0;
     const UpdKernel kern = update_kernel_for(a.width, a.act, ls);
     if (!kern) return cudaErrorInvalidValue;
@@ -485,8 +494,18 @@ cudaError_t launch_update(const UpdArgs &a, cudaStream_t st) {
     const int64_t groups = ls > 0 ? ceil_div(a.N, kWarpsPerCta) : a.groups;
     const int64_t ctas = static_cast<int64_t>(a.slabs) * groups;
     if (ctas > INT32_MAX) return cudaErrorInvalidValue;
-    kern<<<dim3(static_cast<unsigned>(ctas)), kCtaThreads, 0, st>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+    cfg.blockDim = dim3(kCtaThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    if (overlap) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 }  // namespace ccc

@@ -255,8 +255,8 @@ def test_binding_rejects_tensors_off_the_current_device(lib):
 
 
 def test_launch_options(lib):
-    """ccc_fwd_ex / ccc_bwd_ex take CCC_OPT_OVERLAP_PROLOGUE (bit 0) and
-    refuse any other bit before touching CUDA."""
+    """ccc_fwd_ex / ccc_bwd_ex / ccc_update_ex take CCC_OPT_OVERLAP_PROLOGUE
+    (bit 0) and refuse any other bit before touching CUDA."""
     a = fwd_args()
     args = [P(a["x"]), a["rows"], a["C"], a["xs"], P(a["w"]), a["wd"], a["W"], P(a["b"]), a["bd"], a["act"],
             P(a["state"]), a["slots"], a["L"], a["s0"], a["s1"], a["s2"], P(a["cu"]), a["N"], P(a["ci"]),
@@ -270,3 +270,9 @@ def test_launch_options(lib):
          P(A * 5), 256, P(A * 6), None, None, P(A * 9), 1 << 30]
     assert lib.ccc_bwd_ex(*b, 2, None) == E_SHAPE
     assert lib.ccc_bwd_ex(*b, 4, None) == E_SHAPE
+    u = [P(A), 64, 256, 256, P(A * 2), 0, 4, None, -1, 1, P(A * 6), 8, 4, 1024, 4, 1, P(A * 3), 4, P(A * 7),
+         None, P(A * 4), 256]
+    for bad in (2, 8, 1 << 31):
+        assert lib.ccc_update_ex(*u, bad, None) == E_SHAPE
+    u[1] = 0  # rows == 0: checks pass, nothing launched
+    assert lib.ccc_update_ex(*u, _lib.OPT_OVERLAP_PROLOGUE, None) == OK

@@ -1,7 +1,8 @@
-"""CCC_OPT_OVERLAP_PROLOGUE (ccc_fwd_ex / ccc_bwd_ex): the kernels launched
-as programmatic dependents of the previous kernel give the same bits as
-ordinary launches -- eagerly, and as K back-to-back training steps captured
-in one CUDA graph (each kernel then a dependent of the one before)."""
+"""CCC_OPT_OVERLAP_PROLOGUE (ccc_fwd_ex, ccc_bwd_ex, ccc_update_ex): the
+kernels launched as programmatic dependents of the previous kernel give the
+same bits as ordinary launches -- eagerly, and as back-to-back training or
+decode steps captured in one CUDA graph (each kernel then a dependent of the
+one before)."""
 import pytest
 import torch
 
@@ -80,3 +81,38 @@ def test_overlap_steps_in_one_graph(cuda_device):
         g.replay()
     torch.cuda.synchronize()
     _same(plain, over)
+
+
+@pytest.mark.parametrize("name", ["decode", "spec_decode"])
+def test_overlap_update_steps_equal_plain(cuda_device, name):
+    """ccc_update_ex with the option: three decode steps eagerly, then three
+    more captured in one CUDA graph (each a dependent of the step before, on
+    the pool it wrote), leave the same outputs and pool bits as six plain
+    steps."""
+    wl = workloads.WORKLOADS[name](device=cuda_device)
+    acc = wl.num_accepted if wl.lengths.max() > 1 else None
+
+    def run(pool, out, overlap, stream=None):
+        ccc.ccc_update(wl.x, wl.weight, wl.bias, pool, wl.cu_seqlens, wl.cache_indices, acc, out,
+                       stream=stream, overlap=overlap)
+
+    pool_p, out_p = wl.conv_state.clone(), torch.zeros_like(wl.x)
+    pool_o, out_o = wl.conv_state.clone(), torch.zeros_like(wl.x)
+    for _ in range(3):
+        run(pool_p, out_p, False)
+        run(pool_o, out_o, True)
+    torch.cuda.synchronize()
+    assert torch.equal(out_p.view(torch.int16), out_o.view(torch.int16))
+    assert torch.equal(pool_p.view(torch.int16), pool_o.view(torch.int16))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(3):
+            run(pool_o, out_o, True, stream=s)
+    g.replay()
+    for _ in range(3):
+        run(pool_p, out_p, False)
+    torch.cuda.synchronize()
+    assert torch.equal(out_p.view(torch.int16), out_o.view(torch.int16))
+    assert torch.equal(pool_p.view(torch.int16), pool_o.view(torch.int16))
