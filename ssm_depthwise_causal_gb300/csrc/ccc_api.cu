@@ -339,7 +339,8 @@ int ccc_bwd_ex(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
     a.slabs = ccc::bwd_slabs(C);
     a.taps_vec = ccc::kBwdVec == 8 && ccc::kBwdRing > 0 && aligned(weight, 16) && (!bias || aligned(bias, 16));
     a.runs = ccc::bwd_runs(rows, C);
-    if (ccc::launch_bwd(a, st, (options & CCC_OPT_OVERLAP_PROLOGUE) != 0) != cudaSuccess) return CCC_ERR_CUDA;
+    if (ccc::launch_bwd(a, st, (options & CCC_OPT_OVERLAP_PROLOGUE) != 0, device_facts().sms) != cudaSuccess)
+        return CCC_ERR_CUDA;
     if (ccc::launch_reduce(a.part, a.runs, C, width, dweight, dbias, st) != cudaSuccess) return CCC_ERR_CUDA;
     g_last_launches = 2;
     return CCC_OK;

@@ -95,8 +95,10 @@ __device__ __forceinline__ void ring_partials(float2 (&g)[W][NV], float2 (&gb)[N
 // P = 0: each lane loads its U rows of x and dy straight into registers.
 // P > 0: each lane streams the rows of its walk through a P-stage ring of
 // U-row batches in shared memory (cp.async), keeping up to P-1 batches in
-// flight ahead of the math.
-template <int VEC, int U, int P, int W, bool ACT>
+// flight ahead of the math.  CW: warps per CTA (kWarpsPerCta for a grid that
+// fills every SM, 1 for a smaller one, whose one-warp CTAs the block
+// scheduler then spreads over the SMs instead of packing 8 tasks on one).
+template <int VEC, int U, int P, int W, bool ACT, int CW>
 __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const BwdArgs a) {
     constexpr int NV = VEC / 2;
     constexpr int H = W - 1;                            // history rows
@@ -107,7 +109,7 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
     __shared__ SeqMeta<kBwdStageSeqs> meta;  // (before any exit: the whole CTA stages it)
     const bool staged = stage_meta(meta, a.cu, a.N, a.rows, a.cache, a.has_init);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int gw = blockIdx.x * kWarpsPerCta + warp;  // this warp's task
+    const int gw = blockIdx.x * CW + warp;  // this warp's task
     if (gw >= a.slabs * a.runs) return;               // (whole warp) no task in the last CTA
     const int slab = gw % a.slabs, run = gw / a.slabs;
     const int cv = slab * 32 + lane;
@@ -511,34 +513,43 @@ __global__ void __launch_bounds__(256) reduce_kernel(const float *part, int G, i
 using BwdKernel = void (*)(const BwdArgs);
 
 template <int W, bool ACT>
-constexpr BwdKernel bwd_kernel_of() {
-    return bwd_kernel<kBwdVec, kBwdUnroll, kBwdRing, W, ACT>;
+constexpr BwdKernel bwd_kernel_of(bool one_warp) {
+    return one_warp ? bwd_kernel<kBwdVec, kBwdUnroll, kBwdRing, W, ACT, 1>
+                    : bwd_kernel<kBwdVec, kBwdUnroll, kBwdRing, W, ACT, kWarpsPerCta>;
 }
 
-// The instantiation for (width, activation); nullptr for an unsupported pair.
-BwdKernel bwd_kernel_for(int width, int act) {
+// The instantiation for (width, activation, CTA size); nullptr for an
+// unsupported pair.
+BwdKernel bwd_kernel_for(int width, int act, bool one_warp) {
     switch (width * 2 + (act ? 1 : 0)) {
-        case 4: return bwd_kernel_of<2, false>();
-        case 5: return bwd_kernel_of<2, true>();
-        case 6: return bwd_kernel_of<3, false>();
-        case 7: return bwd_kernel_of<3, true>();
-        case 8: return bwd_kernel_of<4, false>();
-        case 9: return bwd_kernel_of<4, true>();
+        case 4: return bwd_kernel_of<2, false>(one_warp);
+        case 5: return bwd_kernel_of<2, true>(one_warp);
+        case 6: return bwd_kernel_of<3, false>(one_warp);
+        case 7: return bwd_kernel_of<3, true>(one_warp);
+        case 8: return bwd_kernel_of<4, false>(one_warp);
+        case 9: return bwd_kernel_of<4, true>(one_warp);
         default: return nullptr;
     }
 }
 
 }  // namespace
 
-cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t st, bool overlap) {
-    const BwdKernel kern = bwd_kernel_for(a.width, a.act);
+cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t st, bool overlap, int sms) {
+    // Where spreading the tasks evenly would leave every SM fewer than 8 of
+    // them, one-warp CTAs, which the block scheduler spreads over all SMs
+    // (a tiny batch's 65 tasks on 65 SMs, not on 9 SMs in 8-warp CTAs).
+    // Which warp runs a task changes nothing it computes.
+    const int64_t tasks = static_cast<int64_t>(a.slabs) * a.runs;
+    const bool one_warp = tasks <= static_cast<int64_t>(sms) * (kWarpsPerCta - 1);
+    const int cw = one_warp ? 1 : kWarpsPerCta;
+    const BwdKernel kern = bwd_kernel_for(a.width, a.act, one_warp);
     if (!kern) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(static_cast<int64_t>(a.slabs) * a.runs, kWarpsPerCta)));
-    cfg.blockDim = dim3(kCtaThreads);
+    cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(tasks, cw)));
+    cfg.blockDim = dim3(static_cast<unsigned>(32 * cw));
     cfg.stream = st;
     constexpr int P = kBwdRing;
-    constexpr size_t ring_bytes = static_cast<size_t>(P) * kBwdUnroll * 2 * 32 * kBwdVec * 2 * kWarpsPerCta;
+    const size_t ring_bytes = static_cast<size_t>(P) * kBwdUnroll * 2 * 32 * kBwdVec * 2 * cw;
     if (ring_bytes > 48 * 1024) {
         // Opt in to more than 48 KB of dynamic shared memory.  Set on every
         // launch (a host-side attribute, no device work): no flag shared

@@ -257,7 +257,9 @@ inline int bwd_runs(int64_t rows, int C) {
 // the stream (the prologue may run while that kernel finishes; the kernel
 // waits for it before touching activations, history, state or outputs).
 cudaError_t launch_fwd(const FwdArgs &a, cudaStream_t st, bool overlap);
-cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t st, bool overlap);
+// sms: the device's SM count (a grid of at most 7 tasks per SM runs as
+// one-warp CTAs).
+cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t st, bool overlap, int sms);
 // Resident forward CTAs per SM on the current device (occupancy query).
 int fwd_ctas_per_sm();
 cudaError_t launch_reduce(const float *part, int G, int C, int width, float *dweight, float *dbias,
