@@ -450,15 +450,17 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
 // the bias) into dweight[c][k] and dbias[c].  A CTA owns one k and 128
 // consecutive channels, 4 per lane (16-byte loads); its warp w (of
 // m = min(8, G)) sums the contiguous block of rows [w*G/m, (w+1)*G/m) in row
-// order -- the rows are loaded kRedBatch at a time before they are added, so
-// a warp waits for one round trip per batch, not per row -- and warp 0 adds
-// the m block sums in block order.  The order of every addition depends
+// order (the first row, then each next one added) -- the rows are loaded
+// kRedBatch at a time before they are added, so a warp waits for one round
+// trip per batch, not per row, and a block of up to kRedBatch rows (every
+// block while G <= 128) for one -- and warp 0 adds the m block sums in block
+// order.  The order of every addition depends
 // only on G and C, so the result is the same bit for bit on every run.  The
 // partials are written by the backward grid, which may still be running when
 // this grid becomes resident (programmatic dependent launch): they are read
 // after griddepcontrol.wait, with L2-coherent loads.
 constexpr int kRedChannels = 128;  // channels per CTA (4 per lane)
-constexpr int kRedBatch = 8;       // rows loaded before they are added
+constexpr int kRedBatch = 16;      // rows loaded before they are added
 
 __device__ __forceinline__ float4 f4_add(float4 a, float4 b) {
     return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
@@ -480,9 +482,15 @@ __global__ void __launch_bounds__(256) reduce_kernel(const float *part, int G, i
         const int g1 = static_cast<int>(static_cast<int64_t>(warp + 1) * G / m);
         const int64_t step = static_cast<int64_t>(5) * C / 4;  // one partial row, in float4
         const float4 *p = reinterpret_cast<const float4 *>(part + static_cast<int64_t>(k) * C + c);
-        float4 s = __ldcg(p + g0 * step);
-        for (int g = g0 + 1; g < g1; g += kRedBatch) {
-            float4 v[kRedBatch];
+        float4 v[kRedBatch];
+#pragma unroll
+        for (int u = 0; u < kRedBatch; ++u)  // the first batch (g0 < g1: m <= G)
+            v[u] = g0 + u < g1 ? __ldcg(p + (g0 + u) * step) : make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 s = v[0];
+#pragma unroll
+        for (int u = 1; u < kRedBatch; ++u)
+            if (g0 + u < g1) s = f4_add(s, v[u]);
+        for (int g = g0 + kRedBatch; g < g1; g += kRedBatch) {
 #pragma unroll
             for (int u = 0; u < kRedBatch; ++u)
                 v[u] = g + u < g1 ? __ldcg(p + (g + u) * step) : make_float4(0.f, 0.f, 0.f, 0.f);
