@@ -1,4 +1,4 @@
-// ccc_bwd.cu -- fused backward: dx, d_init_state and per-CTA FP32
+// ccc_bwd.cu -- fused backward: dx, d_init_state and per-warp-task FP32
 // dweight/dbias partials in one pass, then an ordered reduction.
 //
 // FlashInfer "cake_causal_conv1d_train.cake_causal_conv1d_kcp" (Returns): one
@@ -22,9 +22,8 @@
 //
 // Mapping.  As in the forward: a warp owns a 32*VEC-channel slab, a lane
 // owns VEC channels, and each warp walks a run of rows (an equal share of
-// the valid rows, RunWalker).  Along one sequence the lane walks i = o0,
-// o0+1, ...
-// without a break: it keeps a sliding window of 3 history rows and the 3
+// the valid rows' cost, RunWalker).  Along one sequence the lane walks
+// i = o0, o0+1, ... without a break: it keeps a sliding window of 3 history rows and the 3
 // previous dz values in registers, emits dx for row i-3 once dz_i is known,
 // and accumulates dz_j * h[j+k] and dz_j of its own rows into 5*VEC FP32
 // registers.  Only where a walk starts inside a sequence does it re-read the
@@ -134,8 +133,9 @@ __global__ void __launch_bounds__(kCtaThreads, kBwdMinBlocks) bwd_kernel(const B
         gb[v] = f2_zero();
     }
 
-    // This warp's run: a fixed share of the rows (the same for every slab),
-    // so the operand order of every partial sum is fixed.
+    // This warp's run: a fixed share of the batch's cost (its rows plus a
+    // fixed cost per sequence; the same for every slab), so the operand
+    // order of every partial sum is fixed.
     RunWalker<kBwdChunk> walk;
     walk.init(a.cu, a.N, a.rows, run, a.runs, H, true, lane, kBwdWalkRows, staged ? meta.cu : nullptr);
 

@@ -391,3 +391,26 @@ def test_unaligned_taps(cuda_device, width, w_dtype, b_dtype, which):
     b = _offset_view(wl.bias) if which in ("bias", "both") and wl.bias is not None else wl.bias
     wl = dataclasses.replace(wl, weight=w, bias=b)
     check(wl, H.run_gpu(wl))
+
+
+# ------------------------------------- backward CTA size at its threshold --
+# The backward runs its tasks (slabs x runs) as one-warp CTAs when they would
+# give every SM at most 7, else as 8-warp CTAs.  Both sides of that switch,
+# at C = 256 (1 slab) and 512 (2 slabs), against the oracle on every channel.
+
+@pytest.mark.parametrize("slabs", [1, 2])
+@pytest.mark.parametrize("side", [0, 1])
+def test_backward_cta_size_threshold(cuda_device, slabs, side):
+    sms = torch.cuda.get_device_properties(cuda_device).multi_processor_count
+    runs = 7 * sms // slabs + side           # tasks = slabs * runs: <= 7 * sms, then just above
+    rows = 16 * runs                          # runs = ceil(rows / 16) (below the width cap)
+    assert runs <= 1216 // slabs
+    rng = np.random.default_rng(runs)
+    lengths = [int(v) for v in rng.integers(1, 400, 200)]
+    while sum(lengths) > rows - 5:
+        lengths.pop()
+    wl = workloads.make_custom(tuple(lengths), 256 * slabs, rows=rows, seed=runs, device=cuda_device,
+                               n_minus_one=3, has_init_p=0.5)
+    g = torch.Generator(device=cuda_device).manual_seed(runs)
+    d_final = torch.randn((wl.n_seqs, 3, wl.C), generator=g, device=cuda_device)
+    check(wl, H.run_gpu(wl, d_final=d_final), d_final=d_final)
