@@ -17,6 +17,11 @@ Entry points (same names as the C ABI):
 * ``ccc_update(...)`` -- speculative / single-token decode step on the pool
 * ``ccc_bwd_noalloc(...)`` -- ``ccc_bwd`` on the library's own scratch
 
+``ccc_fwd``, ``ccc_bwd`` and ``ccc_update`` take ``overlap=True`` to call
+``ccc_fwd_ex`` / ``ccc_bwd_ex`` / ``ccc_update_ex`` with
+``CCC_OPT_OVERLAP_PROLOGUE`` (the kernel's prologue may overlap the kernel
+before it; the contract is in ``include/ccc.h``).
+
 The width W is the second dimension of ``weight`` ([C, W], W in 2..4) and
 ``activation`` is ``"silu"`` (default) or ``None`` (Megatron-Core
 ``core.ssm.causal_conv1d``, causal_conv1d_cp).  On top: the allocating
