@@ -321,10 +321,13 @@ def run_reference(args, ws, rank):
     wl = workloads.packed(device="cpu")
     vals = []
     threads, sample = 0, ""
+    # each step a bounded sample: at most --ref-seconds, and about 150 s for
+    # all K steps together, so the whole run ends within a few minutes
+    target = max(2.0, min(args.ref_seconds, 150.0 / max(1, args.steps)))
     for _ in range(args.warmup):
         time_oracle(wl, target_s=2.0)
     for _ in range(args.steps):
-        v, threads, sample, _ = time_oracle(wl, target_s=args.ref_seconds)
+        v, threads, sample, _ = time_oracle(wl, target_s=target)
         vals.append(v)
     v = statistics.median(vals)
     line = {
