@@ -249,6 +249,7 @@ def capture(call, stream, reps=1):
     `stream` and returns how many kernels they launched) captured as one
     CUDA graph, after one eager call outside the capture; returns the graph
     and the kernel launches one replay makes."""
+    stream.wait_stream(torch.cuda.current_stream())  # inputs made on the default stream
     with torch.cuda.stream(stream):
         call()
     torch.cuda.synchronize()
