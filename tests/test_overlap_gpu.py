@@ -68,6 +68,7 @@ def test_overlap_steps_in_one_graph(cuda_device):
     torch.cuda.synchronize()
     over = _buffers(wl)
     s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
         _step(wl, over, True, stream=s)  # outside the capture first
     torch.cuda.synchronize()
