@@ -343,3 +343,18 @@ def test_one_hot_taps_read_offsets(cuda_device, width):
 
 def H_fill(rows, C, dev):
     return H.fill_sentinel(torch.empty((rows, C), dtype=torch.bfloat16, device=dev))
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_random_decode_chains(cuda_device, seed):
+    """Random prefill + speculative chains: width, activation, pool layout and
+    length, channel count (partial slabs), batch size, draft counts, dtypes."""
+    rng = np.random.default_rng(7000 + seed)
+    width = int(rng.integers(2, 5))
+    L = int(rng.integers(width - 1, 9))
+    _run_chain(cuda_device, width=width, act="silu" if rng.random() < 0.6 else None,
+               layout=["dense", "channel", "padded"][int(rng.integers(0, 3))],
+               C=8 * int(rng.integers(1, 80)), N=int(rng.integers(2, 40)), L=L,
+               kmax=int(rng.integers(1, 6)), steps=4, seed=seed,
+               w_dtype=torch.bfloat16 if rng.random() < 0.5 else torch.float32,
+               b_dtype=[None, torch.float32, torch.bfloat16][int(rng.integers(0, 3))])
