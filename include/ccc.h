@@ -51,8 +51,9 @@
  *    caller-owned constraints: if invalid, the results are undefined, but
  *    the kernels clamp offsets to [0, rows] and skip slot IDs outside
  *    [0, n_slots), so they do not access memory outside the buffers given.
- *  - rows == 0 or N == 0 returns CCC_OK (the backward still zeroes dweight /
- *    dbias).
+ *  - rows == 0 or N == 0 returns CCC_OK with no row read or written (with
+ *    rows == 0 the row buffers x, out, dy and dx may be NULL); the backward
+ *    still zeroes dweight, dbias and d_init_state.
  *  - Concurrent calls on different streams need disjoint live slots, outputs
  *    and workspaces.
  */

@@ -164,7 +164,7 @@ int ccc_fwd_ex(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
         if (!state_layout_ok(n_slots, C, state_len, st_slot, st_c, st_l)) return CCC_ERR_SHAPE;
     }
     // ---- pointers
-    if (!x || !weight || !cu_seqlens || !out) return CCC_ERR_NULL;
+    if (!weight || !cu_seqlens || (rows > 0 && (!x || !out))) return CCC_ERR_NULL;  // x, out: none if no rows
     if (conv_state && !cache_indices) return CCC_ERR_NULL;
     if (!aligned(x, 16) || !aligned(out, 16) || (saved_hist && !aligned(saved_hist, 16))) return CCC_ERR_ALIGN;
     if (!aligned(weight, dtype_size(w_dtype)) || (bias && !aligned(bias, dtype_size(b_dtype)))) return CCC_ERR_ALIGN;
@@ -271,7 +271,7 @@ int ccc_bwd_ex(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
     if (bias ? (b_dtype != CCC_F32 && b_dtype != CCC_BF16) : (b_dtype != CCC_NONE)) return CCC_ERR_DTYPE;
     if (!width_ok(width) || !activation_ok(activation)) return CCC_ERR_SHAPE;
     const int H = width - 1;
-    if (!x || !weight || !cu_seqlens || !dy || !dx || !dweight) return CCC_ERR_NULL;
+    if (!weight || !cu_seqlens || !dweight || (rows > 0 && (!x || !dy || !dx))) return CCC_ERR_NULL;
     if (!aligned(x, 16) || !aligned(dy, 16) || !aligned(dx, 16) || (saved_hist && !aligned(saved_hist, 16)) ||
         (d_final_state && !aligned(d_final_state, 16)) || (d_init_state && !aligned(d_init_state, 16)))
         return CCC_ERR_ALIGN;
@@ -305,10 +305,13 @@ int ccc_bwd_ex(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
 
     g_last_launches = 0;
     cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-    if (rows == 0 || N == 0) {  // no token: the gradients are zero
+    if (rows == 0 || N == 0) {  // no token: the gradients are zero (every sequence is empty)
         if (cudaMemsetAsync(dweight, 0, static_cast<size_t>(C) * width * sizeof(float), st) != cudaSuccess)
             return CCC_ERR_CUDA;
         if (dbias && cudaMemsetAsync(dbias, 0, static_cast<size_t>(C) * sizeof(float), st) != cudaSuccess)
+            return CCC_ERR_CUDA;
+        if (d_init_state && N > 0 &&
+            cudaMemsetAsync(d_init_state, 0, static_cast<size_t>(N) * H * C * sizeof(float), st) != cudaSuccess)
             return CCC_ERR_CUDA;
         return CCC_OK;
     }
@@ -375,7 +378,7 @@ int ccc_update_ex(const void *x, int64_t rows, int32_t C, int64_t x_row_stride,
     if (w_dtype != CCC_F32 && w_dtype != CCC_BF16) return CCC_ERR_DTYPE;
     if (bias ? (b_dtype != CCC_F32 && b_dtype != CCC_BF16) : (b_dtype != CCC_NONE)) return CCC_ERR_DTYPE;
     if (!width_ok(width) || !activation_ok(activation)) return CCC_ERR_SHAPE;
-    if (!x || !weight || !cu_seqlens || !out || !conv_state || !cache_indices) return CCC_ERR_NULL;
+    if (!weight || !cu_seqlens || !conv_state || !cache_indices || (rows > 0 && (!x || !out))) return CCC_ERR_NULL;
     if (state_len < width - 1 || n_slots < 1) return CCC_ERR_SHAPE;
     if (!state_layout_ok(n_slots, C, state_len, st_slot, st_c, st_l)) return CCC_ERR_SHAPE;
     if (!aligned(x, 16) || !aligned(out, 16) || !aligned(conv_state, 2) || !aligned(cu_seqlens, 4) ||

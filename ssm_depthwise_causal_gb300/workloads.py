@@ -87,6 +87,8 @@ def normal_bf16(shape, g: torch.Generator, device, std: float = 1.0,
     """N(0, std^2) drawn in FP32 and rounded to BF16 (RNE), in row chunks so
     that multi-GB tensors never need an FP32 copy of the whole thing."""
     out = torch.empty(shape, dtype=torch.bfloat16, device=device)
+    if out.numel() == 0:  # an empty batch: nothing to draw
+        return out
     flat = out.view(shape[0], -1) if len(shape) > 1 else out.view(-1, 1)
     for r0 in range(0, flat.shape[0], chunk_rows):
         r1 = min(flat.shape[0], r0 + chunk_rows)

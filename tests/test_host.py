@@ -276,3 +276,16 @@ def test_launch_options(lib):
         assert lib.ccc_update_ex(*u, bad, None) == E_SHAPE
     u[1] = 0  # rows == 0: checks pass, nothing launched
     assert lib.ccc_update_ex(*u, _lib.OPT_OVERLAP_PROLOGUE, None) == OK
+
+
+def test_empty_batch_takes_null_row_buffers(lib):
+    """rows == 0: the row buffers may be NULL (an empty tensor has no storage);
+    the forward and the decode step return CCC_OK without any CUDA call, and
+    the pointers that are still required stay required."""
+    assert call_fwd(lib, fwd_args(rows=0, x=None, out=None)) == OK
+    assert call_fwd(lib, fwd_args(rows=0, x=None, out=None, w=None)) == E_NULL
+    assert call_fwd(lib, fwd_args(rows=0, x=None, out=None, cu=None)) == E_NULL
+    assert call_fwd(lib, fwd_args(rows=1, x=None)) == E_NULL
+    assert call_update(lib, rows=0, x=None, out=None) == OK
+    assert call_update(lib, rows=0, x=None, out=None, state=None) == E_NULL
+    assert call_update(lib, rows=1, out=None) == E_NULL

@@ -414,3 +414,31 @@ def test_backward_cta_size_threshold(cuda_device, slabs, side):
     g = torch.Generator(device=cuda_device).manual_seed(runs)
     d_final = torch.randn((wl.n_seqs, 3, wl.C), generator=g, device=cuda_device)
     check(wl, H.run_gpu(wl, d_final=d_final), d_final=d_final)
+
+
+# ------------------------------------------------------- an empty batch --
+# rows == 0 (every sequence empty; the row tensors have no storage): the
+# forward touches nothing, the backward's gradients are all zero -- dweight,
+# dbias and the initial-state gradient of every (empty) sequence.
+
+def test_all_empty_batch(cuda_device):
+    import ssm_depthwise_causal_gb300 as ccc
+    dev, C, N = cuda_device, 264, 3
+    x = torch.empty((0, C), dtype=torch.bfloat16, device=dev)
+    w = torch.randn((C, 4), device=dev)
+    b = torch.randn((C,), device=dev)
+    pool = torch.randn((5, C, 4), device=dev).to(torch.bfloat16)
+    before = pool.clone()
+    cu = torch.zeros(N + 1, dtype=torch.int32, device=dev)
+    cache = torch.tensor([0, -1, 3], dtype=torch.int32, device=dev)
+    hi = torch.ones(N, dtype=torch.uint8, device=dev)
+    hist = torch.full((N, 3, C), float("nan"), device=dev).to(torch.bfloat16)
+    ccc.ccc_fwd(x, w, b, pool, cu, cache, hi, torch.empty_like(x), hist)
+    dw = torch.full((C, 4), float("nan"), device=dev)
+    db = torch.full((C,), float("nan"), device=dev)
+    di = torch.full((N, 3, C), float("nan"), device=dev)
+    ccc.ccc_bwd(x, w, b, hist, cu, cache, hi, torch.empty_like(x), None, torch.empty_like(x), dw, db, di, None)
+    torch.cuda.synchronize()
+    assert torch.equal(pool.view(torch.int16), before.view(torch.int16))
+    assert torch.isnan(hist.float()).all()
+    assert (dw == 0).all() and (db == 0).all() and (di == 0).all()
