@@ -88,3 +88,39 @@ def test_noalloc_largest_scratch_shape(cuda_device):
     want = _grads(wl, hist, noalloc=False)
     got = _grads(wl, hist, noalloc=True)
     _check_same(wl, got, want)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("seed", range(8))
+def test_noalloc_random_batches(cuda_device, seed):
+    # random packed batches (widths 2-4, with and without SiLU, -1 requests,
+    # flags, dtypes; the draw of tests/test_random_batches_gpu.py), each
+    # backward run twice in a row on the shared scratch
+    from tests import test_random_batches_gpu as R
+    lengths, C, rows, width, act, kw = R._case(seed)
+    wl = workloads.make_custom(lengths, C, rows=rows, seed=seed, device=cuda_device, width=width,
+                               activation=act, **kw)
+    hist = torch.zeros((wl.n_seqs, width - 1, C), dtype=torch.bfloat16, device=cuda_device)
+    ccc.ccc_fwd(wl.x, wl.weight, wl.bias, wl.conv_state.clone(), wl.cu_seqlens, wl.cache_indices,
+                wl.has_initial_state, torch.empty_like(wl.x), hist, activation=act)
+    outs = []
+    for noalloc in (False, True, True):
+        dx = torch.zeros_like(wl.x)
+        dw = torch.zeros((C, width), device=cuda_device)
+        db = torch.zeros((C,), device=cuda_device) if wl.bias is not None else None
+        di = torch.zeros((wl.n_seqs, width - 1, C), device=cuda_device)
+        args = (wl.x, wl.weight, wl.bias, hist, wl.cu_seqlens, wl.cache_indices, wl.has_initial_state,
+                wl.dy, None, dx, dw, db, di)
+        if noalloc:
+            ccc.ccc_bwd_noalloc(*args, activation=act)
+        else:
+            ws = torch.empty(ccc.ccc_workspace_size(wl.rows, wl.n_seqs, C, True), dtype=torch.uint8,
+                             device=cuda_device)
+            ccc.ccc_bwd(*args, ws, activation=act)
+        torch.cuda.synchronize()
+        outs.append((dx, dw, db, di))
+    for got in outs[1:]:
+        for g, w in zip(got, outs[0]):
+            if w is not None:
+                assert torch.equal(g.view(torch.int16) if g.dtype == torch.bfloat16 else g.view(torch.int32),
+                                   w.view(torch.int16) if w.dtype == torch.bfloat16 else w.view(torch.int32))
