@@ -33,7 +33,6 @@ history) and the autograd wrapper ``causal_conv1d`` / ``CausalConv1dFn``.
 """
 from __future__ import annotations
 
-import ctypes
 from typing import Optional
 
 import torch
@@ -70,7 +69,9 @@ def last_launch_count() -> int:
 
 
 def _ptr(t: Optional[torch.Tensor]):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # a plain int: the entry points declare their pointers c_void_p, which
+    # takes one directly (cheaper than building a c_void_p per argument)
+    return None if t is None else t.data_ptr()
 
 
 def _dtype_code(t: Optional[torch.Tensor]) -> int:
@@ -105,20 +106,20 @@ def _on_current_device(*tensors) -> None:
     for t in tensors:
         if t is None:
             continue
-        if not t.is_cuda:
+        d = t.get_device()  # -1 for a CPU tensor
+        if d < 0:
             raise ValueError(f"expected CUDA tensors, got one on {t.device}")
         if cur is None:
             cur = torch.cuda.current_device()
-        if t.device.index != cur:
-            raise ValueError(f"a tensor is on cuda:{t.device.index} but the current device is cuda:{cur}; "
-                             f"call inside torch.cuda.device({t.device.index})")
+        if d != cur:
+            raise ValueError(f"a tensor is on cuda:{d} but the current device is cuda:{cur}; "
+                             f"call inside torch.cuda.device({d})")
 
 
-def _stream(stream) -> ctypes.c_void_p:
+def _stream(stream) -> int:
     if stream is None:
         stream = torch.cuda.current_stream()
-    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
-    return ctypes.c_void_p(handle)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
 def _rows_view(t: torch.Tensor, name: str):
