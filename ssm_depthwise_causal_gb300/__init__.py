@@ -116,8 +116,15 @@ def _on_current_device(*tensors) -> None:
                              f"call inside torch.cuda.device({d})")
 
 
+# The current stream's raw handle without building a torch.cuda.Stream
+# object (a few microseconds per call); the public route where absent.
+_raw_current_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream) -> int:
     if stream is None:
+        if _raw_current_stream is not None:
+            return _raw_current_stream(torch.cuda.current_device())
         stream = torch.cuda.current_stream()
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 

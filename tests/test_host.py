@@ -289,3 +289,16 @@ def test_empty_batch_takes_null_row_buffers(lib):
     assert call_update(lib, rows=0, x=None, out=None) == OK
     assert call_update(lib, rows=0, x=None, out=None, state=None) == E_NULL
     assert call_update(lib, rows=1, out=None) == E_NULL
+
+
+@pytest.mark.gpu
+def test_stream_handle_is_the_current_stream(cuda_device):
+    """The binding's stream argument for stream=None is torch's current stream
+    on the current device (also inside a torch.cuda.stream context)."""
+    import torch
+    import ssm_depthwise_causal_gb300 as ccc
+    assert ccc._stream(None) == torch.cuda.current_stream().cuda_stream
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        assert ccc._stream(None) == s.cuda_stream
+    assert ccc._stream(s) == s.cuda_stream
