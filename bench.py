@@ -327,7 +327,7 @@ def run_reference(args, ws, rank):
     # the plan), so the whole run ends within a few minutes
     target = max(2.0, min(args.ref_seconds, 100.0 / max(1, args.steps)))
     for _ in range(args.warmup):
-        time_oracle(wl, target_s=2.0)
+        time_oracle(wl, target_s=min(2.0, target))
     for _ in range(args.steps):
         v, threads, sample, _ = time_oracle(wl, target_s=target)
         vals.append(v)
