@@ -45,12 +45,18 @@ def check(wl_gpu, res, *, chans=None, backward=True, d_final=None):
 
 def report(name, stats):
     """Print how the reduction outputs passed (visible with pytest -s / -rP)
-    and bound the share that passes only through the conditioning floor."""
+    and bound them.  An element passes through the floor only when its sum
+    cancels to below 1 % of the size of its terms (|err| > 1e-4 |ref| and
+    |err| <= 1e-6 sum|terms| imply |ref| < 1e-2 sum|terms|), so how many do
+    is a property of the data -- a few percent for sums of a million random
+    terms; what bounds the arithmetic is the error against the terms' scale,
+    held here to 1e-7 (ten times tighter than the floor)."""
     for what, st in stats.items():
         print(f"[reduction] {name} {what}: {st['n']} elements, {st['floor_only']} within the floor "
               f"1e-6*sum|terms| only, max |err|/|ref| {st['max_rel']:.3g}, "
               f"max |err|/sum|terms| {st['max_err_terms']:.3g}")
-        assert st["floor_only"] <= max(2, st["n"] // 100), f"{name} {what}: too many elements need the floor"
+        assert st["max_err_terms"] <= 1e-7, f"{name} {what}: error above 1e-7 of the terms' scale"
+        assert st["floor_only"] <= max(2, st["n"] // 20), f"{name} {what}: too many elements need the floor"
 
 
 def test_tiny(cuda_device):
@@ -155,9 +161,12 @@ def test_packed_full_and_deterministic(cuda_device):
 
 
 def test_serving_full(cuda_device):
+    """The serving prefill (273 403 rows, C 8192, 256 sequences, pool) on every
+    8th channel and both sides of every slab edge, then the pool rule on
+    every channel."""
     wl = workloads.serving(device=cuda_device)
     before = wl.conv_state.clone()
-    res = _full_size(wl, backward=False)
+    res = _full_size(wl, backward=False, chans=every_kth_channel(wl.C, 8))
     # full-size state properties (every channel)
     cu = wl.cu_seqlens.cpu().tolist()
     ci = wl.cache_indices.cpu().tolist()
@@ -221,8 +230,8 @@ def test_long_context_split_equals_unsplit(cuda_device):
     assert torch.equal(dx_s.view(torch.int16), dx_u.view(torch.int16)), "split dx != unsplit"
     assert torch.equal(pool[0, :, 0:3].view(torch.int16), wl.x[T - 3:T].t().contiguous().view(torch.int16))
     assert torch.all(d_carry == 0), "the first fragment read no state: d_init must be 0"
-    # unsplit vs the oracle on a channel subset
-    chans = spread_channels(C, n=24)
+    # unsplit vs the oracle on every 32nd channel and both sides of every slab edge
+    chans = every_kth_channel(C, 32)
     sub = H.subset(wl, chans)
     ref = H.run_oracle(sub)
     res = H.GpuResult(out=out_u, state=None, hist=H.fill_sentinel(torch.empty((1, 3, C), dtype=torch.bfloat16, device=dev)),
