@@ -1,10 +1,11 @@
 """GPU path (through the C ABI) against the float64 oracle.
 
 Small cases are compared element by element on every channel; the five
-workloads run at full size and are compared on a spread of channels (every
-channel slab boundary the kernels use is included) -- exact for those
-channels, since channels never interact -- plus full-size properties (state
-bits, untouched slots, -1 rows, padding, determinism, split = unsplit).
+workloads run at full size and are compared on every channel (tiny, dense,
+packed) or on every 8th / 32nd channel plus both sides of every slab edge
+(serving, the one-million-token document) -- exact for those channels,
+since channels never interact -- plus full-size properties (state bits,
+untouched slots, -1 rows, padding, determinism, split = unsplit).
 """
 import numpy as np
 import pytest
